@@ -1,0 +1,161 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
+
+This module holds input recipes only - shapes, seeds, context-length laws,
+initial free-list permutations and random values - and none of the method's
+arithmetic: no slot computation, no block tables, no attention, no FP8
+encoding.  Both the CUDA library and the oracle consume what it produces.
+
+The five workloads are decode steps shaped like the pages' LLaMA-7B / 70B
+examples ("LLM inference tutorial" sections 4.1-4.4: 7B = 32 layers x 32 heads
+x 128, 70B = 64 query heads / 8 KV heads x 128; "TGI architecture" section
+3.2: blocks of 128-256 tokens; "nano-vLLM architecture" section 4.3 pool
+formula).  No dataset is involved; these stand in for the pages' ShareGPT-style
+benchmark traffic.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+F32, BF16, FP8 = "f32", "bf16", "fp8_e4m3"
+ELEM_BYTES = {F32: 4, BF16: 2, FP8: 1}
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    kv_dtype: str
+    q_dtype: str
+    seed: int
+    num_layers: int = 1
+    ctx_law: str = "uniform"          # "fixed" | "uniform" | "lognormal"
+    ctx_fixed: tuple = ()
+    ctx_lo: int = 1
+    ctx_hi: int = 1
+    lognormal_median: float = 1024.0
+    lognormal_sigma: float = 1.0
+    pool_slack: float = 1.5
+    fixed_num_blocks: int = 0         # overrides the slack sizing when > 0
+    k_head_scale: tuple = ()          # (lo, hi): K of head g scaled by linspace
+    prefix_tokens: int = 0            # shared prompt prefix (whole blocks)
+    prefix_seqs: int = 0              # sequences 0 .. prefix_seqs-1 share it
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def scale(self) -> float:
+        """Logit scale 1/sqrt(head_dim) as float32 (section 4.4 forward)."""
+        return float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+
+TINY = DecodeWorkload("tiny_fp32_mha", 2, 4, 4, 64, 16, F32, F32, seed=0,
+                      ctx_law="fixed", ctx_fixed=(37, 70), fixed_num_blocks=16)
+LLAMA7B_LAYER = DecodeWorkload("llama7b_layer_bf16", 32, 32, 32, 128, 16, BF16, BF16,
+                               seed=1, ctx_lo=512, ctx_hi=4096)
+LLAMA70B_GQA = DecodeWorkload("llama70b_gqa8_bf16", 64, 64, 8, 128, 128, BF16, BF16,
+                              seed=2, ctx_lo=1024, ctx_hi=8192)
+LONG_CTX = DecodeWorkload("long_ctx_splitkv_bf16", 8, 32, 8, 128, 256, BF16, BF16,
+                          seed=3, ctx_lo=32768, ctx_hi=131072, k_head_scale=(1.0, 4.5))
+RAGGED_FP8 = DecodeWorkload("ragged_32layer_fp8", 256, 32, 32, 128, 16, FP8, BF16,
+                            seed=4, num_layers=32, ctx_law="lognormal", ctx_lo=1,
+                            ctx_hi=16384, pool_slack=1.25, prefix_tokens=2048,
+                            prefix_seqs=128)
+ALL = (TINY, LLAMA7B_LAYER, LLAMA70B_GQA, LONG_CTX, RAGGED_FP8)
+
+
+def rng(seed: int, stream: int = 0) -> np.random.Generator:
+    """PCG64 generator for (workload seed, sub-stream)."""
+    return np.random.default_rng([seed, stream])
+
+
+def context_lens(w: DecodeWorkload) -> np.ndarray:
+    """Context length of each sequence AFTER this step's appended token."""
+    r = rng(w.seed, 1)
+    if w.ctx_law == "fixed":
+        return np.asarray(w.ctx_fixed, dtype=np.int64)
+    if w.ctx_law == "uniform":
+        return r.integers(w.ctx_lo, w.ctx_hi + 1, size=w.num_seqs).astype(np.int64)
+    if w.ctx_law == "lognormal":
+        x = np.exp(r.normal(math.log(w.lognormal_median), w.lognormal_sigma, w.num_seqs))
+        lens = np.clip(np.rint(x), w.ctx_lo, w.ctx_hi).astype(np.int64)
+        if w.prefix_tokens:
+            # sharers: prefix + own suffix (at least 1 token), total <= ctx_hi
+            suf = np.clip(lens[: w.prefix_seqs], 1, w.ctx_hi - w.prefix_tokens)
+            lens[: w.prefix_seqs] = w.prefix_tokens + suf
+        return lens
+    raise ValueError(w.ctx_law)
+
+
+def blocks_needed(w: DecodeWorkload, lens: np.ndarray) -> int:
+    """Physical blocks the workload occupies (prefix blocks counted once).
+
+    Each sequence holds ceil(len / block_size) blocks (at least one), and a
+    sharer's prefix blocks are the owner's.
+    """
+    bs = w.block_size
+    per = np.maximum(1, -(-lens // bs))
+    n = int(per.sum())
+    if w.prefix_tokens:
+        n -= (w.prefix_tokens // bs) * w.prefix_seqs
+        n += w.prefix_tokens // bs          # the owner's copy
+    return n
+
+
+def num_blocks(w: DecodeWorkload, lens: np.ndarray) -> int:
+    if w.fixed_num_blocks:
+        return w.fixed_num_blocks
+    return int(math.ceil(w.pool_slack * blocks_needed(w, lens)))
+
+
+def free_order(w: DecodeWorkload, nblocks: int) -> np.ndarray:
+    """Seeded initial free-list permutation (blocks handed out shuffled)."""
+    return rng(w.seed, 2).permutation(nblocks).astype(np.int32)
+
+
+def normal_f32(seed: int, stream: int, shape) -> np.ndarray:
+    return rng(seed, stream).standard_normal(shape, dtype=np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Store float32 values as bfloat16 (round to nearest even), as uint16 bits.
+
+    This is how synthetic inputs are stored, not a step of the method.
+    """
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    r = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    r = r.astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+def store(x_f32: np.ndarray, dtype: str) -> np.ndarray:
+    """Synthetic float32 values in the storage type of q / k_new / v_new."""
+    if dtype == F32:
+        return np.asarray(x_f32, dtype=np.float32)
+    if dtype == BF16:
+        return f32_to_bf16_bits(x_f32)
+    raise ValueError(dtype)
+
+
+def k_head_scales(w: DecodeWorkload) -> np.ndarray:
+    """Per-KV-head multiplier of K (long-context logits spanning about +-20)."""
+    if not w.k_head_scale:
+        return np.ones(w.num_kv_heads, dtype=np.float32)
+    lo, hi = w.k_head_scale
+    return np.linspace(lo, hi, w.num_kv_heads).astype(np.float32)
+
+
+def fp8_scale_from_absmax(absmax: np.ndarray) -> np.ndarray:
+    """Static per-head FP8 scale absmax / 448 (symmetric rule, qmax = 448)."""
+    a = np.asarray(absmax, dtype=np.float32)
+    return np.where(a > 0, a / np.float32(448.0), np.float32(1.0)).astype(np.float32)
