@@ -1,0 +1,631 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode-attention hot path on one GB300 (or N replicas).
+
+One step = one decode step of the workload: append the new token's K/V of every
+sequence into the paged cache (reshape_and_cache) and attend with one query
+token per sequence over its whole paged context (paged_attention_decode, with
+its split-KV reduce when launched), for every layer of the workload.
+
+Default workload: one LLaMA-7B-shaped layer (32 sequences, 32 query = 32 KV
+heads, head_dim 128, bf16 KV, block_size 16, contexts uniform in [512, 4096],
+shuffled physical blocks).  Metric: effective KV GB/s (K and V bytes the step
+attends over / step time), plus decode tokens/s and attention us per layer.
+
+Arms:
+  (default)          the CUDA library through its C ABI, inputs resident in HBM;
+  --impl reference   the plain CPU oracle on this host's cores, on a bounded
+                     sample of the same workload.
+With torchrun (N>1) every rank runs its own replica ("replicas only": the
+decode step needs no exchange between GPUs) and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+if "--impl" in sys.argv and "reference" in sys.argv:
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
+WORKLOADS = {w.name: w for w in W.ALL}
+DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
+
+# DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
+# valid only while the kernel sources hash to `sources_sha`.
+NCU_TRAFFIC = {}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--partition", type=int, default=0, help="split-KV tokens (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="e2e steps (0 = min(steps, 200))")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def kernel_sources_sha() -> str:
+    """Hash of the CUDA sources, to tie an ncu traffic figure to one kernel version."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_295_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ---
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- distributed ---
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar (the slowest rank sets the job time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------- byte accounting ---
+def row_bytes(w) -> int:
+    """K (or V) bytes of one token of one layer: num_kv_heads * head_dim * elem."""
+    return w.num_kv_heads * w.head_dim * W.ELEM_BYTES[w.kv_dtype]
+
+
+def kv_bytes_logical(w, lens) -> int:
+    """K+V bytes every sequence attends over (a shared prefix counted per reader)."""
+    return int(np.sum(lens)) * 2 * row_bytes(w)
+
+
+def kv_bytes_unique(w, lens) -> int:
+    """K+V bytes of distinct cache rows read (a shared prefix counted once)."""
+    shared = max(0, w.prefix_seqs - 1) * w.prefix_tokens if w.prefix_tokens else 0
+    return (int(np.sum(lens)) - shared) * 2 * row_bytes(w)
+
+
+def attention_alg_bytes(w, lens) -> int:
+    """Algorithmic bytes of one attention launch (one layer): unique K/V rows,
+    q, the float32 output, the block-table entries read and the lengths."""
+    S, hq, d = w.num_seqs, w.num_q_heads, w.head_dim
+    qb = 4 if w.q_dtype == "f32" else 2
+    tables = int(np.sum(-(-np.asarray(lens) // w.block_size))) * 4
+    return kv_bytes_unique(w, lens) + S * hq * d * (qb + 4) + tables + S * 4
+
+
+def append_alg_bytes(w) -> int:
+    """Bytes of one append launch: the new rows read (source type) and written."""
+    src = 2 if w.kv_dtype in ("bf16", "fp8_e4m3") else 4
+    return w.num_seqs * 2 * w.num_kv_heads * w.head_dim * (src + W.ELEM_BYTES[w.kv_dtype]) + \
+        w.num_seqs * 8
+
+
+# --------------------------------------------------- device-side workload ---
+class DeviceStep:
+    """A decode step of workload ``w`` resident on one GPU, run through the C ABI."""
+
+    def __init__(self, w, device, partition=0, nsets=2):
+        import torch
+        import paged_kv_cache_295_gb300 as pkv
+        from paged_kv_cache_295_gb300.engine import PagedKVCache, build_prompts
+        self.w, self.device, self.partition = w, device, partition
+        S, hq, hkv, d, bs = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+        code = {"f32": pkv.F32, "bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3}[w.kv_dtype]
+        self.lens = W.context_lens(w)
+        nb = W.num_blocks(w, self.lens)
+        self.eng = eng = PagedKVCache(w.num_layers, hkv, d, bs, nb, code, device=device,
+                                      initial_free_order=W.free_order(w, nb))
+        _, slots, oslots = build_prompts(eng.pool, self.lens, w.prefix_tokens, w.prefix_seqs)
+        prompt = np.concatenate(([oslots] if oslots is not None else []) + list(slots))
+        step_slots = eng.pool.append_slots(range(S))
+        mb = int(max(len(eng.pool.block_table(s)) for s in range(S)))
+        tables, lens_pool = eng.pool.batch_tables(list(range(S)), mb)
+        assert np.array_equal(lens_pool, self.lens)
+        self.max_ctx = int(self.lens.max())
+        self.tables_h, self.step_slots_h = tables, step_slots
+        self.tables = torch.from_numpy(tables).to(device)
+        self.ctx = torch.from_numpy(self.lens.astype(np.int32)).to(device)
+        self.slots = torch.from_numpy(step_slots).to(device)
+        self.src_dt = torch.float32 if w.kv_dtype == "f32" else torch.bfloat16
+        self.q_dt = torch.float32 if w.q_dtype == "f32" else torch.bfloat16
+        kh = torch.from_numpy(W.k_head_scales(w)).to(device)[None, :, None]
+        prompt_d = torch.from_numpy(prompt).to(device)
+        gen = torch.Generator(device=device)
+        self.q, self.kn, self.vn = [], [], []
+        for layer in range(w.num_layers):
+            gen.manual_seed(w.seed * 1000 + layer)
+            ks, vs = self._randn_rows(gen, prompt.size, kh), self._randn_rows(gen, prompt.size, None)
+            q = [torch.randn((S, hq, d), generator=gen, device=device).to(self.q_dt)
+                 for _ in range(nsets)]
+            kn = [(torch.randn((S, hkv, d), generator=gen, device=device) * kh).to(self.src_dt)
+                  for _ in range(nsets)]
+            vn = [torch.randn((S, hkv, d), generator=gen, device=device).to(self.src_dt)
+                  for _ in range(nsets)]
+            if code == pkv.FP8_E4M3:
+                # static per-head scale absmax / 448 over the layer's data
+                ka = torch.maximum(ks.float().abs().amax((0, 2)), torch.stack(kn).float().abs().amax((0, 1, 3)))
+                va = torch.maximum(vs.float().abs().amax((0, 2)), torch.stack(vn).float().abs().amax((0, 1, 3)))
+                eng.k_scale[layer] = torch.where(ka > 0, ka / 448.0, torch.ones_like(ka))
+                eng.v_scale[layer] = torch.where(va > 0, va / 448.0, torch.ones_like(va))
+            if prompt.size:
+                eng.append(layer, ks, vs, prompt_d)
+            del ks, vs
+            self.q.append(q)
+            self.kn.append(kn)
+            self.vn.append(vn)
+        self.out = torch.empty((S, hq, d), dtype=torch.float32, device=device)
+        self.ws = eng.workspace_for(S, hq, self.max_ctx, partition, device=device)
+        self.P = pkv.partition_tokens(S, hkv, self.max_ctx, partition)
+        self.max_parts = max(1, -(-self.max_ctx // self.P))
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def _randn_rows(self, gen, n, kh, chunk=1 << 18):
+        import torch
+        w = self.w
+        out = torch.empty((n, w.num_kv_heads, w.head_dim), dtype=self.src_dt, device=self.device)
+        for a in range(0, n, chunk):
+            b = min(n, a + chunk)
+            x = torch.randn((b - a, w.num_kv_heads, w.head_dim), generator=gen, device=self.device)
+            out[a:b] = (x * kh if kh is not None else x).to(self.src_dt)
+        return out
+
+    def launches_per_step(self) -> int:
+        """Our kernels per step: per layer one append, one decode, one reduce if split."""
+        return self.w.num_layers * (2 + (1 if self.max_parts > 1 else 0))
+
+    def run(self, i, ev=None):
+        """One decode step (every layer); ``ev`` = (start, end) event lists per layer."""
+        eng, k = self.eng, i % len(self.q[0])
+        for layer in range(self.w.num_layers):
+            eng.append(layer, self.kn[layer][k], self.vn[layer][k], self.slots,
+                       device_status=self.status)
+            if ev is not None:
+                ev[0][layer].record()
+            eng.attend(layer, self.q[layer][k], self.tables, self.ctx, self.max_ctx, out=self.out,
+                       workspace=self.ws, partition=self.partition, device_status=self.status)
+            if ev is not None:
+                ev[1][layer].record()
+
+
+# ------------------------------------------------- in-run HBM references ---
+def in_run_bandwidth(device, nbytes=4 << 30, reps=10):
+    """GB/s of the library's copy kernel (2N bytes) and read kernel (N bytes)."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    a = torch.empty(nbytes // 2, dtype=torch.uint8, device=device)
+    b = torch.empty_like(a)
+    a.fill_(1)
+    r = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    r.fill_(2)
+    sink = torch.empty(pkv.read_kernel_sink_floats(), dtype=torch.float32, device=device)
+    res = {}
+    for name, fn, moved in (("copy_gbs", lambda: pkv.copy_kernel(a, b), 2 * a.numel()),
+                            ("read_gbs", lambda: pkv.read_kernel(r, sink), r.numel())):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        res[name] = moved / min(ts) / 1e9
+    del a, b, r
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------- our arm ---
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be >= 3")
+    bw = in_run_bandwidth(dev)
+    st = DeviceStep(w, dev, partition=args.partition)
+    L = w.num_layers
+    for i in range(Wm):
+        st.run(i)
+    torch.cuda.synchronize(dev)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(2)]
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        st.run(i, ev[i])
+    t1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    dt_local = t0.elapsed_time(t1) * 1e-3
+    dt = max_over_ranks(dt_local, world, dev)
+    attn_s = [ev[i][0][l].elapsed_time(ev[i][1][l]) * 1e-3 for i in range(K) for l in range(L)]
+    status = int(st.status.item())
+
+    kv_log = kv_bytes_logical(w, st.lens) * L
+    kv_uni = kv_bytes_unique(w, st.lens) * L
+    total_kv = sum_over_ranks(kv_log * K, world, dev)
+    value = total_kv / dt / 1e9
+    attn_bytes = attention_alg_bytes(w, st.lens)
+    attn_avg = statistics.fmean(attn_s)
+    peak, peak_src = measured_peaks()
+    achieved = attn_bytes / attn_avg / 1e9
+    sha = kernel_sources_sha()
+    traffic = NCU_TRAFFIC.get("bytes_per_launch") if NCU_TRAFFIC.get("sources_sha") == sha else None
+
+    e2e = run_e2e(st, args, dev, world)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(w, st.lens, st.eng.num_blocks),
+        "launch": {"partition_tokens": st.P, "max_partitions": st.max_parts,
+                   "parallelism": f"replicas x{world}"},
+        "kv_gb_per_step": {"logical": kv_log / 1e9, "unique": kv_uni / 1e9},
+        "value_unique_gbs": round(sum_over_ranks(kv_uni * K, world, dev) / dt / 1e9, 2),
+        "decode_tokens_per_s": round(world * w.num_seqs * K / dt, 1),
+        "attention_us_per_layer": round(attn_avg * 1e6, 3),
+        "append_plus_attention_us_per_layer": round(dt_local / K / L * 1e6, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6800 GB/s",
+                     "kernel": "paged_decode_kernel" + (" + paged_decode_reduce_kernel"
+                                                        if st.max_parts > 1 else ""),
+                     "alg_bytes_per_launch": attn_bytes,
+                     "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4),
+                     "frac_of_in_run_read": round(achieved / bw["read_gbs"], 4)},
+        "in_run_bandwidth_gbs": {k: round(v, 1) for k, v in bw.items()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * st.launches_per_step(),
+        "clocks": clk,
+        "device_status": status,
+        "kernel_sources_sha": sha,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(st, args, dev, world):
+    """The same step through the public API from pinned host buffers each step:
+    host block tables from the pool, H2D of q / new K,V / slots / tables /
+    lengths, append + attention for every layer, D2H of the output, sync."""
+    import torch
+    w = st.w
+    n = args.e2e_steps or min(args.steps, 200)
+    L, S = w.num_layers, w.num_seqs
+    mb = st.tables_h.shape[1]
+    pin = dict(pin_memory=True)
+    q_h = [[x.cpu().pin_memory() for x in st.q[l]] for l in range(L)]
+    kn_h = [[x.cpu().pin_memory() for x in st.kn[l]] for l in range(L)]
+    vn_h = [[x.cpu().pin_memory() for x in st.vn[l]] for l in range(L)]
+    slots_h = torch.from_numpy(st.step_slots_h.copy()).pin_memory()
+    tables_h = torch.empty((S, mb), dtype=torch.int32, **pin)
+    lens_h = torch.empty((S,), dtype=torch.int32, **pin)
+    out_h = torch.empty((S, w.num_q_heads, w.head_dim), dtype=torch.float32, **pin)
+    q_d = [torch.empty_like(st.q[l][0]) for l in range(L)]
+    kn_d = [torch.empty_like(st.kn[l][0]) for l in range(L)]
+    vn_d = [torch.empty_like(st.vn[l][0]) for l in range(L)]
+    slots_d, tables_d, lens_d = (torch.empty_like(st.slots), torch.empty_like(st.tables),
+                                 torch.empty_like(st.ctx))
+    bi = (sum(x[0].numel() * x[0].element_size() for x in q_h + kn_h + vn_h)
+          + slots_h.numel() * 8 + tables_h.numel() * 4 + lens_h.numel() * 4)
+    bo = out_h.numel() * 4
+    seqs = list(range(S))
+    stream = torch.cuda.current_stream(dev)
+
+    def one(i):
+        k = i % len(q_h[0])
+        st.eng.pool.batch_tables(seqs, mb, tables_h.numpy(), lens_h.numpy())
+        slots_d.copy_(slots_h, non_blocking=True)
+        tables_d.copy_(tables_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        for l in range(L):
+            q_d[l].copy_(q_h[l][k], non_blocking=True)
+            kn_d[l].copy_(kn_h[l][k], non_blocking=True)
+            vn_d[l].copy_(vn_h[l][k], non_blocking=True)
+            st.eng.append(l, kn_d[l], vn_d[l], slots_d)
+            st.eng.attend(l, q_d[l], tables_d, lens_d, st.max_ctx, out=st.out, workspace=st.ws,
+                          partition=st.partition)
+        out_h.copy_(st.out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        one(i)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for i in range(n):
+        one(i)
+    dt = max_over_ranks(time.perf_counter() - t, world, dev)
+    kv = sum_over_ranks(kv_bytes_logical(w, st.lens) * L * n, world, dev)
+    return {"value": round(kv / dt / 1e9, 2), "unit": "GB/s", "steps": n,
+            "ms_per_step": round(dt / n * 1e3, 5),
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "decode_tokens_per_s": round(world * S * n / dt, 1),
+            "timer": "host wall clock, one stream sync per step"}
+
+
+# ------------------------------------------------- reference arm (oracle) ---
+def workload_config(w, lens, nb):
+    """The workload description both arms report (no launch details)."""
+    return {
+        "workload": w.name, "num_layers": w.num_layers, "num_seqs": w.num_seqs,
+        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+        "q_dtype": w.q_dtype, "out_dtype": "f32",
+        "context_lens": (f"{w.ctx_law}[{w.ctx_lo},{w.ctx_hi}] seed {w.seed}"
+                         if w.ctx_law != "fixed" else str(list(w.ctx_fixed))),
+        "prefix": (f"{w.prefix_tokens} tokens shared by {w.prefix_seqs} sequences"
+                   if w.prefix_tokens else None),
+        "sum_ctx": int(np.sum(lens)), "max_ctx": int(np.max(lens)), "num_blocks": int(nb),
+        "l2": f"inputs larger than L2: {kv_bytes_unique(w, lens) * w.num_layers / 1e9:.3f} GB "
+              "of K/V read per step vs 129 MB L2",
+    }
+
+
+class OracleStep:
+    """Layer 0 of the workload on the host for the oracle: one sequence per step."""
+
+    def __init__(self, w, seqs):
+        import torch
+        from oracle import pool as OP
+        from paged_kv_cache_295_gb300.engine import build_prompts
+
+        class OraclePool:   # the oracle pool behind the C pool wrapper's call names
+            def __init__(self, *a, **k):
+                self.p = OP.Pool(*a, **k)
+
+            def seq_create(self, s):
+                self.p.seq_create(s)
+
+            def seq_fork_prefix(self, d, s, n):
+                self.p.seq_fork_prefix(d, s, n)
+
+            def append_tokens(self, s, n):
+                return np.asarray(self.p.seq_append_tokens(s, n), dtype=np.int64)
+
+            def append_slots(self, sids):
+                return np.asarray(self.p.seq_append_slots(list(sids)), dtype=np.int64)
+
+        self.w = w
+        S, hkv, d, bs = w.num_seqs, w.num_kv_heads, w.head_dim, w.block_size
+        self.lens = W.context_lens(w)
+        self.nb = W.num_blocks(w, self.lens)
+        op = OraclePool(w.num_layers, hkv, d, bs, W.ELEM_BYTES[w.kv_dtype], self.nb,
+                        initial_free_order=W.free_order(w, self.nb).tolist())
+        build_prompts(op, self.lens, w.prefix_tokens, w.prefix_seqs)
+        op.append_slots(range(S))
+        mb = max(len(op.p.tables[s]) for s in range(S))
+        self.tables = np.asarray(op.p.padded_tables(list(range(S)), mb)[0], dtype=np.int64)
+        dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}[w.kv_dtype]
+        self.kc = np.zeros((self.nb, bs, hkv, d), dtype=dt)
+        self.vc = np.zeros_like(self.kc)
+        r = W.rng(w.seed, 900)
+        self.k_scale = np.full(hkv, 4.5 / 448, np.float32)
+        self.v_scale = np.full(hkv, 4.5 / 448, np.float32)
+        kh = W.k_head_scales(w)[None, None, :, None]
+        done = set()
+        for s in seqs:
+            for b in self.tables[s][: -(-int(self.lens[s]) // bs)]:
+                if b in done:
+                    continue
+                done.add(int(b))
+                for cache, sc in ((self.kc, self.k_scale), (self.vc, self.v_scale)):
+                    x = r.standard_normal((1, bs, hkv, d), dtype=np.float32)
+                    if cache is self.kc:
+                        x = x * kh
+                    if w.kv_dtype == "fp8_e4m3":   # input generation via torch's float8 cast
+                        y = np.clip(x / sc[None, None, :, None], -448, 448).astype(np.float32)
+                        cache[b] = torch.from_numpy(y[0]).to(torch.float8_e4m3fn).view(
+                            torch.uint8).numpy()
+                    else:
+                        cache[b] = W.store(x[0], w.kv_dtype)
+        self.q = W.store(r.standard_normal((S, w.num_q_heads, d), dtype=np.float32), w.q_dtype)
+
+    def run(self, s):
+        from oracle import attention as OA
+        w = self.w
+        OA.paged_attention_decode(self.q, self.kc, self.vc, self.tables, self.lens, w.scale,
+                                  w.q_dtype, w.kv_dtype, self.k_scale, self.v_scale, seqs=[s])
+        return int(self.lens[s]) * 2 * row_bytes(w)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    order = [i % w.num_seqs for i in range(Wm + K)]
+    st = OracleStep(w, sorted(set(order)))
+    for i in range(Wm):
+        st.run(order[i])
+    byts, t = 0, time.perf_counter()
+    for i in range(K):
+        byts += st.run(order[Wm + i])
+    dt = time.perf_counter() - t
+    value = byts / dt / 1e9
+    sample = (f"layer 0, one sequence per step in order 0..{w.num_seqs - 1} (repeating), "
+              f"{K} steps, numpy float64 oracle, 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, st.lens, st.nb),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(args):
+    """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
+    w = WORKLOADS[args.workload]
+    lens = W.context_lens(w)
+    per_step = float(np.mean(lens)) * w.num_q_heads * 1.2e-6     # ~1.2 us per token-head
+    steps = int(max(2, min(10 * w.num_seqs, args.cpu_seconds / per_step)))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           w.name, "--steps", str(steps), "--warmup", "1"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+        cb = line["cpu_baseline"]
+        cb["cpu_model"] = _cpu_model()
+        return cb
+    except Exception as e:   # the baseline is reported, never the target
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {type(e).__name__}: {e}"[:200]}
+
+
+def _cpu_model():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * pagedkv.h - C ABI of libpagedkv: a paged KV cache and PagedAttention decode
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages on LLM inference):
+ *   [TUT]  "LLM inference tutorial" (xurj.top Tutorial/Detail/167)
+ *          section 4.1 KVCache, 4.2 PagedAttention (class PagedKVCache),
+ *          4.3 Prefix Caching (class PrefixCacheManager), 4.4 MHA/GQA/MQA,
+ *          3.1 symmetric quantisation.
+ *   [NANO] "nano-vLLM architecture" (intelliparadigm 2014318), section 4.2
+ *          PagedAttention (logical -> physical block mapping, attention that
+ *          reads through the mapping) and 4.3 memory-pool formula.
+ *   [TGI]  "TGI architecture" (intelliparadigm 2004249), section 3.2 paged
+ *          blocks of 128-256 tokens shared between requests.
+ *   [TOPG] "ToPG framework" (intelliparadigm 2232463), section 3.3: the KV
+ *          cache stored compressed as FP8.
+ *
+ * Conventions for every call:
+ *   - Host functions never abort; they return a pkv_status.
+ *   - Device functions are asynchronous on the caller's stream: they validate
+ *     their arguments on the host, launch, and return.  They never allocate,
+ *     never synchronise, and report launch failures as PKV_ERR_CUDA.  Errors
+ *     found on the device (a block id or slot out of range, a context longer
+ *     than the block table) skip the offending access and OR a bit into the
+ *     optional caller-owned device word `device_status` (PKV_DEV_* below).
+ *   - All device buffers are owned by the caller and passed as device
+ *     pointers; host buffers are owned by the caller and passed as host
+ *     pointers.
+ *   - A pool handle is not thread-safe: the caller serialises calls on it.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,    /* null pointer, bad size, unknown sequence ... */
+  PKV_ERR_NO_FREE_BLOCK = 2,  /* free list cannot cover the request [TUT 4.2] */
+  PKV_ERR_BAD_BLOCK = 3,      /* block id outside [0, num_blocks) */
+  PKV_ERR_REFCOUNT = 4,       /* ref or free of a block whose count is 0 */
+  PKV_ERR_UNSUPPORTED = 5,    /* head_dim / block_size / dtype / group not built */
+  PKV_ERR_CUDA = 6,           /* a CUDA runtime call or launch failed */
+  PKV_ERR_HOST_MEMORY = 7     /* host allocation failed */
+} pkv_status;
+
+/* Bits a kernel ORs into *device_status (when that pointer is non-null). */
+#define PKV_DEV_BAD_BLOCK 0x1     /* a block-table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_SLOT 0x2      /* a slot >= num_blocks * block_size */
+#define PKV_DEV_BAD_CONTEXT 0x4   /* context_lens[s] < 0 or > max_blocks_per_seq * block_size */
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Human-readable name of a status (static string). */
+const char* pkv_status_string(int32_t status);
+
+/* ------------------------------------------------------------------------ */
+/* Host block pool [TUT 4.2, 4.3; NANO 4.3].                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t num_layers;      /* layers sharing one block id (one view per layer) */
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;      /* tokens per block, > 0 */
+  int32_t kv_dtype;        /* pkv_dtype of the cache elements */
+  int64_t num_blocks;      /* physical blocks; 0 => free_bytes / block_bytes */
+  int64_t free_bytes;      /* memory for the pool when num_blocks == 0 */
+  /* Optional permutation of 0..num_blocks-1: the initial free-list order
+   * (NULL => 0, 1, 2, ...).  Copied at init; not retained. */
+  const int32_t* initial_free_order;
+} pkv_pool_config;
+
+typedef struct {
+  int64_t total_blocks;
+  int64_t used_blocks;     /* total - free */
+  int64_t free_blocks;
+  double utilization;      /* used / total * 100 [TUT 4.2 memory_usage] */
+  int64_t block_bytes;     /* pkv_block_bytes() of the pool's config */
+  int64_t total_bytes;     /* total_blocks * block_bytes */
+  int64_t used_bytes;      /* used_blocks * block_bytes */
+} pkv_pool_stats;
+
+typedef struct pkv_pool pkv_pool;
+
+/* Bytes of one physical block over all layers, K and V:
+ * 2 * num_layers * block_size * num_kv_heads * head_dim * dtype_size
+ * [NANO 4.3].  Returns -1 if cfg is NULL or a field is not positive. */
+int64_t pkv_block_bytes(const pkv_pool_config* cfg);
+
+/* Create a pool (host metadata only; the caller allocates the device cache,
+ * one [num_blocks, block_size, num_kv_heads, head_dim] view per layer and per
+ * K/V, as the pool tensor of [TUT 4.2]).  With num_blocks == 0 the pool gets
+ * free_bytes / block_bytes blocks [NANO 4.3].  *out receives the handle.
+ * INVALID_ARG for bad fields or a non-permutation free order. */
+pkv_status kv_pool_init(const pkv_pool_config* cfg, pkv_pool** out);
+void kv_pool_destroy(pkv_pool* pool);
+
+/* Take the block at the FRONT of the free list (FIFO, [TUT 4.2] pop(0)) and
+ * set its reference count to 1.  NO_FREE_BLOCK when the list is empty. */
+pkv_status block_alloc(pkv_pool* pool, int32_t* block_id);
+/* Share a block: count += 1 [TUT 4.3].  BAD_BLOCK / REFCOUNT (count 0). */
+pkv_status block_ref(pkv_pool* pool, int32_t block_id);
+/* Drop one reference; at 0 the block goes to the TAIL of the free list
+ * [TUT 4.2 free_sequence].  BAD_BLOCK / REFCOUNT (already free). */
+pkv_status block_free(pkv_pool* pool, int32_t block_id);
+/* Current reference count of a block (0 = free). */
+pkv_status block_refcount(const pkv_pool* pool, int32_t block_id, int32_t* count);
+pkv_status kv_pool_stats(const pkv_pool* pool, pkv_pool_stats* out);
+/* Copy the free list, front first, into out[0 .. cap); *n = its length.
+ * INVALID_ARG if cap < *n (nothing beyond cap is written). */
+pkv_status kv_pool_free_list(const pkv_pool* pool, int32_t* out, int64_t cap, int64_t* n);
+
+/* Sequences.  seq_create takes one block at once and starts at length 0, as
+ * allocate_sequence in [TUT 4.2]; INVALID_ARG if seq_id exists. */
+pkv_status seq_create(pkv_pool* pool, int64_t seq_id);
+/* New sequence dst sharing src's first ntok tokens: ntok must be a positive
+ * multiple of block_size and <= src's length; each shared block gets one more
+ * reference [TUT 4.3].  dst's next token opens a private block, so no shared
+ * block is ever written. */
+pkv_status seq_fork_prefix(pkv_pool* pool, int64_t dst, int64_t src, int32_t ntok);
+/* Append ONE token to each of n distinct sequences.  For the token at
+ * position p: logical block p / block_size, offset p % block_size; a new block
+ * is taken from the free list when that logical block is not in the table;
+ * slot_mapping_out[i] = table[p / block_size] * block_size + p % block_size
+ * [TUT 4.2 append_token].  All-or-nothing: NO_FREE_BLOCK / INVALID_ARG leave
+ * the pool unchanged.  slot_mapping_out is a host array of n int64. */
+pkv_status seq_append_slots(pkv_pool* pool, const int64_t* seq_ids, int32_t n,
+                            int64_t* slot_mapping_out);
+/* Append n tokens to one sequence (a prompt).  Same rule and all-or-nothing
+ * behaviour; slots_out (host, n int64) may be NULL. */
+pkv_status seq_append_tokens(pkv_pool* pool, int64_t seq_id, int32_t n, int64_t* slots_out);
+pkv_status seq_length(const pkv_pool* pool, int64_t seq_id, int32_t* len);
+/* Copy a sequence's block table into out[0 .. cap); *nblocks = its length;
+ * INVALID_ARG if cap < *nblocks. */
+pkv_status seq_block_table(const pkv_pool* pool, int64_t seq_id, int32_t* out, int32_t cap,
+                           int32_t* nblocks);
+/* Batch view for a decode step: tables_out is a host [n, max_blocks] int32
+ * row-major array (rows padded with -1), context_lens_out a host [n] int32
+ * array of current lengths.  INVALID_ARG if a table is longer than
+ * max_blocks. */
+pkv_status seq_batch_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n,
+                            int32_t max_blocks, int32_t* tables_out, int32_t* context_lens_out);
+/* Drop one reference on each block of the table, in table order (blocks that
+ * reach 0 go to the free-list tail), and forget the sequence. */
+pkv_status seq_free(pkv_pool* pool, int64_t seq_id);
+
+/* ------------------------------------------------------------------------ */
+/* Device: cache append [TUT 4.2 append_token, write half; TOPG 3.3].        */
+/* ------------------------------------------------------------------------ */
+
+/* Write the K and V rows of num_tokens new tokens into one layer's cache.
+ *   k_new, v_new  : device [num_tokens, num_kv_heads, head_dim], src_dtype.
+ *   slot_mapping  : device [num_tokens] int64; token i goes to physical block
+ *                   slot / block_size, offset slot % block_size.  A negative
+ *                   slot skips the token; slot >= num_blocks * block_size is
+ *                   skipped and flagged PKV_DEV_BAD_SLOT.
+ *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, head_dim],
+ *                   cache_dtype.
+ *   src_dtype == cache_dtype (f32 or bf16): the row bytes are copied.
+ *   cache_dtype == FP8_E4M3 with src f32 or bf16: each element becomes
+ *     E4M3(round-to-nearest-even, saturate to +-448)(float(x) / k_scale[h])
+ *     with an IEEE float32 division [TUT 3.1 symmetric rule, qmax = 448];
+ *     k_scale / v_scale are device [num_kv_heads] float32.
+ * Requirements: all buffers 16-byte aligned; head_dim * elem_size a multiple of
+ * 16 bytes.  UNSUPPORTED for other dtype pairs. */
+pkv_status reshape_and_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                             void* k_cache, void* v_cache, int32_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int64_t num_blocks, int32_t src_dtype, int32_t cache_dtype,
+                             const float* k_scale, const float* v_scale,
+                             int32_t* device_status, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device: PagedAttention decode [NANO 4.2; TUT 4.2 get_kv + 4.4 forward].   */
+/* ------------------------------------------------------------------------ */
+
+/* Tokens per split-KV partition that paged_attention_decode uses for this
+ * problem when its partition_tokens argument is 0 (depends on the current
+ * device's SM count).  Returns 0 on bad arguments. */
+int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_kv_heads,
+                                         int32_t max_context_len, int32_t partition_tokens);
+
+/* Device scratch that paged_attention_decode needs for its split-KV partials
+ * (0 when every sequence fits one partition): num_seqs * num_q_heads *
+ * ceil(max_context_len / P) * (head_dim + 2) * 4 bytes, P as above. */
+size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t max_context_len, int32_t partition_tokens);
+
+/* One query token per sequence attends over its whole paged context.
+ *   q            : device [num_seqs, num_q_heads, head_dim], q_dtype (f32|bf16).
+ *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, head_dim],
+ *                  kv_dtype (f32|bf16|fp8_e4m3); one layer's views.
+ *   block_tables : device [num_seqs, max_blocks_per_seq] int32, row-major;
+ *                  entry j of row s is the physical block of logical block j.
+ *                  Entries at or beyond ceil(context_lens[s]/block_size) are
+ *                  never read.
+ *   context_lens : device [num_seqs] int32, tokens to attend (including the
+ *                  token appended this step).  0 gives an output of 0.
+ *   max_context_len : host upper bound of context_lens (sizes the grid).
+ *   scale        : logit scale (1/sqrt(head_dim) in [TUT 4.4]).
+ *   k_scale, v_scale : device [num_kv_heads] float32 dequant scales, FP8 only
+ *                  (value = float(e4m3) * scale[kv_head]); else ignored.
+ *   out          : device [num_seqs, num_q_heads, head_dim] float32.
+ *   workspace    : device scratch of workspace_bytes >=
+ *                  paged_attention_workspace_bytes(...) (may be NULL when that
+ *                  is 0); contents need not be initialised.
+ *   partition_tokens : split-KV partition length in tokens (a multiple of 64,
+ *                  or 0 = automatic).
+ * Computes, for every sequence s and query head h with G = num_q_heads /
+ * num_kv_heads and KV head g = h / G [TUT 4.4 repeat_interleave]:
+ *   out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K[s,t,g,:]) * V[s,t,g,:]
+ * over t < context_lens[s], K/V gathered through the block table [TUT 4.2
+ * get_kv], with float32 accumulation and a running (online) softmax.
+ * Supported: head_dim in {64, 128, 256} with head_dim * kv_elem_size in
+ * [64, 512] bytes; G in {1, 2, 4, 8}; block_size a power of two in [1, 4096];
+ * 16-byte aligned buffers.  UNSUPPORTED / INVALID_ARG otherwise. */
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                  int32_t max_blocks_per_seq, int32_t max_context_len,
+                                  float scale, int32_t q_dtype, int32_t kv_dtype,
+                                  const float* k_scale, const float* v_scale, float* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  int32_t partition_tokens, int32_t* device_status,
+                                  pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device: bandwidth reference kernels (the roofline denominators).          */
+/* ------------------------------------------------------------------------ */
+
+/* dst[0 .. bytes) = src[0 .. bytes) with 16-byte vector loads/stores; bytes a
+ * multiple of 16, both pointers 16-byte aligned. */
+pkv_status pkv_copy_kernel(const void* src, void* dst, size_t bytes, pkv_stream_t stream);
+/* Reads src[0 .. bytes) with 16-byte loads and writes one float per CTA of a
+ * checksum into sink (device, >= pkv_read_kernel_sink_floats() floats). */
+pkv_status pkv_read_kernel(const void* src, size_t bytes, float* sink, pkv_stream_t stream);
+int32_t pkv_read_kernel_sink_floats(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,327 @@
+"""Python binding of libpagedkv (paged KV cache + PagedAttention decode, sm_103a).
+
+Argument marshalling only: every step of the path runs in the C++ pool and the
+CUDA kernels of ``libpagedkv.so``; torch provides device memory and the
+current stream.  There is no CPU fallback: if the library is missing or the
+device is not a CUDA GPU, the calls raise.
+
+Names follow the C ABI in ``include/pagedkv.h``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+F32, BF16, FP8_E4M3 = 0, 1, 2
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E4M3: "fp8_e4m3"}
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT = 0x1, 0x2, 0x4
+
+STATUS = {0: "ok", 1: "invalid_arg", 2: "no_free_block", 3: "bad_block", 4: "refcount",
+          5: "unsupported", 6: "cuda", 7: "host_memory"}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class _PoolConfig(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("block_size", C.c_int32),
+                ("kv_dtype", C.c_int32), ("num_blocks", C.c_int64),
+                ("free_bytes", C.c_int64), ("initial_free_order", C.POINTER(C.c_int32))]
+
+
+class _PoolStats(C.Structure):
+    _fields_ = [("total_blocks", C.c_int64), ("used_blocks", C.c_int64),
+                ("free_blocks", C.c_int64), ("utilization", C.c_double),
+                ("block_bytes", C.c_int64), ("total_bytes", C.c_int64),
+                ("used_bytes", C.c_int64)]
+
+
+_lib = None
+P, I32, I64, SZ, FL = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
+_SIGS = {
+    "pkv_status_string": (C.c_char_p, [I32]),
+    "pkv_block_bytes": (I64, [C.POINTER(_PoolConfig)]),
+    "kv_pool_init": (I32, [C.POINTER(_PoolConfig), C.POINTER(P)]),
+    "kv_pool_destroy": (None, [P]),
+    "block_alloc": (I32, [P, C.POINTER(I32)]),
+    "block_ref": (I32, [P, I32]),
+    "block_free": (I32, [P, I32]),
+    "block_refcount": (I32, [P, I32, C.POINTER(I32)]),
+    "kv_pool_stats": (I32, [P, C.POINTER(_PoolStats)]),
+    "kv_pool_free_list": (I32, [P, P, I64, C.POINTER(I64)]),
+    "seq_create": (I32, [P, I64]),
+    "seq_fork_prefix": (I32, [P, I64, I64, I32]),
+    "seq_append_slots": (I32, [P, P, I32, P]),
+    "seq_append_tokens": (I32, [P, I64, I32, P]),
+    "seq_length": (I32, [P, I64, C.POINTER(I32)]),
+    "seq_block_table": (I32, [P, I64, P, I32, C.POINTER(I32)]),
+    "seq_batch_tables": (I32, [P, P, I32, I32, P, P]),
+    "seq_free": (I32, [P, I64]),
+    "reshape_and_cache": (I32, [P, P, P, P, P, I32, I32, I32, I32, I64, I32, I32, P, P, P, P]),
+    "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32]),
+    "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+    "paged_attention_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32, I32, FL,
+                                     I32, I32, P, P, P, P, SZ, I32, P, P]),
+    "pkv_copy_kernel": (I32, [P, P, SZ, P]),
+    "pkv_read_kernel": (I32, [P, SZ, P, P]),
+    "pkv_read_kernel_sink_floats": (I32, []),
+}
+
+
+def library():
+    """Load ``libpagedkv.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpagedkv.so not built at {LIB_PATH}: run "
+                               "paged_kv_cache_295_gb300._build.build_library()")
+        lib = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise PagedKVError(code, where)
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def block_bytes(num_layers, block_size, num_kv_heads, head_dim, kv_dtype=BF16) -> int:
+    cfg = _PoolConfig(num_layers, num_kv_heads, head_dim, block_size, kv_dtype, 0, 0, None)
+    return int(library().pkv_block_bytes(C.byref(cfg)))
+
+
+class Pool:
+    """Host block pool (C++): FIFO free list, refcounts, tables and slots."""
+
+    def __init__(self, num_layers, num_kv_heads, head_dim, block_size, kv_dtype=BF16,
+                 num_blocks=0, free_bytes=0, initial_free_order=None):
+        lib = library()
+        order = None
+        if initial_free_order is not None:
+            self._order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            order = self._order.ctypes.data_as(C.POINTER(C.c_int32))
+        cfg = _PoolConfig(num_layers, num_kv_heads, head_dim, block_size, kv_dtype,
+                          num_blocks, free_bytes, order)
+        h = C.c_void_p()
+        _check(lib.kv_pool_init(C.byref(cfg), C.byref(h)), "kv_pool_init")
+        self._h = h
+        self.block_size = block_size
+        self.num_blocks = self.stats()["total_blocks"]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            library().kv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def block_alloc(self) -> int:
+        b = C.c_int32()
+        _check(library().block_alloc(self._h, C.byref(b)), "block_alloc")
+        return b.value
+
+    def block_ref(self, b: int):
+        _check(library().block_ref(self._h, b), "block_ref")
+
+    def block_free(self, b: int):
+        _check(library().block_free(self._h, b), "block_free")
+
+    def refcount(self, b: int) -> int:
+        c = C.c_int32()
+        _check(library().block_refcount(self._h, b, C.byref(c)), "block_refcount")
+        return c.value
+
+    def stats(self) -> dict:
+        s = _PoolStats()
+        _check(library().kv_pool_stats(self._h, C.byref(s)), "kv_pool_stats")
+        return {f: getattr(s, f) for f, _ in _PoolStats._fields_}
+
+    def free_list(self) -> list:
+        n = C.c_int64()
+        buf = np.empty(self.num_blocks, dtype=np.int32)
+        _check(library().kv_pool_free_list(self._h, _np_ptr(buf), buf.size, C.byref(n)),
+               "kv_pool_free_list")
+        return buf[: n.value].tolist()
+
+    def seq_create(self, sid: int):
+        _check(library().seq_create(self._h, sid), "seq_create")
+
+    def seq_fork_prefix(self, dst: int, src: int, ntok: int):
+        _check(library().seq_fork_prefix(self._h, dst, src, ntok), "seq_fork_prefix")
+
+    def append_slots(self, sids) -> np.ndarray:
+        ids = np.ascontiguousarray(sids, dtype=np.int64)
+        out = np.empty(ids.size, dtype=np.int64)
+        _check(library().seq_append_slots(self._h, _np_ptr(ids), ids.size, _np_ptr(out)),
+               "seq_append_slots")
+        return out
+
+    def append_tokens(self, sid: int, n: int, want_slots: bool = True):
+        out = np.empty(n, dtype=np.int64) if want_slots else None
+        _check(library().seq_append_tokens(self._h, sid, n,
+                                           _np_ptr(out) if want_slots else None),
+               "seq_append_tokens")
+        return out
+
+    def seq_length(self, sid: int) -> int:
+        n = C.c_int32()
+        _check(library().seq_length(self._h, sid, C.byref(n)), "seq_length")
+        return n.value
+
+    def block_table(self, sid: int) -> list:
+        n = C.c_int32()
+        st = library().seq_block_table(self._h, sid, None, 0, C.byref(n))
+        if st not in (0, 1):
+            _check(st, "seq_block_table")
+        buf = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(library().seq_block_table(self._h, sid, _np_ptr(buf), buf.size, C.byref(n)),
+               "seq_block_table")
+        return buf[: n.value].tolist()
+
+    def batch_tables(self, sids, max_blocks: int, tables=None, lens=None):
+        """``[n, max_blocks]`` int32 tables (pad -1) and ``[n]`` int32 lengths.
+
+        ``tables`` / ``lens`` may be caller-owned contiguous int32 arrays (for
+        example views of pinned host tensors) to write into.
+        """
+        ids = np.ascontiguousarray(sids, dtype=np.int64)
+        if tables is None:
+            tables = np.empty((ids.size, max_blocks), dtype=np.int32)
+        if lens is None:
+            lens = np.empty(ids.size, dtype=np.int32)
+        if (tables.dtype != np.int32 or lens.dtype != np.int32 or tables.size < ids.size * max_blocks
+                or lens.size < ids.size or not tables.flags.c_contiguous
+                or not lens.flags.c_contiguous):
+            raise ValueError("tables/lens must be contiguous int32 arrays of the batch's size")
+        _check(library().seq_batch_tables(self._h, _np_ptr(ids), ids.size, max_blocks,
+                                          _np_ptr(tables), _np_ptr(lens)), "seq_batch_tables")
+        return tables, lens
+
+    def seq_free(self, sid: int):
+        _check(library().seq_free(self._h, sid), "seq_free")
+
+
+# ---------------------------------------------------------------------------
+# Device calls (torch tensors in, async on the current stream).
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=None,
+                      v_scale=None, device_status=None, stream=None):
+    """Append token rows ``[T, Hkv, D]`` into one layer's ``[NB, bs, Hkv, D]`` cache."""
+    T, hkv, d = k_new.shape
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    st = library().reshape_and_cache(
+        _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(slot_mapping, "slot_mapping"),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), T, hkv, d, bs, nb,
+        _dtype_code(k_new), _dtype_code(k_cache), _dev(k_scale, "k_scale"),
+        _dev(v_scale, "v_scale"), _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "reshape_and_cache")
+
+
+def partition_tokens(num_seqs, num_kv_heads, max_context_len, requested=0) -> int:
+    return int(library().paged_attention_partition_tokens(num_seqs, num_kv_heads,
+                                                           max_context_len, requested))
+
+
+def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                    partition=0) -> int:
+    return int(library().paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                         head_dim, max_context_len, partition))
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
+                           max_context_len, out=None, k_scale=None, v_scale=None,
+                           workspace=None, partition=0, device_status=None, stream=None):
+    """Decode attention; returns ``out [S, Hq, D]`` float32 (allocated if None).
+
+    ``max_context_len`` is a host int (an upper bound of ``context_lens``).
+    The split-KV workspace is allocated with torch when not given.
+    """
+    torch = _torch()
+    S, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((S, hq, d), dtype=torch.float32, device=q.device)
+    need = workspace_bytes(S, hq, hkv, d, max_context_len, partition)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = library().paged_attention_decode(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), S, hq, hkv, d,
+        bs, nb, mb, int(max_context_len), float(scale), _dtype_code(q), _dtype_code(k_cache),
+        _dev(k_scale, "k_scale"), _dev(v_scale, "v_scale"), _dev(out, "out"),
+        _dev(workspace, "workspace") if workspace is not None else None, ws_bytes,
+        int(partition), _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "paged_attention_decode")
+    return out
+
+
+def copy_kernel(src, dst, stream=None):
+    n = src.numel() * src.element_size()
+    _check(library().pkv_copy_kernel(_dev(src, "src"), _dev(dst, "dst"), n, _stream(stream)),
+           "pkv_copy_kernel")
+
+
+def read_kernel(src, sink, stream=None):
+    n = src.numel() * src.element_size()
+    _check(library().pkv_read_kernel(_dev(src, "src"), n, _dev(sink, "sink"), _stream(stream)),
+           "pkv_read_kernel")
+
+
+def read_kernel_sink_floats() -> int:
+    return int(library().pkv_read_kernel_sink_floats())

@@ -1,0 +1,184 @@
+// Host entry points of the decode path: argument validation, split-KV
+// partition choice, workspace layout and dispatch to the kernel instantiation
+// for (KV type, head_dim, query-group size).
+#include <cmath>
+
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;   // GB300 has 152 SMs; used only when no device answers
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int64_t x) {
+  int r = 0;
+  while ((int64_t{1} << r) < x) ++r;
+  return r;
+}
+
+// Split-KV partition length.  Aim for about 16 work items (CTAs that have
+// tokens) per SM over the longest sequence, so the grid runs many waves and
+// a ragged tail costs little; keep partitions between 256 and 4096 tokens so
+// per-CTA set-up and the partial round trip stay a small share of the bytes.
+int32_t auto_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_ctx) {
+  const double work = static_cast<double>(num_seqs) * num_kv_heads * (max_ctx > 0 ? max_ctx : 1);
+  const double items = 16.0 * device_sm_count();
+  int64_t want = static_cast<int64_t>(work / items);
+  int64_t P = 256;
+  while (P * 2 <= want && P < 4096) P *= 2;
+  return static_cast<int32_t>(P);
+}
+
+int32_t resolve_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_ctx, int32_t req) {
+  if (req < 0 || (req > 0 && req % 64 != 0)) return 0;
+  return req > 0 ? req : auto_partition(num_seqs, num_kv_heads, max_ctx);
+}
+
+int32_t parts_for(int32_t max_ctx, int32_t P) {
+  const int64_t n = (static_cast<int64_t>(max_ctx) + P - 1) / P;
+  return static_cast<int32_t>(n > 0 ? n : 1);
+}
+
+using LaunchFn = pkv_status (*)(const DecodeLaunch&);
+
+template <typename KV, int D>
+LaunchFn pick_group(int G) {
+  switch (G) {
+    case 1: return launch_decode<KV, D, 1>;
+    case 2: return launch_decode<KV, D, 2>;
+    case 4: return launch_decode<KV, D, 4>;
+    case 8: return launch_decode<KV, D, 8>;
+    default: return nullptr;
+  }
+}
+
+LaunchFn pick(int32_t kv_dtype, int D, int G) {
+  switch (kv_dtype) {
+    case PKV_F32:
+      if (D == 64) return pick_group<F32, 64>(G);
+      if (D == 128) return pick_group<F32, 128>(G);
+      return nullptr;
+    case PKV_BF16:
+      if (D == 64) return pick_group<BF16, 64>(G);
+      if (D == 128) return pick_group<BF16, 128>(G);
+      if (D == 256) return pick_group<BF16, 256>(G);
+      return nullptr;
+    case PKV_FP8_E4M3:
+      if (D == 64) return pick_group<FP8, 64>(G);
+      if (D == 128) return pick_group<FP8, 128>(G);
+      if (D == 256) return pick_group<FP8, 256>(G);
+      return nullptr;
+    default:
+      return nullptr;
+  }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_kv_heads,
+                                                    int32_t max_context_len,
+                                                    int32_t partition_tokens) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
+  return pkv::resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+}
+
+extern "C" size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t max_context_len,
+                                                  int32_t partition_tokens) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_context_len < 0)
+    return 0;
+  const int32_t P = pkv::resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+  if (P <= 0) return 0;
+  const int32_t parts = pkv::parts_for(max_context_len, P);
+  if (parts <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+extern "C" pkv_status paged_attention_decode(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
+    const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
+    int32_t partition_tokens, int32_t* device_status, pkv_stream_t stream) {
+  using namespace pkv;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      num_blocks <= 0 || num_blocks > INT32_MAX || max_blocks_per_seq <= 0 || max_context_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!is_pow2(block_size) || block_size > 4096) return PKV_ERR_UNSUPPORTED;
+  if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (partition_tokens < 0 || partition_tokens % 64 != 0) return PKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  LaunchFn fn = pick(kv_dtype, head_dim, G);
+  if (!fn) return PKV_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return PKV_ERR_INVALID_ARG;
+  if (kv_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+
+  const int32_t P = resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+  const int32_t parts = parts_for(max_context_len, P);
+  const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                      head_dim, max_context_len, P);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return PKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(parts) > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+
+  DecodeLaunch a{};
+  DecodeParams& p = a.p;
+  p.q = q;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.out = out;
+  float* ws = static_cast<float*>(workspace);
+  p.part_ml = need > 0 ? ws : nullptr;
+  p.part_o = need > 0 ? ws + static_cast<size_t>(num_seqs) * num_q_heads * parts * 2 : nullptr;
+  p.status = device_status;
+  p.num_kv_heads = num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.bs_log2 = log2i(block_size);
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.partition_tokens = P;
+  p.max_parts = parts;
+  p.q_is_bf16 = q_dtype == PKV_BF16;
+  p.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.num_seqs = num_seqs;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return fn(a);
+}

@@ -1,0 +1,47 @@
+// Launch helper for one (KV type, head_dim, group) instantiation of the decode
+// kernels; included by the per-KV-type translation units.
+#pragma once
+
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+// CTA shape of the CUDA-core path: 4 warps, 3-stage rings (2 chunks = 16 KiB
+// of K+V in flight per warp, 96 KiB per CTA, two CTAs per SM).
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 3;
+
+template <typename KV, int D, int G>
+pkv_status launch_decode(const DecodeLaunch& a) {
+  using SM = DecodeSmem<KV, D, G, kDecodeWarps, kDecodeStages>;
+  const DecodeParams& p = a.p;
+  const int bs = 1 << p.bs_log2;
+  const int table_entries = (p.partition_tokens + bs - 1) / bs + 2;
+  const size_t smem = SM::bytes(table_entries);
+  auto kern = paged_decode_kernel<KV, D, G, kDecodeWarps, kDecodeStages>;
+  static int configured_bytes = 0;   // largest dynamic smem opted in so far
+  if (static_cast<int>(smem) > configured_bytes) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    configured_bytes = static_cast<int>(smem);
+  }
+  dim3 grid(p.max_parts, p.num_kv_heads, a.num_seqs);
+  kern<<<grid, kDecodeWarps * 32, smem, a.stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  if (p.max_parts > 1) {
+    paged_decode_reduce_kernel<D><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+#define PKV_INSTANTIATE_DECODE(KV, D)                                   \
+  template pkv_status launch_decode<KV, D, 1>(const DecodeLaunch&);    \
+  template pkv_status launch_decode<KV, D, 2>(const DecodeLaunch&);    \
+  template pkv_status launch_decode<KV, D, 4>(const DecodeLaunch&);    \
+  template pkv_status launch_decode<KV, D, 8>(const DecodeLaunch&);
+
+}  // namespace pkv

@@ -1,0 +1,349 @@
+// Host block pool: FIFO free list, per-block reference counts, per-sequence
+// block tables and slot arithmetic.
+//
+// Behaviour follows "LLM inference tutorial" section 4.2 (class PagedKVCache:
+// free list 0..N-1, allocate_sequence takes the front block at once,
+// append_token's block/offset rule, free_sequence returns blocks to the tail,
+// memory_usage), section 4.3 (prefix sharing by reference count; a block is
+// released when its count reaches zero) and "nano-vLLM architecture" section
+// 4.3 (block_bytes and available_blocks = free_memory // block_bytes).
+//
+// The free list is a ring buffer of capacity num_blocks: a block id is in it
+// at most once, so it never overflows and both ends are O(1).
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace {
+
+int dtype_size(int32_t dt) {
+  switch (dt) {
+    case PKV_F32: return 4;
+    case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+struct Seq {
+  std::vector<int32_t> table;
+  int32_t len = 0;
+};
+
+}  // namespace
+
+struct pkv_pool {
+  pkv_pool_config cfg{};
+  int64_t num_blocks = 0;
+  int64_t block_bytes = 0;
+  std::vector<int32_t> ring;   // free list storage
+  int64_t head = 0;            // index of the front
+  int64_t count = 0;           // number of free blocks
+  std::vector<int32_t> ref;    // reference count per block (0 = free)
+  std::unordered_map<int64_t, Seq> seqs;
+
+  int32_t pop_front() {
+    int32_t b = ring[head];
+    head = (head + 1) % num_blocks;
+    --count;
+    return b;
+  }
+  void push_back(int32_t b) {
+    ring[(head + count) % num_blocks] = b;
+    ++count;
+  }
+  bool valid(int64_t b) const { return b >= 0 && b < num_blocks; }
+};
+
+namespace {
+
+bool seq_needs_block(const pkv_pool* p, const Seq& s) {
+  return static_cast<int64_t>(s.len / p->cfg.block_size) >= static_cast<int64_t>(s.table.size());
+}
+
+// Advance a sequence by one token, taking a block from the free-list front
+// when the token's logical block is not in the table yet.
+void append_one(pkv_pool* p, Seq& s) {
+  const int32_t blk = s.len / p->cfg.block_size;
+  if (blk >= static_cast<int32_t>(s.table.size())) {
+    const int32_t b = p->pop_front();
+    p->ref[b] = 1;
+    s.table.push_back(b);
+  }
+  ++s.len;
+}
+
+int64_t slot_of(const pkv_pool* p, const Seq& s, int32_t pos) {
+  const int32_t bs = p->cfg.block_size;
+  return static_cast<int64_t>(s.table[pos / bs]) * bs + pos % bs;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int32_t st) {
+  switch (st) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_NO_FREE_BLOCK: return "no free block";
+    case PKV_ERR_BAD_BLOCK: return "block id out of range";
+    case PKV_ERR_REFCOUNT: return "reference count error";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_HOST_MEMORY: return "host allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int64_t pkv_block_bytes(const pkv_pool_config* c) {
+  if (!c) return -1;
+  const int es = dtype_size(c->kv_dtype);
+  if (c->num_layers <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0 ||
+      es == 0)
+    return -1;
+  return 2LL * c->num_layers * c->block_size * c->num_kv_heads * c->head_dim * es;
+}
+
+pkv_status kv_pool_init(const pkv_pool_config* cfg, pkv_pool** out) {
+  if (!cfg || !out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int64_t bb = pkv_block_bytes(cfg);
+  if (bb <= 0) return PKV_ERR_INVALID_ARG;
+  int64_t nb = cfg->num_blocks;
+  if (nb == 0) nb = cfg->free_bytes > 0 ? cfg->free_bytes / bb : 0;
+  if (nb <= 0 || nb > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  pkv_pool* p = new (std::nothrow) pkv_pool();
+  if (!p) return PKV_ERR_HOST_MEMORY;
+  try {
+    p->cfg = *cfg;
+    p->cfg.initial_free_order = nullptr;
+    p->cfg.num_blocks = nb;
+    p->num_blocks = nb;
+    p->block_bytes = bb;
+    p->ring.resize(nb);
+    p->ref.assign(nb, 0);
+    if (cfg->initial_free_order) {
+      std::vector<char> seen(nb, 0);
+      for (int64_t i = 0; i < nb; ++i) {
+        const int32_t b = cfg->initial_free_order[i];
+        if (b < 0 || b >= nb || seen[b]) {
+          delete p;
+          return PKV_ERR_INVALID_ARG;
+        }
+        seen[b] = 1;
+        p->ring[i] = b;
+      }
+    } else {
+      for (int64_t i = 0; i < nb; ++i) p->ring[i] = static_cast<int32_t>(i);
+    }
+    p->head = 0;
+    p->count = nb;
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return PKV_ERR_HOST_MEMORY;
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+void kv_pool_destroy(pkv_pool* p) { delete p; }
+
+pkv_status block_alloc(pkv_pool* p, int32_t* id) {
+  if (!p || !id) return PKV_ERR_INVALID_ARG;
+  if (p->count == 0) return PKV_ERR_NO_FREE_BLOCK;
+  const int32_t b = p->pop_front();
+  p->ref[b] = 1;
+  *id = b;
+  return PKV_OK;
+}
+
+pkv_status block_ref(pkv_pool* p, int32_t id) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  if (!p->valid(id)) return PKV_ERR_BAD_BLOCK;
+  if (p->ref[id] <= 0) return PKV_ERR_REFCOUNT;
+  ++p->ref[id];
+  return PKV_OK;
+}
+
+pkv_status block_free(pkv_pool* p, int32_t id) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  if (!p->valid(id)) return PKV_ERR_BAD_BLOCK;
+  if (p->ref[id] <= 0) return PKV_ERR_REFCOUNT;
+  if (--p->ref[id] == 0) p->push_back(id);
+  return PKV_OK;
+}
+
+pkv_status block_refcount(const pkv_pool* p, int32_t id, int32_t* count) {
+  if (!p || !count) return PKV_ERR_INVALID_ARG;
+  if (!p->valid(id)) return PKV_ERR_BAD_BLOCK;
+  *count = p->ref[id];
+  return PKV_OK;
+}
+
+pkv_status kv_pool_stats(const pkv_pool* p, pkv_pool_stats* o) {
+  if (!p || !o) return PKV_ERR_INVALID_ARG;
+  o->total_blocks = p->num_blocks;
+  o->free_blocks = p->count;
+  o->used_blocks = p->num_blocks - p->count;
+  o->utilization = static_cast<double>(o->used_blocks) / static_cast<double>(p->num_blocks) * 100.0;
+  o->block_bytes = p->block_bytes;
+  o->total_bytes = p->num_blocks * p->block_bytes;
+  o->used_bytes = o->used_blocks * p->block_bytes;
+  return PKV_OK;
+}
+
+pkv_status kv_pool_free_list(const pkv_pool* p, int32_t* out, int64_t cap, int64_t* n) {
+  if (!p || !n) return PKV_ERR_INVALID_ARG;
+  *n = p->count;
+  if (cap < p->count || (!out && p->count > 0)) return PKV_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < p->count; ++i) out[i] = p->ring[(p->head + i) % p->num_blocks];
+  return PKV_OK;
+}
+
+pkv_status seq_create(pkv_pool* p, int64_t sid) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  if (p->seqs.count(sid)) return PKV_ERR_INVALID_ARG;
+  if (p->count == 0) return PKV_ERR_NO_FREE_BLOCK;
+  try {
+    Seq s;
+    s.table.reserve(8);
+    const int32_t b = p->pop_front();
+    p->ref[b] = 1;
+    s.table.push_back(b);
+    p->seqs.emplace(sid, std::move(s));
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_fork_prefix(pkv_pool* p, int64_t dst, int64_t src, int32_t ntok) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(src);
+  if (it == p->seqs.end() || p->seqs.count(dst)) return PKV_ERR_INVALID_ARG;
+  const int32_t bs = p->cfg.block_size;
+  if (ntok <= 0 || ntok % bs != 0 || ntok > it->second.len) return PKV_ERR_INVALID_ARG;
+  try {
+    Seq s;
+    s.table.assign(it->second.table.begin(), it->second.table.begin() + ntok / bs);
+    s.len = ntok;
+    for (int32_t b : s.table) ++p->ref[b];
+    p->seqs.emplace(dst, std::move(s));
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_append_slots(pkv_pool* p, const int64_t* ids, int32_t n, int64_t* slots) {
+  if (!p || n < 0 || (n > 0 && (!ids || !slots))) return PKV_ERR_INVALID_ARG;
+  std::vector<Seq*> v;
+  try {
+    v.reserve(n);
+    std::unordered_set<int64_t> seen;
+    seen.reserve(static_cast<size_t>(n) * 2);
+    int64_t need = 0;
+    for (int32_t i = 0; i < n; ++i) {
+      auto it = p->seqs.find(ids[i]);
+      if (it == p->seqs.end() || !seen.insert(ids[i]).second) return PKV_ERR_INVALID_ARG;
+      if (seq_needs_block(p, it->second)) ++need;
+      v.push_back(&it->second);
+    }
+    if (need > p->count) return PKV_ERR_NO_FREE_BLOCK;
+    for (int32_t i = 0; i < n; ++i) {
+      Seq& s = *v[i];
+      if (seq_needs_block(p, s)) s.table.reserve(s.table.size() + 1);
+    }
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    Seq& s = *v[i];
+    const int32_t pos = s.len;
+    append_one(p, s);
+    slots[i] = slot_of(p, s, pos);
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_append_tokens(pkv_pool* p, int64_t sid, int32_t n, int64_t* slots) {
+  if (!p || n < 0) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  Seq& s = it->second;
+  const int64_t bs = p->cfg.block_size;
+  const int64_t have = static_cast<int64_t>(s.table.size()) * bs;
+  const int64_t over = static_cast<int64_t>(s.len) + n - have;
+  const int64_t need = over > 0 ? (over + bs - 1) / bs : 0;
+  if (need > p->count) return PKV_ERR_NO_FREE_BLOCK;
+  if (static_cast<int64_t>(s.len) + n > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  try {
+    s.table.reserve(s.table.size() + need);
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t pos = s.len;
+    append_one(p, s);
+    if (slots) slots[i] = slot_of(p, s, pos);
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_length(const pkv_pool* p, int64_t sid, int32_t* len) {
+  if (!p || !len) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  *len = it->second.len;
+  return PKV_OK;
+}
+
+pkv_status seq_block_table(const pkv_pool* p, int64_t sid, int32_t* out, int32_t cap,
+                           int32_t* nblocks) {
+  if (!p || !nblocks) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  const auto& t = it->second.table;
+  *nblocks = static_cast<int32_t>(t.size());
+  if (cap < static_cast<int32_t>(t.size()) || (!out && !t.empty())) return PKV_ERR_INVALID_ARG;
+  if (!t.empty()) std::memcpy(out, t.data(), t.size() * sizeof(int32_t));
+  return PKV_OK;
+}
+
+pkv_status seq_batch_tables(const pkv_pool* p, const int64_t* ids, int32_t n, int32_t mb,
+                            int32_t* tables, int32_t* lens) {
+  if (!p || n < 0 || mb < 0 || (n > 0 && (!ids || !lens || (mb > 0 && !tables))))
+    return PKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = p->seqs.find(ids[i]);
+    if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(it->second.table.size()) > mb) return PKV_ERR_INVALID_ARG;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const Seq& s = p->seqs.find(ids[i])->second;
+    int32_t* row = tables + static_cast<int64_t>(i) * mb;
+    const int32_t k = static_cast<int32_t>(s.table.size());
+    for (int32_t j = 0; j < k; ++j) row[j] = s.table[j];
+    for (int32_t j = k; j < mb; ++j) row[j] = -1;
+    lens[i] = s.len;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_free(pkv_pool* p, int64_t sid) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  for (int32_t b : it->second.table) {
+    if (--p->ref[b] == 0) p->push_back(b);
+  }
+  p->seqs.erase(it);
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+"""Builders for GPU parity cases: the same seeded decode step run through the
+C-ABI library (C++ pool + CUDA kernels) and through the oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import workloads as W
+from oracle import attention as OA
+from oracle import fp8 as OF8
+from oracle import pool as OP
+
+CODE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
+POISON = {"f32": (np.float32, np.float32(np.nan)), "bf16": (np.uint16, 0x7FC0),
+          "fp8_e4m3": (np.uint8, 0x7F)}
+
+
+class OraclePool:
+    """The oracle pool behind the call names of the C pool wrapper."""
+
+    def __init__(self, *a, **k):
+        self.p = OP.Pool(*a, **k)
+
+    def seq_create(self, s):
+        self.p.seq_create(s)
+
+    def seq_fork_prefix(self, d, s, n):
+        self.p.seq_fork_prefix(d, s, n)
+
+    def append_tokens(self, s, n):
+        return np.asarray(self.p.seq_append_tokens(s, n), dtype=np.int64)
+
+    def append_slots(self, sids):
+        return np.asarray(self.p.seq_append_slots(list(sids)), dtype=np.int64)
+
+
+def src_dtype(w):
+    return "bf16" if w.kv_dtype == "fp8_e4m3" else w.kv_dtype
+
+
+def torch_dtype(code_name):
+    import torch
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[code_name]
+
+
+def to_torch(a, name, device="cuda"):
+    """numpy storage array -> torch tensor of the storage dtype on device."""
+    import torch
+    if name == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def from_torch(t, name):
+    import torch
+    if name == "bf16":
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+@dataclasses.dataclass
+class SmallCase:
+    """Every input of one decode step, small enough for the oracle end to end."""
+    w: W.DecodeWorkload
+    lens: np.ndarray
+    nb: int
+    order: np.ndarray
+    prompt_slots: list          # per layer-independent slot arrays (owner first if any)
+    prompt_k: list              # per layer: [U, Hkv, D] storage arrays
+    prompt_v: list
+    step_slots: np.ndarray
+    k_new: list                 # per layer [S, Hkv, D]
+    v_new: list
+    q: list                     # per layer [S, Hq, D]
+    k_scale: list               # per layer [Hkv] float32 (fp8) or None
+    v_scale: list
+    tables: np.ndarray          # oracle pool's [S, MB] padded -1
+    max_blocks: int
+
+
+def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None) -> tuple:
+    """Build a small case; returns (case, c-pool) after checking both pools agree."""
+    import paged_kv_cache_295_gb300 as pkv
+    from paged_kv_cache_295_gb300.engine import build_prompts
+    lens = W.context_lens(w) if lens is None else np.asarray(lens, dtype=np.int64)
+    nb = W.num_blocks(w, lens) if nb is None else nb
+    order = W.free_order(w, nb)
+    L = w.num_layers if layers is None else layers
+    esz = W.ELEM_BYTES[w.kv_dtype]
+    cpool = pkv.Pool(L, w.num_kv_heads, w.head_dim, w.block_size, CODE[w.kv_dtype],
+                     num_blocks=nb, initial_free_order=order)
+    opool = OraclePool(L, w.num_kv_heads, w.head_dim, w.block_size, esz, nb,
+                       initial_free_order=order.tolist())
+    c_owner, c_slots, c_oslots = build_prompts(cpool, lens, w.prefix_tokens, w.prefix_seqs)
+    o_owner, o_slots, o_oslots = build_prompts(opool, lens, w.prefix_tokens, w.prefix_seqs)
+    assert c_owner == o_owner
+    for a, b in zip(c_slots, o_slots):
+        assert np.array_equal(a, b)
+    if c_oslots is not None:
+        assert np.array_equal(c_oslots, o_oslots)
+    step_c = cpool.append_slots(range(len(lens)))
+    step_o = opool.append_slots(range(len(lens)))
+    assert np.array_equal(step_c, step_o)
+    mb = max(len(opool.p.tables[s]) for s in range(len(lens)))
+    t_o, l_o = opool.p.padded_tables(list(range(len(lens))), mb)
+    t_c, l_c = cpool.batch_tables(list(range(len(lens))), mb)
+    assert np.array_equal(np.asarray(t_o), t_c) and np.array_equal(np.asarray(l_o), l_c)
+    assert np.array_equal(l_c, lens)
+
+    prompt_slots = ([o_oslots] if o_oslots is not None else []) + list(o_slots)
+    prompt_slots = np.concatenate(prompt_slots) if prompt_slots else np.zeros(0, np.int64)
+    U = prompt_slots.size
+    S, hkv, hq, d = len(lens), w.num_kv_heads, w.num_q_heads, w.head_dim
+    sd = src_dtype(w)
+    kh = W.k_head_scales(w)[None, :, None]
+    pk, pv, kn, vn, qq, ks_l, vs_l = [], [], [], [], [], [], []
+    for layer in range(L):
+        base = 100 * (layer + 1)
+        k32 = W.normal_f32(w.seed, base + 0, (U, hkv, d)) * kh
+        v32 = W.normal_f32(w.seed, base + 1, (U, hkv, d))
+        kn32 = W.normal_f32(w.seed, base + 2, (S, hkv, d)) * kh
+        vn32 = W.normal_f32(w.seed, base + 3, (S, hkv, d))
+        q32 = W.normal_f32(w.seed, base + 4, (S, hq, d))
+        pk.append(W.store(k32, sd))
+        pv.append(W.store(v32, sd))
+        kn.append(W.store(kn32, sd))
+        vn.append(W.store(vn32, sd))
+        qq.append(W.store(q32, w.q_dtype))
+        if w.kv_dtype == "fp8_e4m3":
+            ka = np.abs(np.concatenate([OA.to_f64(pk[-1], sd), OA.to_f64(kn[-1], sd)])).max((0, 2))
+            va = np.abs(np.concatenate([OA.to_f64(pv[-1], sd), OA.to_f64(vn[-1], sd)])).max((0, 2))
+            ks_l.append(W.fp8_scale_from_absmax(ka))
+            vs_l.append(W.fp8_scale_from_absmax(va))
+        else:
+            ks_l.append(None)
+            vs_l.append(None)
+    case = SmallCase(w, lens, nb, order, prompt_slots, pk, pv, step_c, kn, vn, qq, ks_l, vs_l,
+                     np.asarray(t_o, dtype=np.int32), mb)
+    return case, cpool
+
+
+def oracle_caches(case: SmallCase, layer: int):
+    """Oracle cache state after the prompts and the step's append (numpy)."""
+    w = case.w
+    dt, pz = POISON[w.kv_dtype]
+    shape = (case.nb, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = np.full(shape, pz, dtype=dt)
+    vc = np.full(shape, pz, dtype=dt)
+    sd = src_dtype(w)
+    OA.reshape_and_cache(case.prompt_k[layer], case.prompt_v[layer], case.prompt_slots, kc, vc,
+                         sd, w.kv_dtype, case.k_scale[layer], case.v_scale[layer])
+    OA.reshape_and_cache(case.k_new[layer], case.v_new[layer], case.step_slots, kc, vc, sd,
+                         w.kv_dtype, case.k_scale[layer], case.v_scale[layer])
+    return kc, vc
+
+
+def oracle_out(case: SmallCase, layer: int, kc, vc, seqs=None):
+    w = case.w
+    return OA.paged_attention_decode(case.q[layer], kc, vc, case.tables, case.lens, w.scale,
+                                     w.q_dtype, w.kv_dtype, case.k_scale[layer],
+                                     case.v_scale[layer], seqs=seqs)
+
+
+def run_gpu(case: SmallCase, partition=0, layers=None, tables=None):
+    """Product path for every layer: append prompts, append the step, attend.
+
+    Returns (engine, list of per-layer outputs as numpy float32, status word).
+    """
+    import torch
+    from paged_kv_cache_295_gb300.engine import PagedKVCache
+    w = case.w
+    L = len(case.prompt_k) if layers is None else layers
+    eng = PagedKVCache(L, w.num_kv_heads, w.head_dim, w.block_size, case.nb, CODE[w.kv_dtype],
+                       initial_free_order=case.order)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sd = src_dtype(w)
+    slots_p = torch.from_numpy(case.prompt_slots).cuda()
+    slots_s = torch.from_numpy(case.step_slots).cuda()
+    bt = torch.from_numpy(case.tables if tables is None else tables).cuda()
+    cl = torch.from_numpy(case.lens.astype(np.int32)).cuda()
+    outs = []
+    for layer in range(L):
+        if eng.k_scale is not None:
+            eng.k_scale[layer] = torch.from_numpy(case.k_scale[layer]).cuda()
+            eng.v_scale[layer] = torch.from_numpy(case.v_scale[layer]).cuda()
+        if case.prompt_slots.size:
+            eng.append(layer, to_torch(case.prompt_k[layer], sd), to_torch(case.prompt_v[layer], sd),
+                       slots_p, device_status=status)
+        eng.append(layer, to_torch(case.k_new[layer], sd), to_torch(case.v_new[layer], sd),
+                   slots_s, device_status=status)
+        out = eng.attend(layer, to_torch(case.q[layer], w.q_dtype), bt, cl, int(case.lens.max()),
+                         partition=partition, device_status=status)
+        outs.append(out.cpu().numpy())
+    torch.cuda.synchronize()
+    return eng, outs, int(status.item())

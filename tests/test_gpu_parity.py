@@ -1,0 +1,216 @@
+"""GPU parity: the C-ABI library against the oracle on seeded small decode steps.
+
+Slots, tables and cache bytes must be bit-exact; attention outputs within the
+stated max-abs tolerances (2e-3 for bf16/f32 KV, 1e-2 for FP8 KV).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import gpu_cases as GC
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2}
+
+
+@pytest.fixture(scope="module")
+def torch_cuda(lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    return torch
+
+
+def _check_layer(case, eng, outs, layer, tol=None):
+    kc, vc = GC.oracle_caches(case, layer)
+    w = case.w
+    gk = GC.from_torch(eng.k_cache(layer), w.kv_dtype)
+    gv = GC.from_torch(eng.v_cache(layer), w.kv_dtype)
+    assert gk.tobytes() == kc.tobytes(), "K cache bytes differ from the oracle append"
+    assert gv.tobytes() == vc.tobytes(), "V cache bytes differ from the oracle append"
+    ref = GC.oracle_out(case, layer, kc, vc)
+    got = outs[layer]
+    assert np.isfinite(got).all()
+    err = np.abs(got.astype(np.float64) - ref).max()
+    assert err <= (TOL[w.kv_dtype] if tol is None else tol), f"max abs err {err}"
+    return err
+
+
+def test_tiny_fp32_workload(torch_cuda):
+    case, _ = GC.make_small(W.TINY)
+    eng, outs, st = GC.run_gpu(case)
+    assert st == 0
+    err = _check_layer(case, eng, outs, 0, tol=1e-5)
+    assert err < 1e-5
+
+
+SMALL = {
+    "llama7b_mha_bf16": (dataclasses.replace(W.LLAMA7B_LAYER, num_seqs=6),
+                         [1, 16, 17, 255, 256, 700]),
+    "llama70b_gqa8_bf16": (dataclasses.replace(W.LLAMA70B_GQA, num_seqs=4), [1, 128, 129, 1500]),
+    "long_ctx_gqa4_bf16": (dataclasses.replace(W.LONG_CTX, num_seqs=2), [5000, 9000]),
+    "ragged_fp8_prefix": (dataclasses.replace(W.RAGGED_FP8, num_seqs=10, num_layers=2,
+                                              prefix_tokens=64, prefix_seqs=5),
+                          [65, 66, 100, 300, 64 + 17, 1, 2, 33, 250, 400]),
+    "d64_bf16_g2_bs1": (W.DecodeWorkload("d64g2", 3, 8, 4, 64, 1, "bf16", "bf16", seed=9,
+                                         ctx_law="fixed"), [1, 7, 300]),
+    "d256_bf16_mha_bs32": (W.DecodeWorkload("d256", 3, 2, 2, 256, 32, "bf16", "f32", seed=10,
+                                            ctx_law="fixed"), [31, 32, 333]),
+    "d64_fp8_g4_bs8": (W.DecodeWorkload("d64fp8", 3, 8, 2, 64, 8, "fp8_e4m3", "bf16", seed=11,
+                                        ctx_law="fixed"), [3, 64, 513]),
+    "d128_f32_g8_bs64": (W.DecodeWorkload("f32g8", 2, 16, 2, 128, 64, "f32", "f32", seed=12,
+                                          ctx_law="fixed"), [64, 777]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("partition", [0, 64])
+def test_small_parity(torch_cuda, name, partition):
+    w, lens = SMALL[name]
+    case, _ = GC.make_small(w, lens=lens)
+    eng, outs, st = GC.run_gpu(case, partition=partition)
+    assert st == 0
+    for layer in range(len(outs)):
+        _check_layer(case, eng, outs, layer)
+
+
+@pytest.mark.parametrize("name", ["llama7b_mha_bf16", "long_ctx_gqa4_bf16"])
+def test_split_count_invariance(torch_cuda, name):
+    w, lens = SMALL[name]
+    case, _ = GC.make_small(w, lens=lens)
+    ref = None
+    for part in (0, 64, 192, 4096):
+        _, outs, st = GC.run_gpu(case, partition=part)
+        assert st == 0
+        if ref is None:
+            ref = outs[0]
+        else:
+            assert np.abs(outs[0] - ref).max() <= 1e-5
+
+
+def test_block_permutation_bit_identical(torch_cuda):
+    torch = torch_cuda
+    w, lens = SMALL["llama7b_mha_bf16"]
+    case, _ = GC.make_small(w, lens=lens)
+    eng, outs, _ = GC.run_gpu(case)
+    perm = np.random.default_rng(3).permutation(case.nb)
+    st2 = torch.empty_like(eng.storage)
+    st2[:, :, torch.from_numpy(perm).cuda()] = eng.storage
+    t2 = np.where(case.tables >= 0, perm[np.maximum(case.tables, 0)], -1).astype(np.int32)
+    q = GC.to_torch(case.q[0], w.q_dtype)
+    import paged_kv_cache_295_gb300 as pkv
+    out2 = pkv.paged_attention_decode(q, st2[0, 0], st2[0, 1], torch.from_numpy(t2).cuda(),
+                                      torch.from_numpy(case.lens.astype(np.int32)).cuda(),
+                                      w.scale, int(case.lens.max()))
+    assert out2.cpu().numpy().tobytes() == outs[0].tobytes()
+
+
+def test_context_one_and_constant_v(torch_cuda):
+    torch = torch_cuda
+    w = W.DecodeWorkload("c1", 4, 8, 2, 128, 16, "bf16", "bf16", seed=13, ctx_law="fixed")
+    case, _ = GC.make_small(w, lens=[1, 1, 40, 90])
+    eng, outs, _ = GC.run_gpu(case)
+    G = 4
+    for s in (0, 1):
+        row = GC.OA.to_f64(case.k_new[0][s], "bf16")  # ctx 1: the step's own token
+        vrow = GC.OA.to_f64(case.v_new[0][s], "bf16")
+        for h in range(8):
+            assert np.array_equal(outs[0][s, h].astype(np.float64), vrow[h // G])
+        del row
+    # constant V rows: overwrite every V slot of the layer with one row per head
+    const = GC.W.store(np.random.default_rng(2).standard_normal((2, 128), dtype=np.float32), "bf16")
+    eng.v_cache(0)[:] = GC.to_torch(const, "bf16")[None, None]
+    import paged_kv_cache_295_gb300 as pkv
+    out = eng.attend(0, GC.to_torch(case.q[0], "bf16"),
+                     torch.from_numpy(case.tables).cuda(),
+                     torch.from_numpy(case.lens.astype(np.int32)).cuda(), 90).cpu().numpy()
+    want = GC.OA.to_f64(const, "bf16")
+    for s in range(4):
+        for h in range(8):
+            np.testing.assert_allclose(out[s, h], want[h // G], rtol=1e-5, atol=0)
+
+
+def test_empty_context_and_status_flags(torch_cuda):
+    torch = torch_cuda
+    w, lens = SMALL["llama7b_mha_bf16"]
+    case, _ = GC.make_small(w, lens=lens)
+    eng, outs, _ = GC.run_gpu(case)
+    import paged_kv_cache_295_gb300 as pkv
+    q = GC.to_torch(case.q[0], w.q_dtype)
+    lens0 = case.lens.astype(np.int32).copy()
+    lens0[2] = 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = eng.attend(0, q, torch.from_numpy(case.tables).cuda(), torch.from_numpy(lens0).cuda(),
+                     int(case.lens.max()), device_status=status).cpu().numpy()
+    assert (out[2] == 0).all() and status.item() == 0
+    assert out[1].tobytes() == outs[0][1].tobytes()
+    # an out-of-range block id is skipped (never read) and flagged
+    bad = case.tables.copy()
+    bad[5, 3] = case.nb + 7
+    out = eng.attend(0, q, torch.from_numpy(bad).cuda(),
+                     torch.from_numpy(case.lens.astype(np.int32)).cuda(), int(case.lens.max()),
+                     device_status=status).cpu().numpy()
+    torch.cuda.synchronize()
+    assert status.item() & pkv.DEV_BAD_BLOCK
+    assert out[:5].tobytes() == outs[0][:5].tobytes()
+    # a context longer than the launch covers is clamped and flagged
+    status.zero_()
+    lens2 = case.lens.astype(np.int32).copy()
+    lens2[0] = 700
+    eng.attend(0, q, torch.from_numpy(case.tables).cuda(), torch.from_numpy(lens2).cuda(), 256,
+               device_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & pkv.DEV_BAD_CONTEXT
+    # negative slots skip, slots beyond the pool are flagged and skipped
+    status.zero_()
+    before = eng.storage.clone()
+    k1 = GC.to_torch(case.k_new[0][:2], "bf16")
+    eng.append(0, k1, k1, torch.tensor([-1, case.nb * 16 + 3], dtype=torch.int64, device="cuda"),
+               device_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & pkv.DEV_BAD_SLOT
+    assert torch.equal(before.view(torch.int16), eng.storage.view(torch.int16))
+
+
+def _halfway_f32():
+    from oracle import fp8 as OF8
+    vals = sorted(set(OF8.decode_code(c) for c in range(0x00, 0x7F)))
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    out = []
+    for m in mids:
+        m32 = np.float32(m)
+        out += [m32, np.nextafter(m32, np.float32(0)), np.nextafter(m32, np.float32(1e9))]
+    out += [448.0, 449.0, 464.0, 465.0, 1e6, 2.0 ** -10, 2.0 ** -11, 0.0]
+    out = np.array(out, dtype=np.float32)
+    return np.concatenate([out, -out])
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37])
+def test_fp8_append_rounding_bit_exact(torch_cuda, scale):
+    """Every E4M3 halfway case (and its neighbours) through the quantising append."""
+    torch = torch_cuda
+    import paged_kv_cache_295_gb300 as pkv
+    from oracle import attention as OA
+    x = _halfway_f32() * np.float32(scale)
+    hkv, d = 2, 16
+    n = -(-x.size // (hkv * d))
+    pad = np.zeros(n * hkv * d, np.float32)
+    pad[: x.size] = x
+    k = pad.reshape(n, hkv, d)
+    v = -k
+    nb, bs = n, 1
+    slots = np.random.default_rng(0).permutation(nb).astype(np.int64)
+    sc = np.array([scale, scale], np.float32)
+    kc = torch.zeros((nb, bs, hkv, d), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    pkv.reshape_and_cache(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                          torch.from_numpy(slots).cuda(), kc, vc, torch.from_numpy(sc).cuda(),
+                          torch.from_numpy(sc).cuda())
+    okc = np.zeros((nb, bs, hkv, d), np.uint8)
+    ovc = okc.copy()
+    OA.reshape_and_cache(k, v, slots, okc, ovc, "f32", "fp8_e4m3", sc, sc)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
