@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--partition", type=int, default=0, help="split-KV tokens (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=0, help="e2e steps (0 = min(steps, 200))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bandwidth-ref", action="store_true",
+                    help="skip the in-run copy/read reference kernels (profiling runs)")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -337,7 +339,7 @@ def run_ours(args):
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
-    bw = in_run_bandwidth(dev)
+    bw = None if args.no_bandwidth_ref else in_run_bandwidth(dev)
     st = DeviceStep(w, dev, partition=args.partition)
     L = w.num_layers
     for i in range(Wm):
@@ -399,9 +401,9 @@ def run_ours(args):
                      "kernel": "paged_decode_kernel" + (" + paged_decode_reduce_kernel"
                                                         if st.max_parts > 1 else ""),
                      "alg_bytes_per_launch": attn_bytes,
-                     "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4),
-                     "frac_of_in_run_read": round(achieved / bw["read_gbs"], 4)},
-        "in_run_bandwidth_gbs": {k: round(v, 1) for k, v in bw.items()},
+                     "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4) if bw else None,
+                     "frac_of_in_run_read": round(achieved / bw["read_gbs"], 4) if bw else None},
+        "in_run_bandwidth_gbs": {k: round(v, 1) for k, v in bw.items()} if bw else None,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * st.launches_per_step(),
