@@ -56,6 +56,8 @@ typedef enum {
 #define PKV_DEV_BAD_BLOCK 0x1     /* a block-table entry outside [0, num_blocks) */
 #define PKV_DEV_BAD_SLOT 0x2      /* a slot >= num_blocks * block_size */
 #define PKV_DEV_BAD_CONTEXT 0x4   /* context_lens[s] < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEV_TIMEOUT 0x8       /* an asynchronous copy did not land within 2 s; the CTA
+                                     stopped early and its output is not valid */
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
 DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E4M3: "fp8_e4m3"}
-DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT = 0x1, 0x2, 0x4
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 STATUS = {0: "ok", 1: "invalid_arg", 2: "no_free_block", 3: "bad_block", 4: "refcount",
           5: "unsupported", 6: "cuda", 7: "host_memory"}

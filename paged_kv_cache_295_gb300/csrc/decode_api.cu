@@ -2,6 +2,8 @@
 // partition choice, workspace layout and dispatch to the kernel instantiation
 // for (KV type, head_dim, query-group size).
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "decode_kernel.cuh"
 
@@ -28,6 +30,13 @@ int device_sm_count() {
 namespace {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// PKV_DECODE_PATH=simt forces the CUDA-core kernel where the tensor-core one
+// would run (used by the tests to check both paths on the same inputs).
+bool force_simt() {
+  const char* v = std::getenv("PKV_DECODE_PATH");
+  return v && std::strcmp(v, "simt") == 0;
+}
 
 int log2i(int64_t x) {
   int r = 0;
@@ -180,5 +189,7 @@ extern "C" pkv_status paged_attention_decode(
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (!force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks))
+    return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32);
   return fn(a);
 }

@@ -63,12 +63,29 @@ SMALL = {
                                         ctx_law="fixed"), [3, 64, 513]),
     "d128_f32_g8_bs64": (W.DecodeWorkload("f32g8", 2, 16, 2, 128, 64, "f32", "f32", seed=12,
                                           ctx_law="fixed"), [64, 777]),
+    "d64_bf16_g16_bs8_qf32": (W.DecodeWorkload("g16", 3, 32, 2, 64, 8, "bf16", "f32", seed=14,
+                                               ctx_law="fixed"), [8, 9, 700]),
+    "d128_bf16_g1_bs32_qf32": (W.DecodeWorkload("qf32", 3, 4, 4, 128, 32, "bf16", "f32",
+                                                seed=15, ctx_law="fixed"), [1, 33, 1000]),
+    "d128_bf16_g16_bs16": (W.DecodeWorkload("g16b", 2, 16, 1, 128, 16, "bf16", "bf16",
+                                            seed=16, ctx_law="fixed"), [15, 1200]),
 }
+
+
+@pytest.fixture(params=["auto", "simt"])
+def decode_path(request, monkeypatch):
+    """'auto' = the library's own kernel choice (tensor-core path for 16-bit
+    caches it supports); 'simt' forces the CUDA-core kernel everywhere."""
+    if request.param == "simt":
+        monkeypatch.setenv("PKV_DECODE_PATH", "simt")
+    else:
+        monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
+    return request.param
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 @pytest.mark.parametrize("partition", [0, 64])
-def test_small_parity(torch_cuda, name, partition):
+def test_small_parity(torch_cuda, name, partition, decode_path):
     w, lens = SMALL[name]
     case, _ = GC.make_small(w, lens=lens)
     eng, outs, st = GC.run_gpu(case, partition=partition)
@@ -77,8 +94,8 @@ def test_small_parity(torch_cuda, name, partition):
         _check_layer(case, eng, outs, layer)
 
 
-@pytest.mark.parametrize("name", ["llama7b_mha_bf16", "long_ctx_gqa4_bf16"])
-def test_split_count_invariance(torch_cuda, name):
+@pytest.mark.parametrize("name", ["llama7b_mha_bf16", "long_ctx_gqa4_bf16", "d64_bf16_g16_bs8_qf32"])
+def test_split_count_invariance(torch_cuda, name, decode_path):
     w, lens = SMALL[name]
     case, _ = GC.make_small(w, lens=lens)
     ref = None
@@ -91,7 +108,7 @@ def test_split_count_invariance(torch_cuda, name):
             assert np.abs(outs[0] - ref).max() <= 1e-5
 
 
-def test_block_permutation_bit_identical(torch_cuda):
+def test_block_permutation_bit_identical(torch_cuda, decode_path):
     torch = torch_cuda
     w, lens = SMALL["llama7b_mha_bf16"]
     case, _ = GC.make_small(w, lens=lens)
@@ -108,7 +125,7 @@ def test_block_permutation_bit_identical(torch_cuda):
     assert out2.cpu().numpy().tobytes() == outs[0].tobytes()
 
 
-def test_context_one_and_constant_v(torch_cuda):
+def test_context_one_and_constant_v(torch_cuda, decode_path):
     torch = torch_cuda
     w = W.DecodeWorkload("c1", 4, 8, 2, 128, 16, "bf16", "bf16", seed=13, ctx_law="fixed")
     case, _ = GC.make_small(w, lens=[1, 1, 40, 90])
@@ -133,7 +150,7 @@ def test_context_one_and_constant_v(torch_cuda):
             np.testing.assert_allclose(out[s, h], want[h // G], rtol=1e-5, atol=0)
 
 
-def test_empty_context_and_status_flags(torch_cuda):
+def test_empty_context_and_status_flags(torch_cuda, decode_path):
     torch = torch_cuda
     w, lens = SMALL["llama7b_mha_bf16"]
     case, _ = GC.make_small(w, lens=lens)
