@@ -143,8 +143,10 @@ extern "C" pkv_status paged_attention_decode(
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
+  const bool use_mma =
+      !force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   LaunchFn fn = pick(kv_dtype, head_dim, G);
-  if (!fn) return PKV_ERR_UNSUPPORTED;
+  if (!use_mma && !fn) return PKV_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
@@ -189,7 +191,7 @@ extern "C" pkv_status paged_attention_decode(
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
-  if (!force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks))
+  if (use_mma)
     return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32);
   return fn(a);
 }

@@ -87,6 +87,8 @@ def decode_path(request, monkeypatch):
 @pytest.mark.parametrize("partition", [0, 64])
 def test_small_parity(torch_cuda, name, partition, decode_path):
     w, lens = SMALL[name]
+    if decode_path == "simt" and w.group > 8:
+        pytest.skip("the CUDA-core kernel is built for groups of 1, 2, 4 and 8")
     case, _ = GC.make_small(w, lens=lens)
     eng, outs, st = GC.run_gpu(case, partition=partition)
     assert st == 0
