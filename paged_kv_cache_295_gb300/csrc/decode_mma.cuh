@@ -26,8 +26,9 @@
 //    a running max / sum per query row (online softmax, base 2).
 //
 //  * PV.  O[h][d] += P[h][t] V[t][d] with the probabilities re-used from the QK
-//    accumulator layout as the A operand (16 tokens = one k-step) and V as the
-//    B operand via ldmatrix.trans.  Accumulation is float32.
+//    accumulator layout as the A operand (16 tokens = one k-step; P is split
+//    into bf16 hi + lo parts, two products) and V as the B operand via
+//    ldmatrix.trans.  Accumulation is float32.
 //
 // The epilogue (combining warps, writing the output or split-KV partials) is
 // the same as the CUDA-core path's.
@@ -387,7 +388,9 @@ __global__ void __launch_bounds__(NW * 32)
       m0 = mn0;
       if (ROWS16) m1 = mn1;
     }
-    uint32_t pa[4];
+    // P as the A operand, split into bf16 hi + lo parts so the PV product
+    // keeps ~2^-17 relative precision (a single bf16 P would cost ~2^-9).
+    uint32_t pa[4], pl[4];
     {
       float pr[2][4];
 #pragma unroll
@@ -399,10 +402,13 @@ __global__ void __launch_bounds__(NW * 32)
         l0 += pr[j][0] + pr[j][1];
         if (ROWS16) l1 += pr[j][2] + pr[j][3];
       }
-      pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-      pa[1] = pack_bf16(pr[0][2], pr[0][3]);
-      pa[2] = pack_bf16(pr[1][0], pr[1][1]);
-      pa[3] = pack_bf16(pr[1][2], pr[1][3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x0 = pr[k >> 1][(k & 1) * 2], x1 = pr[k >> 1][(k & 1) * 2 + 1];
+        pa[k] = pack_bf16(x0, x1);
+        const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&pa[k]);
+        pl[k] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
+      }
     }
     // ---- O += P V: 16 tokens x D dims -------------------------------------------
 #pragma unroll
@@ -415,6 +421,8 @@ __global__ void __launch_bounds__(NW * 32)
       ldsm_x4_t(vb_a + hh * SM::kBoxBytes + swz(r, u), b00, b01, b10, b11);
       mma_bf16(o[j], pa, b00, b01);
       mma_bf16(o[j + 1], pa, b10, b11);
+      mma_bf16(o[j], pl, b00, b01);
+      mma_bf16(o[j + 1], pl, b10, b11);
     }
     // All lanes are done reading this stage before it is refilled; order the
     // generic-proxy accesses before the next async-proxy write.

@@ -99,6 +99,8 @@ def test_small_parity(torch_cuda, name, partition, decode_path):
 @pytest.mark.parametrize("name", ["llama7b_mha_bf16", "long_ctx_gqa4_bf16", "d64_bf16_g16_bs8_qf32"])
 def test_split_count_invariance(torch_cuda, name, decode_path):
     w, lens = SMALL[name]
+    if decode_path == "simt" and w.group > 8:
+        pytest.skip("the CUDA-core kernel is built for groups of 1, 2, 4 and 8")
     case, _ = GC.make_small(w, lens=lens)
     ref = None
     for part in (0, 64, 192, 4096):
