@@ -49,7 +49,9 @@ typedef enum {
   PKV_ERR_REFCOUNT = 4,       /* ref or free of a block whose count is 0 */
   PKV_ERR_UNSUPPORTED = 5,    /* head_dim / block_size / dtype / group not built */
   PKV_ERR_CUDA = 6,           /* a CUDA runtime call or launch failed */
-  PKV_ERR_HOST_MEMORY = 7     /* host allocation failed */
+  PKV_ERR_HOST_MEMORY = 7,    /* host allocation failed */
+  PKV_ERR_SCRATCH_LIMIT = 8   /* paged_attention_decode_noalloc: the request needs more
+                                 than PKV_NOALLOC_SCRATCH_BYTES of split-KV scratch */
 } pkv_status;
 
 /* Bits a kernel ORs into *device_status (when that pointer is non-null). */
@@ -236,6 +238,39 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   void* workspace, size_t workspace_bytes,
                                   int32_t partition_tokens, int32_t* device_status,
                                   pkv_stream_t stream);
+
+/* Size of the device scratch compiled into the library for
+ * paged_attention_decode_noalloc (held on every GPU that loads the library,
+ * until the process exits). */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* paged_attention_decode for callers that cannot allocate device memory.
+ * The source pages have no counterpart of this call; it exists for code that
+ * may not call cudaMalloc or any allocating routine - a plug-in inside a host
+ * program that owns every device allocation, a runtime that plans all of its
+ * memory once at start-up and forbids allocation on the per-token path, or a
+ * caller that cannot afford the device-wide synchronisation an allocation can
+ * cause.  Arguments and results are those of paged_attention_decode without
+ * the workspace: the split-KV partials go to a fixed device array inside the
+ * library, PKV_NOALLOC_SCRATCH_BYTES long.  The call allocates nothing.
+ *   - A request whose partials need more than PKV_NOALLOC_SCRATCH_BYTES
+ *     (paged_attention_workspace_bytes(...) of the same arguments) returns
+ *     PKV_ERR_SCRATCH_LIMIT without launching anything.
+ *   - All calls on a device share that array.  Calls whose kernels may overlap
+ *     on the GPU (different streams with no ordering between them) race on it
+ *     and can corrupt each other's outputs; calls on one stream are safe.
+ *   - The array keeps the previous call's contents; nothing in it needs to
+ *     start at zero, since a call writes every partial before reading it.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture begins. */
+pkv_status paged_attention_decode_noalloc(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
+    const float* v_scale, float* out, int32_t partition_tokens, int32_t* device_status,
+    pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Device: bandwidth reference kernels (the roofline denominators).          */

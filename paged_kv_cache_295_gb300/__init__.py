@@ -22,7 +22,8 @@ DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E4M3: "fp8_e4m3"}
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 STATUS = {0: "ok", 1: "invalid_arg", 2: "no_free_block", 3: "bad_block", 4: "refcount",
-          5: "unsupported", 6: "cuda", 7: "host_memory"}
+          5: "unsupported", 6: "cuda", 7: "host_memory", 8: "scratch_limit"}
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class PagedKVError(RuntimeError):
@@ -72,6 +73,8 @@ _SIGS = {
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "paged_attention_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32, I32, FL,
                                      I32, I32, P, P, P, P, SZ, I32, P, P]),
+    "paged_attention_decode_noalloc": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32,
+                                             I32, FL, I32, I32, P, P, P, I32, P, P]),
     "pkv_copy_kernel": (I32, [P, P, SZ, P]),
     "pkv_read_kernel": (I32, [P, SZ, P, P]),
     "pkv_read_kernel_sink_floats": (I32, []),
@@ -308,6 +311,23 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         _dev(workspace, "workspace") if workspace is not None else None, ws_bytes,
         int(partition), _dev(device_status, "device_status"), _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   max_context_len, out, k_scale=None, v_scale=None, partition=0,
+                                   device_status=None, stream=None):
+    """``paged_attention_decode`` into a caller-owned ``out`` with the library's
+    built-in split-KV scratch (no device allocation by the library or here)."""
+    S, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    st = library().paged_attention_decode_noalloc(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), S, hq, hkv, d,
+        bs, nb, block_tables.shape[1], int(max_context_len), float(scale), _dtype_code(q),
+        _dtype_code(k_cache), _dev(k_scale, "k_scale"), _dev(v_scale, "v_scale"),
+        _dev(out, "out"), int(partition), _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "paged_attention_decode_noalloc")
     return out
 
 

@@ -96,6 +96,7 @@ const char* pkv_status_string(int32_t st) {
     case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_HOST_MEMORY: return "host allocation failed";
+    case PKV_ERR_SCRATCH_LIMIT: return "request exceeds the library's built-in decode scratch";
     default: return "unknown status";
   }
 }
