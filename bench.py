@@ -208,6 +208,13 @@ def append_alg_bytes(w) -> int:
         w.num_seqs * 8
 
 
+def decode_kernel_name(w) -> str:
+    """The decode kernel the library picks for this workload's shape."""
+    tensor_core = (w.kv_dtype == "bf16" and w.head_dim in (64, 128) and w.group <= 16
+                   and w.block_size >= 8 and os.environ.get("PKV_DECODE_PATH") != "simt")
+    return "paged_decode_mma_kernel" if tensor_core else "paged_decode_kernel"
+
+
 # --------------------------------------------------- device-side workload ---
 class DeviceStep:
     """A decode step of workload ``w`` resident on one GPU, run through the C ABI."""
@@ -398,7 +405,7 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6800 GB/s",
-                     "kernel": "paged_decode_kernel" + (" + paged_decode_reduce_kernel"
+                     "kernel": decode_kernel_name(w) + (" + paged_decode_reduce_kernel"
                                                         if st.max_parts > 1 else ""),
                      "alg_bytes_per_launch": attn_bytes,
                      "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4) if bw else None,
