@@ -49,7 +49,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"sources_sha": "ac0f6f7be18391f7", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma_kernel 1.239609 GB read + 9.208 MB written, plus the
+               # reduce kernel's 1.433 MB (profiles/decode_mma_llama7b_bf16.md)
+               "bytes_per_launch": 1239609000 + 9208320 + 1433000}
 
 
 def parse_args(argv=None):
@@ -380,7 +383,9 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     achieved = attn_bytes / attn_avg / 1e9
     sha = kernel_sources_sha()
-    traffic = NCU_TRAFFIC.get("bytes_per_launch") if NCU_TRAFFIC.get("sources_sha") == sha else None
+    traffic = (NCU_TRAFFIC.get("bytes_per_launch")
+               if NCU_TRAFFIC.get("sources_sha") == sha and NCU_TRAFFIC.get("workload") == w.name
+               else None)
 
     e2e = run_e2e(st, args, dev, world)
     cpu = None
