@@ -222,7 +222,7 @@ def decode_kernel_name(w) -> str:
 class DeviceStep:
     """A decode step of workload ``w`` resident on one GPU, run through the C ABI."""
 
-    def __init__(self, w, device, partition=0, nsets=2):
+    def __init__(self, w, device, partition=0, nsets=2, keep_layers=()):
         import torch
         import paged_kv_cache_295_gb300 as pkv
         from paged_kv_cache_295_gb300.engine import PagedKVCache, build_prompts
@@ -235,6 +235,11 @@ class DeviceStep:
                                       initial_free_order=W.free_order(w, nb))
         _, slots, oslots = build_prompts(eng.pool, self.lens, w.prefix_tokens, w.prefix_seqs)
         prompt = np.concatenate(([oslots] if oslots is not None else []) + list(slots))
+        # rows of the prompt tensor: the prefix owner's first, then each sequence's own
+        self.owner_rows = (0, len(oslots)) if oslots is not None else None
+        starts = np.cumsum([0] + [len(x) for x in slots]) + (len(oslots) if oslots is not None else 0)
+        self.seq_rows = [(int(starts[i]), int(starts[i + 1])) for i in range(S)]
+        self.src = {}
         step_slots = eng.pool.append_slots(range(S))
         mb = int(max(len(eng.pool.block_table(s)) for s in range(S)))
         tables, lens_pool = eng.pool.batch_tables(list(range(S)), mb)
@@ -267,6 +272,8 @@ class DeviceStep:
                 eng.v_scale[layer] = torch.where(va > 0, va / 448.0, torch.ones_like(va))
             if prompt.size:
                 eng.append(layer, ks, vs, prompt_d)
+            if layer in keep_layers:   # kept for oracle checks of this layer
+                self.src[layer] = (ks, vs)
             del ks, vs
             self.q.append(q)
             self.kn.append(kn)
