@@ -213,9 +213,13 @@ def append_alg_bytes(w) -> int:
 
 def decode_kernel_name(w) -> str:
     """The decode kernel the library picks for this workload's shape."""
-    tensor_core = (w.kv_dtype == "bf16" and w.head_dim in (64, 128) and w.group <= 16
-                   and w.block_size >= 8 and os.environ.get("PKV_DECODE_PATH") != "simt")
-    return "paged_decode_mma_kernel" if tensor_core else "paged_decode_kernel"
+    if os.environ.get("PKV_DECODE_PATH") == "simt" or w.group > 16 or w.block_size < 8:
+        return "paged_decode_kernel"
+    if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
+        return "paged_decode_mma_kernel"
+    if w.kv_dtype == "fp8_e4m3" and w.head_dim == 128:
+        return "paged_decode_mma_fp8_kernel"
+    return "paged_decode_kernel"
 
 
 # --------------------------------------------------- device-side workload ---

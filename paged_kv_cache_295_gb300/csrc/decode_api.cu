@@ -192,6 +192,7 @@ extern "C" pkv_status paged_attention_decode(
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   if (use_mma)
-    return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32);
+    return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
+                             kv_dtype == PKV_FP8_E4M3);
   return fn(a);
 }

@@ -391,6 +391,6 @@ pkv_status launch_decode(const DecodeLaunch& a);
 bool mma_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                         int64_t num_blocks);
 pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                             int head_dim, int64_t num_blocks, bool q_f32);
+                             int head_dim, int64_t num_blocks, bool q_f32, bool fp8);
 
 }  // namespace pkv

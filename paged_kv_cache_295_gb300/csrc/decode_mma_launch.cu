@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "decode_mma.cuh"
+#include "decode_mma_fp8.cuh"
 
 namespace pkv {
 
@@ -26,20 +27,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over one layer's cache viewed as [rows = num_blocks*block_size]
-// [num_kv_heads][head_dim] of 16-bit elements; box = [box_rows][1][64],
-// 128-byte swizzle (the smem tile layout the ldmatrix addressing assumes).
+// [num_kv_heads][head_dim]; box = [box_rows][1][128 bytes of one row], 128-byte
+// swizzle (the smem tile layout the fragment addressing assumes).  16-bit
+// caches take two boxes per row (64 elements each), FP8 caches one.
 bool make_map(CUtensorMap* m, const void* base, int head_dim, int num_kv_heads, int64_t rows,
-              int box_rows) {
+              int box_rows, bool fp8) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t esz = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
                         static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                           static_cast<cuuint64_t>(head_dim) * 2 * num_kv_heads};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kMmaBoxCols), 1u, static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * esz,
+                           static_cast<cuuint64_t>(head_dim) * esz * num_kv_heads};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 1u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -77,12 +81,40 @@ pkv_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams&
   return PKV_OK;
 }
 
+// FP8 caches (head_dim 128): 4 KiB stages, six deep, two CTAs per SM.
+template <bool QF32, bool ROWS16>
+pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
+                      int num_seqs, cudaStream_t stream) {
+  constexpr int NW = 4, STAGES = 6;
+  using SM = MmaFp8Smem<NW, STAGES>;
+  const int bs = 1 << mp.p.bs_log2;
+  const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
+  const size_t smem = SM::bytes(table_entries);
+  auto kern = paged_decode_mma_fp8_kernel<QF32, ROWS16, NW, STAGES>;
+  static int configured = 0;
+  if (static_cast<int>(smem) > configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured = static_cast<int>(smem);
+  }
+  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
 }  // namespace
 
 bool mma_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                         int64_t num_blocks) {
-  if (kv_dtype != PKV_BF16) return false;
-  if (head_dim != 64 && head_dim != 128) return false;
+  if (kv_dtype == PKV_BF16) {
+    if (head_dim != 64 && head_dim != 128) return false;
+  } else if (kv_dtype == PKV_FP8_E4M3) {
+    if (head_dim != 128) return false;
+  } else {
+    return false;
+  }
   if (group < 1 || group > 16) return false;
   if (block_size < 8) return false;   // a TMA box is at least 8 rows (1 KiB)
   if (num_blocks * block_size > 0x7fffffffLL) return false;
@@ -90,18 +122,25 @@ bool mma_path_supported(int32_t kv_dtype, int head_dim, int group, int block_siz
 }
 
 pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                             int head_dim, int64_t num_blocks, bool q_f32) {
+                             int head_dim, int64_t num_blocks, bool q_f32, bool fp8) {
   const DecodeParams& p = a.p;
   const int bs = 1 << p.bs_log2;
   MmaParams mp{p, bs < kMmaChunk ? bs : kMmaChunk};
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * bs;
-  if (!make_map(&tk, k_cache, head_dim, p.num_kv_heads, rows, mp.box_rows) ||
-      !make_map(&tv, v_cache, head_dim, p.num_kv_heads, rows, mp.box_rows))
+  if (!make_map(&tk, k_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8) ||
+      !make_map(&tv, v_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8))
     return PKV_ERR_CUDA;
   const bool rows16 = p.num_q_heads / p.num_kv_heads > 8;
   pkv_status st;
-  if (head_dim == 128) {
+  if (fp8) {
+    if (q_f32)
+      st = rows16 ? launch_fp8<true, true>(tk, tv, mp, a.num_seqs, a.stream)
+                  : launch_fp8<true, false>(tk, tv, mp, a.num_seqs, a.stream);
+    else
+      st = rows16 ? launch_fp8<false, true>(tk, tv, mp, a.num_seqs, a.stream)
+                  : launch_fp8<false, false>(tk, tv, mp, a.num_seqs, a.stream);
+  } else if (head_dim == 128) {
     if (q_f32)
       st = rows16 ? launch<128, true, true>(tk, tv, mp, a.num_seqs, a.stream)
                   : launch<128, true, false>(tk, tv, mp, a.num_seqs, a.stream);

@@ -69,6 +69,10 @@ SMALL = {
                                                 seed=15, ctx_law="fixed"), [1, 33, 1000]),
     "d128_bf16_g16_bs16": (W.DecodeWorkload("g16b", 2, 16, 1, 128, 16, "bf16", "bf16",
                                             seed=16, ctx_law="fixed"), [15, 1200]),
+    "d128_fp8_g8_bs32_qf32": (W.DecodeWorkload("fp8g8", 3, 16, 2, 128, 32, "fp8_e4m3", "f32",
+                                               seed=17, ctx_law="fixed"), [2, 31, 900]),
+    "d128_fp8_g16_bs8": (W.DecodeWorkload("fp8g16", 2, 32, 2, 128, 8, "fp8_e4m3", "bf16",
+                                          seed=18, ctx_law="fixed"), [9, 1300]),
 }
 
 
