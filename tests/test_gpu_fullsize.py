@@ -94,6 +94,6 @@ def test_fullsize_sampled_parity(lib, name):
             print(f"fullsize {name} layer {layer} seq {s} ctx {L} max_abs_err {err:.3e}")
             checked += 1
             assert err <= TOL[w.kv_dtype], f"{name} layer {layer} seq {s} ctx {L}: {err}"
-    assert checked == len(layers) * len(seqs) >= 3
+    assert checked == len(layers) * len(seqs) >= min(3, w.num_seqs)
     del st
     torch.cuda.empty_cache()
