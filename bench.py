@@ -44,7 +44,7 @@ import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
-WORKLOADS = {w.name: w for w in W.ALL}
+WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA}
 DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,

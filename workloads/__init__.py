@@ -70,6 +70,13 @@ RAGGED_FP8 = DecodeWorkload("ragged_32layer_fp8", 256, 32, 32, 128, 16, FP8, BF1
                             ctx_hi=16384, pool_slack=1.25, prefix_tokens=2048,
                             prefix_seqs=128)
 ALL = (TINY, LLAMA7B_LAYER, LLAMA70B_GQA, LONG_CTX, RAGGED_FP8)
+# One layer of the ragged FP8 step (same per-layer shape; a few GB on the device),
+# for profiling runs.
+RAGGED_FP8_LAYER = DecodeWorkload("ragged_fp8_1layer", 256, 32, 32, 128, 16, FP8, BF16,
+                                  seed=4, num_layers=1, ctx_law="lognormal", ctx_lo=1,
+                                  ctx_hi=16384, pool_slack=1.25, prefix_tokens=2048,
+                                  prefix_seqs=128)
+EXTRA = (RAGGED_FP8_LAYER,)
 
 
 def rng(seed: int, stream: int = 0) -> np.random.Generator:
