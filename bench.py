@@ -213,8 +213,11 @@ def append_alg_bytes(w) -> int:
 
 def decode_kernel_name(w) -> str:
     """The decode kernel the library picks for this workload's shape."""
-    if os.environ.get("PKV_DECODE_PATH") == "simt" or w.group > 16 or w.block_size < 8:
+    forced = os.environ.get("PKV_DECODE_PATH")
+    if forced == "simt" or w.group > 16 or w.block_size < 8:
         return "paged_decode_kernel"
+    if forced != "mma" and w.kv_dtype == "bf16" and w.head_dim == 128:
+        return "paged_decode_tc_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
         return "paged_decode_mma_kernel"
     if w.kv_dtype == "fp8_e4m3" and w.head_dim == 128:

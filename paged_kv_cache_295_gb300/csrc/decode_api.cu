@@ -31,12 +31,14 @@ namespace {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
-// PKV_DECODE_PATH=simt forces the CUDA-core kernel where the tensor-core one
-// would run (used by the tests to check both paths on the same inputs).
-bool force_simt() {
+// PKV_DECODE_PATH=simt forces the CUDA-core kernel and PKV_DECODE_PATH=mma the
+// mma.sync kernel where a newer one would run (the tests check every kernel on
+// the same inputs); unset, the tcgen05 kernel runs wherever it applies.
+bool force_path(const char* name) {
   const char* v = std::getenv("PKV_DECODE_PATH");
-  return v && std::strcmp(v, "simt") == 0;
+  return v && std::strcmp(v, name) == 0;
 }
+bool force_simt() { return force_path("simt"); }
 
 int log2i(int64_t x) {
   int r = 0;
@@ -143,10 +145,12 @@ extern "C" pkv_status paged_attention_decode(
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
+  const bool use_tc = !force_simt() && !force_path("mma") &&
+                      tc_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   const bool use_mma =
-      !force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
+      !use_tc && !force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   LaunchFn fn = pick(kv_dtype, head_dim, G);
-  if (!use_mma && !fn) return PKV_ERR_UNSUPPORTED;
+  if (!use_tc && !use_mma && !fn) return PKV_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
@@ -191,6 +195,7 @@ extern "C" pkv_status paged_attention_decode(
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc) return launch_decode_tc(a, k_cache, v_cache, num_blocks, q_dtype == PKV_F32);
   if (use_mma)
     return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
                              kv_dtype == PKV_FP8_E4M3);

@@ -6,6 +6,7 @@
 
 #include "decode_mma.cuh"
 #include "decode_mma_fp8.cuh"
+#include "decode_tc.cuh"
 
 namespace pkv {
 
@@ -104,7 +105,58 @@ pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPar
   return PKV_OK;
 }
 
+// tcgen05 path (bf16, head_dim 128): one warp per CTA, 3 TMA stages of 64-token tiles.
+template <bool QF32>
+pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
+                     int num_seqs, cudaStream_t stream) {
+  constexpr int STAGES = 3;
+  const int bs = 1 << mp.p.bs_log2;
+  const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
+  const size_t smem = TcLayout::bytes(STAGES, table_entries);
+  auto kern = paged_decode_tc_kernel<QF32, STAGES>;
+  static int configured = 0;
+  if (static_cast<int>(smem) > configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured = static_cast<int>(smem);
+  }
+  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  kern<<<grid, 32, smem, stream>>>(tk, tv, mp);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
 }  // namespace
+
+bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
+                       int64_t num_blocks) {
+  if (kv_dtype != PKV_BF16 || head_dim != kTcD) return false;
+  if (group < 1 || group > 16) return false;
+  if (block_size < 8) return false;
+  if (num_blocks * block_size > 0x7fffffffLL) return false;
+  return encode_fn() != nullptr;
+}
+
+pkv_status launch_decode_tc(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
+                            int64_t num_blocks, bool q_f32) {
+  const DecodeParams& p = a.p;
+  const int bs = 1 << p.bs_log2;
+  MmaParams mp{p, bs < kTcTile ? bs : kTcTile};
+  CUtensorMap tk, tv;
+  const int64_t rows = num_blocks * bs;
+  if (!make_map(&tk, k_cache, kTcD, p.num_kv_heads, rows, mp.box_rows, false) ||
+      !make_map(&tv, v_cache, kTcD, p.num_kv_heads, rows, mp.box_rows, false))
+    return PKV_ERR_CUDA;
+  const pkv_status st = q_f32 ? launch_tc<true>(tk, tv, mp, a.num_seqs, a.stream)
+                              : launch_tc<false>(tk, tv, mp, a.num_seqs, a.stream);
+  if (st != PKV_OK) return st;
+  if (p.max_parts > 1) {
+    paged_decode_reduce_kernel<kTcD><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
 
 bool mma_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                         int64_t num_blocks) {

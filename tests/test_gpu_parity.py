@@ -76,14 +76,15 @@ SMALL = {
 }
 
 
-@pytest.fixture(params=["auto", "simt"])
+@pytest.fixture(params=["auto", "mma", "simt"])
 def decode_path(request, monkeypatch):
-    """'auto' = the library's own kernel choice (tensor-core path for 16-bit
-    caches it supports); 'simt' forces the CUDA-core kernel everywhere."""
-    if request.param == "simt":
-        monkeypatch.setenv("PKV_DECODE_PATH", "simt")
-    else:
+    """'auto' = the library's own kernel choice (tcgen05 where it applies);
+    'mma' forces the mma.sync kernels where they apply; 'simt' forces the
+    CUDA-core kernel everywhere."""
+    if request.param == "auto":
         monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
+    else:
+        monkeypatch.setenv("PKV_DECODE_PATH", request.param)
     return request.param
 
 
