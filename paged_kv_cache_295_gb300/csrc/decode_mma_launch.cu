@@ -105,7 +105,7 @@ pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPar
   return PKV_OK;
 }
 
-// tcgen05 path (bf16, head_dim 128): one warp per CTA, 3 TMA stages of 64-token tiles.
+// tcgen05 path (bf16, head_dim 128): 4 warps per CTA, 3 TMA stages of 64-token tiles.
 template <bool QF32>
 pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
                      int num_seqs, cudaStream_t stream) {
@@ -122,7 +122,7 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
     configured = static_cast<int>(smem);
   }
   dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
-  kern<<<grid, 32, smem, stream>>>(tk, tv, mp);
+  kern<<<grid, kTcThreads, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -1,33 +1,32 @@
 // PagedAttention decode on the 5th-generation tensor cores (tcgen05 + TMEM),
 // 16-bit caches, head_dim 128.
 //
-// Work split: one CTA (one warp) per sequence x KV head x split-KV partition,
+// Work split: one CTA (4 warps) per sequence x KV head x split-KV partition,
 // walking the partition in 64-token tiles that arrive by TMA through the
 // block table ("nano-vLLM architecture" section 4.2: attention addressed
 // through the logical -> physical block mapping).  Two CTAs share an SM.
 //
-// Per tile (heads as the MMA's M dimension, "LLM inference tutorial" section
-// 4.4 GQA: the G query heads of a KV head share every K/V byte):
-//   S[h][t]  = sum_d Q[h][d] K[t][d]        tcgen05.mma M=128 N=64  K=128
-//              A = Q rows in smem (K-major), B = the K tile (K-major, TMA layout),
-//              accumulator in TMEM (lane h, column t).
-//   softmax  : lane h of the warp reads its row of S (64 values), scales by
-//              scale*log2(e), masks tokens past the context, and keeps a
-//              running max / sum (base 2).  The running max only moves when a
-//              tile's max exceeds it by more than 2^8, so O is rarely rescaled
-//              (the final division by the sum uses the same max, so the result
-//              is unchanged).  P = 2^(s - m) is written to smem as bf16 hi + lo
-//              parts (~2^-17 relative).
-//   O[h][d] += sum_t P[h][t] V[t][d]        tcgen05.mma M=128 N=128 K=64 (x2: hi, lo)
-//              A = P (K-major), B = the V tile as stored (MN-major),
-//              accumulator in TMEM (lane h, column d), kept across tiles.
-// Only rows h < G are real; rows G..127 of A read other shared memory and
-// produce ignored accumulator rows.
+// Per tile, tokens are the MMA rows and the G query heads of the KV head the
+// columns ("LLM inference tutorial" section 4.4 GQA: the G heads share every
+// K/V byte, read once):
+//   S^T[t][h] = sum_d K[t][d] Q[h][d]         tcgen05.mma M=64  N=16 K=128
+//               A = the K tile as stored (K-major), B = Q (K-major, 16 rows),
+//               accumulator in TMEM: token t in lane 32*(t/16) + t%16.
+//   softmax   : the thread of token t scales its G logits by scale*log2(e),
+//               masks it if outside the context, and the CTA takes each
+//               head's tile max (warp shuffles + one shared exchange).  The
+//               running max only moves when a tile max exceeds it by more than
+//               2^8, so O is rarely rescaled (the final division by the sum
+//               uses the same max, so the result is unchanged).  P = 2^(s - m)
+//               goes to smem transposed, as bf16 hi + lo parts (~2^-17).
+//   O^T[d][h] += sum_t V[t][d] P[h][t]         tcgen05.mma M=128 N=16 K=64 (x2: hi, lo)
+//               A = the V tile as stored (MN-major), B = P^T (K-major),
+//               accumulator in TMEM: dimension d in lane d, kept across tiles.
 //
-// Overlap: QK of tile i+1 is issued before the softmax of tile i; the TMA ring
-// keeps STAGES tiles in flight; PV(i-1) is waited on only when its P buffer and
-// stage are needed again.  Every mbarrier wait is bounded (2 s) and reports
-// PKV_DEV_TIMEOUT; TMEM is always released before the CTA exits.
+// Overlap: QK of tile i+1 is issued as soon as every warp has read S(i); the
+// TMA ring keeps STAGES tiles in flight; PV(i-1) is waited on only when P, O or
+// its stage are needed again.  Every mbarrier wait is bounded (2 s) and
+// reports PKV_DEV_TIMEOUT; TMEM is always released before the CTA exits.
 #pragma once
 
 #include <cuda.h>
@@ -36,11 +35,12 @@
 
 namespace pkv {
 
-constexpr int kTcTile = 64;   // tokens per tile (MMA N of QK, K of PV)
+constexpr int kTcTile = 64;   // tokens per tile (MMA M of QK, K of PV)
 constexpr int kTcD = 128;
 
 struct TcLayout {
-  // [Q hi 4K][Q lo 4K][P hi 2K][P lo 2K][stages ...][table]; 1024-aligned blocks
+  // [Q hi 4K][Q lo 4K][P^T hi 2K][P^T lo 2K][stages ...][table]; 1024-aligned blocks.
+  // Q: [16 heads][128 d] as two [16][128 B] halves; P^T: [16 heads][64 tokens].
   static constexpr int kQ = 0, kQlo = 4096, kP = 8192, kPlo = 10240, kStages = 12288;
   static constexpr int kHalf = kTcTile * 128;          // [64 rows][128 B] = 8 KB
   static constexpr int kStage = 4 * kHalf;              // K (2 halves) + V (2 halves)
@@ -88,6 +88,35 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
 
+// 16 consecutive TMEM columns of this warp's 32 lanes -> 16 registers.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};\n" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
 // 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -128,11 +157,14 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
 
 namespace pkv {
 
+constexpr int kTcThreads = 128;
+
 template <bool QF32, int STAGES>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kTcThreads)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const MmaParams mp) {
   using LY = TcLayout;
+  constexpr int GMAX = 16;
   const DecodeParams& p = mp.p;
   const int G = p.num_q_heads / p.num_kv_heads;
 
@@ -141,36 +173,37 @@ __global__ void __launch_bounds__(32)
   __shared__ __align__(8) uint64_t bar_s[2];
   __shared__ __align__(8) uint64_t bar_o;
   __shared__ uint32_t tmem_base_sh;
+  __shared__ float red[4][GMAX];
+  __shared__ int ok_sh;
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sma = smem_u32(sm);
 
   const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_tokens;
 
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);
   if (ctx < 0 || ctx > cap) {
-    if (part == 0 && lane == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    if (part == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
     ctx = ctx < 0 ? 0 : cap;
   }
   const int nparts = (ctx + P - 1) / P;
   if (part >= (nparts > 0 ? nparts : 1)) return;
   const int hq0 = g * G;
   if (ctx == 0) {
-    for (int i = lane; i < G * kTcD; i += 32)
+    for (int i = tid; i < G * kTcD; i += kTcThreads)
       p.out[(static_cast<int64_t>(s) * p.num_q_heads + hq0) * kTcD + i] = 0.f;
     return;
   }
   const int t_begin = part * P;
   const int t_end = min(t_begin + P, ctx);
 
-  // block-table entries of the partition
   int32_t* sbt = reinterpret_cast<int32_t*>(sm + LY::kStages + STAGES * LY::kStage);
   const int lb0 = t_begin >> p.bs_log2;
   const int nlb = ((t_end - 1) >> p.bs_log2) - lb0 + 1;
   const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
-  for (int i = lane; i < nlb; i += 32) {
+  for (int i = tid; i < nlb; i += kTcThreads) {
     int32_t b = __ldg(bt_row + lb0 + i);
     if (b < 0 || b >= p.num_blocks) {
       flag_status(p.status, PKV_DEV_BAD_BLOCK);
@@ -178,10 +211,10 @@ __global__ void __launch_bounds__(32)
     }
     sbt[i] = b;
   }
-  // query rows (A operand of QK): 16 rows x 128 dims, bf16 hi (+ lo for float32 q)
+  // Q (B operand of QK): 16 rows x 128 dims, bf16 hi (+ lo for float32 q); P^T rows >= G zeroed
   {
     const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + hq0;
-    for (int i = lane; i < 16 * 16; i += 32) {
+    for (int i = tid; i < GMAX * 16; i += kTcThreads) {
       const int h = i >> 4, u = i & 15, hh = u >> 3, uu = u & 7;
       uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
       if (h < G) {
@@ -206,48 +239,40 @@ __global__ void __launch_bounds__(32)
       }
       *reinterpret_cast<uint4*>(sm + LY::kQ + hh * 2048 + swz(h, uu)) = hi;
       if (QF32) *reinterpret_cast<uint4*>(sm + LY::kQlo + hh * 2048 + swz(h, uu)) = lo;
+      if (hh == 0) {   // P^T rows: zero (rows >= G stay zero for the whole CTA)
+        *reinterpret_cast<uint4*>(sm + LY::kP + swz(h, uu)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + LY::kPlo + swz(h, uu)) = make_uint4(0, 0, 0, 0);
+      }
     }
   }
-  if (lane == 0) {
+  if (tid == 0) {
     for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&full[st]), 1);
     mbar_init(smem_u32(&bar_s[0]), 1);
     mbar_init(smem_u32(&bar_s[1]), 1);
     mbar_init(smem_u32(&bar_o), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  __syncwarp();
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(
-                   smem_u32(&tmem_base_sh))
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 64;\n" ::"r"(
+                     smem_u32(&tmem_base_sh))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
   fence_proxy_async();
   tc_fence_before();
-  __syncwarp();
+  __syncthreads();
   tc_fence_after();
-  const uint32_t tm = tmem_base_sh;        // S buffers at +0 / +64, O at +128
-  const uint32_t tmO = tm + 128;
+  const uint32_t tm = tmem_base_sh;          // S^T buffers at columns 0 / 16, O^T at 32
+  const uint32_t lane_q = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
+  const uint32_t tmO = tm + 32;
 
   const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
   const int box_rows = mp.box_rows;
   const int nbox = kTcTile / box_rows;
-  const uint32_t idesc_qk = tc_idesc(128, kTcTile, false, false, true);
-  const uint32_t idesc_pv = tc_idesc(128, kTcD, false, true, true);
+  const uint32_t idesc_qk = tc_idesc(kTcTile, GMAX, false, false, true);
+  const uint32_t idesc_pv = tc_idesc(kTcD, GMAX, true, false, true);
 
-  // Rows of tile j that hold cache data (inside the context, valid block id).
-  auto filled_rows = [&](int j) -> uint64_t {
-    const int t0 = t_begin + j * kTcTile;
-    uint64_t mask = 0;
-    for (int bx = 0; bx < nbox; ++bx) {
-      const int tb = t0 + bx * box_rows;
-      if (tb >= ctx) break;
-      if (sbt[(tb >> p.bs_log2) - lb0] < 0) continue;
-      const int rows = min(box_rows, ctx - tb);
-      const uint64_t bits = rows >= 64 ? ~0ull : ((1ull << rows) - 1);
-      mask |= bits << (bx * box_rows);
-    }
-    return mask;
-  };
-  auto issue_tma = [&](int j) {   // lane 0
+  auto issue_tma = [&](int j) {   // thread 0
     const int stage = j % STAGES;
     const int t0 = t_begin + j * kTcTile;
     const uint32_t bar = smem_u32(&full[stage]);
@@ -273,187 +298,212 @@ __global__ void __launch_bounds__(32)
       }
     }
   };
-  auto issue_qk = [&](int j) {    // lane 0, tile j landed
+  auto issue_qk = [&](int j) {    // thread 0, tile j landed
     const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
-    const uint32_t dst = tm + (j & 1) * kTcTile;
+    const uint32_t dst = tm + (j & 1) * GMAX;
 #pragma unroll
     for (int ks = 0; ks < kTcD / 16; ++ks) {
       const uint32_t koff = (ks >> 2) * LY::kHalf + (ks & 3) * 32;
       const uint32_t qoff = (ks >> 2) * 2048 + (ks & 3) * 32;
-      const uint64_t bdesc = tc_desc(kb + koff, 0, 1024);
-      tc_mma(dst, tc_desc(sma + LY::kQ + qoff, 0, 1024), bdesc, idesc_qk, ks > 0);
-      if (QF32) tc_mma(dst, tc_desc(sma + LY::kQlo + qoff, 0, 1024), bdesc, idesc_qk, 1);
+      const uint64_t adesc = tc_desc(kb + koff, 0, 1024);
+      tc_mma(dst, adesc, tc_desc(sma + LY::kQ + qoff, 0, 1024), idesc_qk, ks > 0);
+      if (QF32) tc_mma(dst, adesc, tc_desc(sma + LY::kQlo + qoff, 0, 1024), idesc_qk, 1);
     }
     tc_commit(smem_u32(&bar_s[j & 1]));
   };
+  // all threads take one thread's verdict (a failed wait ends the tile loop)
+  auto agree = [&](bool ok_local, int who) -> bool {
+    if (tid == who) ok_sh = ok_local ? 1 : 0;
+    __syncthreads();
+    const bool r = ok_sh != 0;
+    __syncthreads();
+    return r;
+  };
 
-  if (lane == 0)
-    for (int j = 0; j < min(STAGES, ntiles); ++j) issue_tma(j);
   bool alive = true;
   {
     bool ok = true;
-    if (lane == 0) {
+    if (tid == 0) {
+      for (int j = 0; j < min(STAGES, ntiles); ++j) issue_tma(j);
       ok = mbar_wait(smem_u32(&full[0]), 0);
       if (ok) issue_qk(0);
     }
-    alive = __shfl_sync(0xffffffffu, ok, 0);
+    alive = agree(ok, 0);
   }
-  int qk_issued = 1, pv_issued = 0;   // for the bounded drain after a timeout
+  int qk_issued = 1, pv_issued = 0;
 
-  float m = -CUDART_INF_F, l = 0.f;
-  const bool row_real = lane < G;
+  // per-thread state: token row t = 16*warp + lane (lanes < 16), heads in registers
+  const bool tok_lane = lane < 16;
+  const int tloc = 16 * warp + lane;
+  float m[GMAX], lpart[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    m[h] = -CUDART_INF_F;
+    lpart[h] = 0.f;
+  }
   const float sl2 = p.qk_scale_log2;
+
   for (int i = 0; i < ntiles && alive; ++i) {
-    // (a) logits of tile i
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[i & 1]), (i >> 1) & 1))) {
+    const int t0 = t_begin + i * kTcTile;
+    const int tb = t0 + tloc;
+    const bool filled = tok_lane && tb < ctx && sbt[(tb >> p.bs_log2) - lb0] >= 0;
+    // (1) S^T(i): this thread's token, G logits
+    const bool sok = mbar_wait(smem_u32(&bar_s[i & 1]), (i >> 1) & 1);
+    tc_fence_after();
+    float sv[GMAX];
+    tc_ld16(tm + lane_q + (i & 1) * GMAX, sv);
+    // (2) per-head tile max: warp (16 token lanes) then across the 4 warps
+    float mx[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      sv[h] = (filled && h < G) ? sv[h] * sl2 : -CUDART_INF_F;
+      mx[h] = sv[h];
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) red[warp][h] = mx[h];
+    }
+    tc_fence_before();
+    if (!agree(sok, 0)) {   // (also the barrier after which S(i) has been read by all)
       alive = false;
       break;
     }
-    tc_fence_after();
-    float sv[kTcTile];
-    tc_ld32(tm + (i & 1) * kTcTile, sv);
-    tc_ld32(tm + (i & 1) * kTcTile + 32, sv + 32);
-    tc_fence_before();
-    __syncwarp();
-    // (b) QK of tile i+1 overlaps this tile's softmax
+    // (3) QK(i+1) overlaps the rest of this tile
     if (i + 1 < ntiles) {
       bool ok = true;
-      if (lane == 0) {
+      if (tid == 0) {
         tc_fence_after();
         ok = mbar_wait(smem_u32(&full[(i + 1) % STAGES]), ((i + 1) / STAGES) & 1);
         if (ok) issue_qk(i + 1);
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        alive = false;
-        break;
-      }
       ++qk_issued;
+      if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
     }
-    // (c) softmax of tile i (row = lane)
-    const uint64_t fmask = filled_rows(i);
-    float mt = -CUDART_INF_F;
-#pragma unroll
-    for (int t = 0; t < kTcTile; ++t) {
-      sv[t] = ((fmask >> t) & 1) ? sv[t] * sl2 : -CUDART_INF_F;
-      mt = fmaxf(mt, sv[t]);
-    }
+    // (4) running max (lazy), probabilities, partial sums
     bool resc = false;
-    float alpha = 1.f;
-    if (row_real && mt > m + 8.f) {
-      if (m != -CUDART_INF_F) {
-        alpha = exp2f(m - mt);
-        resc = true;
-      }
-      m = mt;
-      l *= alpha;
-    }
-    const float mref = row_real ? m : 0.f;
-    float lsum = 0.f;
+    float alpha[GMAX];
 #pragma unroll
-    for (int t = 0; t < kTcTile; ++t) {
-      sv[t] = exp2f(sv[t] - mref);
-      lsum += sv[t];
+    for (int h = 0; h < GMAX; ++h) {
+      const float mt = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
+      alpha[h] = 1.f;
+      if (h < G && mt > m[h] + 8.f) {
+        if (m[h] != -CUDART_INF_F) {
+          alpha[h] = exp2f(m[h] - mt);
+          resc = true;
+        }
+        m[h] = mt;
+      }
+      const float pr = (h < G && filled) ? exp2f(sv[h] - m[h]) : 0.f;
+      lpart[h] = lpart[h] * alpha[h] + pr;
+      sv[h] = pr;
     }
-    if (row_real) l += lsum;
-    // (d) PV(i-1) done: its P buffer, O and its stage are free again
+    // (5) PV(i-1) done: O, P^T and the stage of tile i-1 are free
     if (i > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o), (i - 1) & 1))) {
-        alive = false;
-        break;
+      const bool ok = mbar_wait(smem_u32(&bar_o), (i - 1) & 1);
+      if (!ok) {
+        if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+        alive = false;   // every thread sees the same barrier; the vote below settles it
       }
       tc_fence_after();
-      if (lane == 0 && i - 1 + STAGES < ntiles) issue_tma(i - 1 + STAGES);
+      if (tid == 0 && ok && i - 1 + STAGES < ntiles) issue_tma(i - 1 + STAGES);
     }
-    // (e) rare rescale of the O rows whose max moved
-    if (__any_sync(0xffffffffu, resc)) {
+    // (6) rare rescale of O^T columns (this thread's lane = dimension d)
+    if (__syncthreads_or(resc)) {
+      float ov[GMAX];
+      tc_ld16(tmO + lane_q, ov);
 #pragma unroll
-      for (int c = 0; c < kTcD; c += 32) {
-        float ov[32];
-        tc_ld32(tmO + c, ov);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-        tc_st32(tmO + c, ov);
-      }
+      for (int h = 0; h < GMAX; ++h) ov[h] *= alpha[h];
+      tc_st16(tmO + lane_q, ov);
     }
-    // (f) P of tile i into smem (rows < 16), zero V rows that hold no cache data
-    if (lane < 16) {
+    // (7) P^T(i) -> smem (bf16 hi + lo); V rows without cache data -> 0
+    if (tok_lane) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float x0 = sv[8 * u + 2 * k], x1 = sv[8 * u + 2 * k + 1];
-          wh[k] = pack_bf16(x0, x1);
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&wh[k]);
-          wl[k] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
+      for (int h = 0; h < GMAX; ++h) {
+        if (h < G) {
+          const __nv_bfloat16 hv = __float2bfloat16_rn(sv[h]);
+          const __nv_bfloat16 lv = __float2bfloat16_rn(sv[h] - __bfloat162float(hv));
+          const uint32_t off = h * 128 + ((((tloc >> 3) ^ (h & 7))) << 4) + (tloc & 7) * 2;
+          *reinterpret_cast<__nv_bfloat16*>(sm + LY::kP + off) = hv;
+          *reinterpret_cast<__nv_bfloat16*>(sm + LY::kPlo + off) = lv;
         }
-        *reinterpret_cast<uint4*>(sm + LY::kP + swz(lane, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(sm + LY::kPlo + swz(lane, u)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
-    }
-    if (fmask != ~0ull) {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[i % STAGES]), (i / STAGES) & 1))) {
-        alive = false;
-        break;
-      }
-      uint8_t* vbase = sm + LY::kStages + (i % STAGES) * LY::kStage + 2 * LY::kHalf;
-      for (int k = lane; k < kTcTile * 16; k += 32) {
-        const int r = k >> 4, hh = (k >> 3) & 1;
-        if (!((fmask >> r) & 1))
-          *reinterpret_cast<uint4*>(vbase + hh * LY::kHalf + r * 128 + ((k & 7) << 4)) =
-              make_uint4(0, 0, 0, 0);
+      if (!filled) {
+        uint8_t* vrow = sm + LY::kStages + (i % STAGES) * LY::kStage + 2 * LY::kHalf + tloc * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          *reinterpret_cast<uint4*>(vrow + (u << 4)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + LY::kHalf + (u << 4)) = make_uint4(0, 0, 0, 0);
+        }
       }
     }
     fence_proxy_async();
     tc_fence_before();
-    __syncwarp();
-    // (g) O += P V
-    if (lane == 0) {
+    if (!__syncthreads_and(alive)) {
+      alive = false;
+      break;
+    }
+    // (8) O^T += V^T P^T
+    if (tid == 0) {
       tc_fence_after();
       const uint32_t vb = sma + LY::kStages + (i % STAGES) * LY::kStage + 2 * LY::kHalf;
 #pragma unroll
       for (int kk = 0; kk < kTcTile / 16; ++kk) {
-        const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kHalf, 1024);
-        tc_mma(tmO, tc_desc(sma + LY::kP + kk * 32, 0, 1024), bdesc, idesc_pv, (i > 0 || kk > 0));
-        tc_mma(tmO, tc_desc(sma + LY::kPlo + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+        const uint64_t adesc = tc_desc(vb + kk * 2048, LY::kHalf, 1024);
+        tc_mma(tmO, adesc, tc_desc(sma + LY::kP + kk * 32, 0, 1024), idesc_pv, (i > 0 || kk > 0));
+        tc_mma(tmO, adesc, tc_desc(sma + LY::kPlo + kk * 32, 0, 1024), idesc_pv, 1);
       }
       tc_commit(smem_u32(&bar_o));
     }
     ++pv_issued;
-    __syncwarp();
   }
 
-  float res[kTcD];
+  // ---- epilogue: O^T (lane d) / l[h] ------------------------------------------------
+  float ov[GMAX];
   bool have = false;
   if (alive && pv_issued > 0) {
-    have = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o), (pv_issued - 1) & 1));
+    have = __syncthreads_and(mbar_wait(smem_u32(&bar_o), (pv_issued - 1) & 1));
     if (have) {
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kTcD; c += 32) tc_ld32(tmO + c, res + c);
+      tc_ld16(tmO + lane_q, ov);
     }
   }
   if (!alive || !have) {
-    if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
-    // bounded drain of the last issued tensor-core work before TMEM is released
+    if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
     if (pv_issued > 0) mbar_wait(smem_u32(&bar_o), (pv_issued - 1) & 1);
     if (qk_issued > 0) mbar_wait(smem_u32(&bar_s[(qk_issued - 1) & 1]), ((qk_issued - 1) >> 1) & 1);
   }
+  // l[h]: sum of the token threads' partial sums
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    float v = tok_lane ? lpart[h] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) red[warp][h] = v;
+  }
   tc_fence_before();
-  __syncwarp();
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tm) : "memory");
-
-  if (!row_real) return;
-  const int64_t sh = static_cast<int64_t>(s) * p.num_q_heads + hq0 + lane;
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;\n" ::"r"(tm) : "memory");
   const bool ok_out = alive && have;
-  if (nparts == 1) {
-    const float inv = ok_out ? 1.f / l : 0.f;
-    for (int d = 0; d < kTcD; ++d) p.out[sh * kTcD + d] = ok_out ? res[d] * inv : 0.f;
-  } else {
-    const int64_t pi = sh * p.max_parts + part;
-    for (int d = 0; d < kTcD; ++d) p.part_o[pi * kTcD + d] = ok_out ? res[d] : 0.f;
-    p.part_ml[pi * 2 + 0] = ok_out ? m : -CUDART_INF_F;
-    p.part_ml[pi * 2 + 1] = ok_out ? l : 0.f;
+  const int d = tid;   // O^T lane = dimension
+  const int64_t sh0 = static_cast<int64_t>(s) * p.num_q_heads + hq0;
+  for (int h = 0; h < G; ++h) {
+    const float L = red[0][h] + red[1][h] + red[2][h] + red[3][h];
+    const float o = ok_out ? ov[h] : 0.f;
+    if (nparts == 1) {
+      p.out[(sh0 + h) * kTcD + d] = ok_out ? o / L : 0.f;
+    } else {
+      const int64_t pi = (sh0 + h) * p.max_parts + part;
+      p.part_o[pi * kTcD + d] = o;
+      if (d == 0) {
+        p.part_ml[pi * 2 + 0] = ok_out ? m[h] : -CUDART_INF_F;
+        p.part_ml[pi * 2 + 1] = ok_out ? L : 0.f;
+      }
+    }
   }
 }
 
