@@ -216,7 +216,7 @@ def decode_kernel_name(w) -> str:
     forced = os.environ.get("PKV_DECODE_PATH")
     if forced == "simt" or w.group > 16 or w.block_size < 8:
         return "paged_decode_kernel"
-    if forced != "mma" and w.kv_dtype == "bf16" and w.head_dim == 128:
+    if forced == "tc" and w.kv_dtype == "bf16" and w.head_dim == 128:
         return "paged_decode_tc_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
         return "paged_decode_mma_kernel"

@@ -31,9 +31,11 @@ namespace {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
-// PKV_DECODE_PATH=simt forces the CUDA-core kernel and PKV_DECODE_PATH=mma the
-// mma.sync kernel where a newer one would run (the tests check every kernel on
-// the same inputs); unset, the tcgen05 kernel runs wherever it applies.
+// Kernel choice.  Unset, the mma.sync tensor-core kernels run wherever they
+// apply (the fastest measured so far), else the CUDA-core kernel.
+// PKV_DECODE_PATH=tc selects the tcgen05 kernel where it applies,
+// PKV_DECODE_PATH=simt forces the CUDA-core kernel; the tests check every
+// kernel on the same inputs.
 bool force_path(const char* name) {
   const char* v = std::getenv("PKV_DECODE_PATH");
   return v && std::strcmp(v, name) == 0;
@@ -145,8 +147,8 @@ extern "C" pkv_status paged_attention_decode(
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  const bool use_tc = !force_simt() && !force_path("mma") &&
-                      tc_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
+  const bool use_tc =
+      force_path("tc") && tc_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   const bool use_mma =
       !use_tc && !force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   LaunchFn fn = pick(kv_dtype, head_dim, G);

@@ -76,10 +76,10 @@ SMALL = {
 }
 
 
-@pytest.fixture(params=["auto", "mma", "simt"])
+@pytest.fixture(params=["auto", "tc", "simt"])
 def decode_path(request, monkeypatch):
-    """'auto' = the library's own kernel choice (tcgen05 where it applies);
-    'mma' forces the mma.sync kernels where they apply; 'simt' forces the
+    """'auto' = the library's own kernel choice (mma.sync where it applies);
+    'tc' selects the tcgen05 kernel where it applies; 'simt' forces the
     CUDA-core kernel everywhere."""
     if request.param == "auto":
         monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
