@@ -1,10 +1,14 @@
 // PagedAttention decode on the 5th-generation tensor cores (tcgen05 + TMEM),
 // 16-bit caches, head_dim 128.
 //
-// Work split: one CTA (4 warps) per sequence x KV head x split-KV partition,
-// walking the partition in 64-token tiles that arrive by TMA through the
-// block table ("nano-vLLM architecture" section 4.2: attention addressed
-// through the logical -> physical block mapping).  Two CTAs share an SM.
+// Work split: one CTA per sequence x KV head x split-KV partition, walking the
+// partition in 64-token tiles that arrive by TMA through the block table
+// ("nano-vLLM architecture" section 4.2: attention addressed through the
+// logical -> physical block mapping).  Two CTAs share an SM.  Warp roles:
+// warps 0-3 softmax and epilogue (one TMEM lane quarter each), warp 4 TMA
+// producer (its lanes issue a tile's boxes in parallel), warp 5 MMA issuer.
+// The roles talk only through mbarriers, so the issue latencies of TMA and
+// tcgen05.mma overlap each other and the softmax.
 //
 // Per tile, tokens are the MMA rows and the G query heads of the KV head the
 // columns ("LLM inference tutorial" section 4.4 GQA: the G heads share every
@@ -23,10 +27,13 @@
 //               A = the V tile as stored (MN-major), B = P^T (K-major),
 //               accumulator in TMEM: dimension d in lane d, kept across tiles.
 //
-// Overlap: QK of tile i+1 is issued as soon as every warp has read S(i); the
-// TMA ring keeps STAGES tiles in flight; PV(i-1) is waited on only when P, O or
-// its stage are needed again.  Every mbarrier wait is bounded (2 s) and
-// reports PKV_DEV_TIMEOUT; TMEM is always released before the CTA exits.
+// Pipeline per tile j: producer loads stage j%STAGES once PV(j-STAGES) has
+// released it; the MMA warp issues QK(j) when the tile has landed and the S
+// buffer j%2 has been read, then PV(j-1) when its P^T is written; softmax warps
+// read S(j), write P^T(j) into buffer j%2 (after PV(j-2) finished with it).
+// Every mbarrier wait is bounded (2 s) and also stops when another role has
+// given up (shared abort flag); a give-up reports PKV_DEV_TIMEOUT.  TMEM is
+// always released before the CTA exits.
 #pragma once
 
 #include <cuda.h>
@@ -39,9 +46,10 @@ constexpr int kTcTile = 64;   // tokens per tile (MMA M of QK, K of PV)
 constexpr int kTcD = 128;
 
 struct TcLayout {
-  // [Q hi 4K][Q lo 4K][P^T hi 2K][P^T lo 2K][stages ...][table]; 1024-aligned blocks.
+  // [Q hi 4K][Q lo 4K][P^T buffer 0: hi 2K, lo 2K][buffer 1][stages ...][table].
   // Q: [16 heads][128 d] as two [16][128 B] halves; P^T: [16 heads][64 tokens].
-  static constexpr int kQ = 0, kQlo = 4096, kP = 8192, kPlo = 10240, kStages = 12288;
+  static constexpr int kQ = 0, kQlo = 4096, kP = 8192, kPBuf = 4096, kPlo = 2048,
+                       kStages = 16384;
   static constexpr int kHalf = kTcTile * 128;          // [64 rows][128 B] = 8 KB
   static constexpr int kStage = 4 * kHalf;              // K (2 halves) + V (2 halves)
   static size_t bytes(int stages, int table_entries) {
@@ -157,7 +165,44 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
 
 namespace pkv {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
+
+// Bounded wait that also gives up once any role of the CTA has given up.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  uint32_t ok = 0;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Barrier of the 4 softmax warps (named barrier 1) that also ANDs a flag, so
+// every softmax warp takes the same loop exit.
+__device__ __forceinline__ bool softmax_bar_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, 128, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
 
 template <bool QF32, int STAGES>
 __global__ void __launch_bounds__(kTcThreads)
@@ -169,14 +214,15 @@ __global__ void __launch_bounds__(kTcThreads)
   const int G = p.num_q_heads / p.num_kv_heads;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[STAGES];
-  __shared__ __align__(8) uint64_t bar_s[2];
-  __shared__ __align__(8) uint64_t bar_o;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
+  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ float red[4][GMAX];
-  __shared__ int ok_sh;
+  __shared__ float red[2][4][GMAX];
+  __shared__ float lred[4][GMAX];
+  __shared__ int abort_sh;
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sma = smem_u32(sm);
+  volatile int* abort_flag = &abort_sh;
 
   const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -211,7 +257,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     sbt[i] = b;
   }
-  // Q (B operand of QK): 16 rows x 128 dims, bf16 hi (+ lo for float32 q); P^T rows >= G zeroed
+  // Q (B operand of QK): 16 rows x 128 dims, bf16 hi (+ lo for float32 q); P^T zeroed
   {
     const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + hq0;
     for (int i = tid; i < GMAX * 16; i += kTcThreads) {
@@ -239,17 +285,24 @@ __global__ void __launch_bounds__(kTcThreads)
       }
       *reinterpret_cast<uint4*>(sm + LY::kQ + hh * 2048 + swz(h, uu)) = hi;
       if (QF32) *reinterpret_cast<uint4*>(sm + LY::kQlo + hh * 2048 + swz(h, uu)) = lo;
-      if (hh == 0) {   // P^T rows: zero (rows >= G stay zero for the whole CTA)
-        *reinterpret_cast<uint4*>(sm + LY::kP + swz(h, uu)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sm + LY::kPlo + swz(h, uu)) = make_uint4(0, 0, 0, 0);
-      }
+      // P^T buffers (hi, lo of both): rows >= G stay zero for the whole CTA
+      *reinterpret_cast<uint4*>(sm + LY::kP + hh * LY::kPBuf + swz(h, uu)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm + LY::kP + hh * LY::kPBuf + LY::kPlo + swz(h, uu)) =
+          make_uint4(0, 0, 0, 0);
     }
   }
   if (tid == 0) {
-    for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&full[st]), 1);
-    mbar_init(smem_u32(&bar_s[0]), 1);
-    mbar_init(smem_u32(&bar_s[1]), 1);
-    mbar_init(smem_u32(&bar_o), 1);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&empty[st]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&s_full[b]), 1);
+      mbar_init(smem_u32(&s_free[b]), 4);
+      mbar_init(smem_u32(&p_full[b]), 4);
+      mbar_init(smem_u32(&o_done[b]), 1);
+    }
+    abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -263,236 +316,222 @@ __global__ void __launch_bounds__(kTcThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = tmem_base_sh;          // S^T buffers at columns 0 / 16, O^T at 32
-  const uint32_t lane_q = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
   const uint32_t tmO = tm + 32;
-
   const int ntiles = (t_end - t_begin + kTcTile - 1) / kTcTile;
   const int box_rows = mp.box_rows;
   const int nbox = kTcTile / box_rows;
-  const uint32_t idesc_qk = tc_idesc(kTcTile, GMAX, false, false, true);
-  const uint32_t idesc_pv = tc_idesc(kTcD, GMAX, true, false, true);
+  int have_out = 0;
+  float ov[GMAX];
+  float m[GMAX];
 
-  auto issue_tma = [&](int j) {   // thread 0
-    const int stage = j % STAGES;
-    const int t0 = t_begin + j * kTcTile;
-    const uint32_t bar = smem_u32(&full[stage]);
-    uint32_t bytes = 0;
-    for (int bx = 0; bx < nbox; ++bx) {
-      const int tb = t0 + bx * box_rows;
-      if (tb >= ctx) break;
-      if (sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 4 * box_rows * 128;
-    }
-    mbar_arrive_expect_tx(bar, bytes);
-    const uint32_t sbase = sma + LY::kStages + stage * LY::kStage;
-    for (int bx = 0; bx < nbox; ++bx) {
-      const int tb = t0 + bx * box_rows;
-      if (tb >= ctx) break;
-      const int32_t b = sbt[(tb >> p.bs_log2) - lb0];
-      if (b < 0) continue;
-      const int z = (b << p.bs_log2) + (tb & ((1 << p.bs_log2) - 1));
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t off = hh * LY::kHalf + bx * box_rows * 128;
-        tma_load_3d(sbase + off, &tmap_k, hh * 64, g, z, bar);
-        tma_load_3d(sbase + 2 * LY::kHalf + off, &tmap_v, hh * 64, g, z, bar);
+  if (warp == 4) {
+    // ------------------------------ TMA producer ------------------------------
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % STAGES;
+      if (j >= STAGES) {
+        bool ok = true;
+        if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-    }
-  };
-  auto issue_qk = [&](int j) {    // thread 0, tile j landed
-    const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
-    const uint32_t dst = tm + (j & 1) * GMAX;
-#pragma unroll
-    for (int ks = 0; ks < kTcD / 16; ++ks) {
-      const uint32_t koff = (ks >> 2) * LY::kHalf + (ks & 3) * 32;
-      const uint32_t qoff = (ks >> 2) * 2048 + (ks & 3) * 32;
-      const uint64_t adesc = tc_desc(kb + koff, 0, 1024);
-      tc_mma(dst, adesc, tc_desc(sma + LY::kQ + qoff, 0, 1024), idesc_qk, ks > 0);
-      if (QF32) tc_mma(dst, adesc, tc_desc(sma + LY::kQlo + qoff, 0, 1024), idesc_qk, 1);
-    }
-    tc_commit(smem_u32(&bar_s[j & 1]));
-  };
-  // all threads take one thread's verdict (a failed wait ends the tile loop)
-  auto agree = [&](bool ok_local, int who) -> bool {
-    if (tid == who) ok_sh = ok_local ? 1 : 0;
-    __syncthreads();
-    const bool r = ok_sh != 0;
-    __syncthreads();
-    return r;
-  };
-
-  bool alive = true;
-  {
-    bool ok = true;
-    if (tid == 0) {
-      for (int j = 0; j < min(STAGES, ntiles); ++j) issue_tma(j);
-      ok = mbar_wait(smem_u32(&full[0]), 0);
-      if (ok) issue_qk(0);
-    }
-    alive = agree(ok, 0);
-  }
-  int qk_issued = 1, pv_issued = 0;
-
-  // per-thread state: token row t = 16*warp + lane (lanes < 16), heads in registers
-  const bool tok_lane = lane < 16;
-  const int tloc = 16 * warp + lane;
-  float m[GMAX], lpart[GMAX];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h) {
-    m[h] = -CUDART_INF_F;
-    lpart[h] = 0.f;
-  }
-  const float sl2 = p.qk_scale_log2;
-
-  for (int i = 0; i < ntiles && alive; ++i) {
-    const int t0 = t_begin + i * kTcTile;
-    const int tb = t0 + tloc;
-    const bool filled = tok_lane && tb < ctx && sbt[(tb >> p.bs_log2) - lb0] >= 0;
-    // (1) S^T(i): this thread's token, G logits
-    const bool sok = mbar_wait(smem_u32(&bar_s[i & 1]), (i >> 1) & 1);
-    tc_fence_after();
-    float sv[GMAX];
-    tc_ld16(tm + lane_q + (i & 1) * GMAX, sv);
-    // (2) per-head tile max: warp (16 token lanes) then across the 4 warps
-    float mx[GMAX];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-      sv[h] = (filled && h < G) ? sv[h] * sl2 : -CUDART_INF_F;
-      mx[h] = sv[h];
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1)
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h) red[warp][h] = mx[h];
-    }
-    tc_fence_before();
-    if (!agree(sok, 0)) {   // (also the barrier after which S(i) has been read by all)
-      alive = false;
-      break;
-    }
-    // (3) QK(i+1) overlaps the rest of this tile
-    if (i + 1 < ntiles) {
-      bool ok = true;
-      if (tid == 0) {
-        tc_fence_after();
-        ok = mbar_wait(smem_u32(&full[(i + 1) % STAGES]), ((i + 1) / STAGES) & 1);
-        if (ok) issue_qk(i + 1);
-      }
-      ++qk_issued;
-      if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
-    }
-    // (4) running max (lazy), probabilities, partial sums
-    bool resc = false;
-    float alpha[GMAX];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-      const float mt = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
-      alpha[h] = 1.f;
-      if (h < G && mt > m[h] + 8.f) {
-        if (m[h] != -CUDART_INF_F) {
-          alpha[h] = exp2f(m[h] - mt);
-          resc = true;
+      const int t0 = t_begin + j * kTcTile;
+      const uint32_t bar = smem_u32(&full[st]);
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int bx = 0; bx < nbox; ++bx) {
+          const int tb = t0 + bx * box_rows;
+          if (tb < ctx && sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 4 * box_rows * 128;
         }
-        m[h] = mt;
+        mbar_arrive_expect_tx(bar, bytes);
       }
-      const float pr = (h < G && filled) ? exp2f(sv[h] - m[h]) : 0.f;
-      lpart[h] = lpart[h] * alpha[h] + pr;
-      sv[h] = pr;
-    }
-    // (5) PV(i-1) done: O, P^T and the stage of tile i-1 are free
-    if (i > 0) {
-      const bool ok = mbar_wait(smem_u32(&bar_o), (i - 1) & 1);
-      if (!ok) {
-        if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
-        alive = false;   // every thread sees the same barrier; the vote below settles it
+      __syncwarp();
+      const uint32_t sbase = sma + LY::kStages + st * LY::kStage;
+      for (int k = lane; k < 4 * nbox; k += 32) {   // (box, K/V, half) per lane
+        const int bx = k >> 2, kv = (k >> 1) & 1, hh = k & 1;
+        const int tb = t0 + bx * box_rows;
+        if (tb >= ctx) continue;
+        const int32_t b = sbt[(tb >> p.bs_log2) - lb0];
+        if (b < 0) continue;
+        const int z = (b << p.bs_log2) + (tb & ((1 << p.bs_log2) - 1));
+        const uint32_t off = kv * 2 * LY::kHalf + hh * LY::kHalf + bx * box_rows * 128;
+        tma_load_3d(sbase + off, kv ? &tmap_v : &tmap_k, hh * 64, g, z, bar);
       }
-      tc_fence_after();
-      if (tid == 0 && ok && i - 1 + STAGES < ntiles) issue_tma(i - 1 + STAGES);
     }
-    // (6) rare rescale of O^T columns (this thread's lane = dimension d)
-    if (__syncthreads_or(resc)) {
-      float ov[GMAX];
-      tc_ld16(tmO + lane_q, ov);
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_qk = tc_idesc(kTcTile, GMAX, false, false, true);
+      const uint32_t idesc_pv = tc_idesc(kTcD, GMAX, true, false, true);
+      auto issue_pv = [&](int j) {
+        const uint32_t vb = sma + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kHalf;
+        const uint32_t pb = sma + LY::kP + (j & 1) * LY::kPBuf;
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) ov[h] *= alpha[h];
-      tc_st16(tmO + lane_q, ov);
+        for (int kk = 0; kk < kTcTile / 16; ++kk) {
+          const uint64_t adesc = tc_desc(vb + kk * 2048, LY::kHalf, 1024);
+          tc_mma(tmO, adesc, tc_desc(pb + kk * 32, 0, 1024), idesc_pv, (j > 0 || kk > 0));
+          tc_mma(tmO, adesc, tc_desc(pb + LY::kPlo + kk * 32, 0, 1024), idesc_pv, 1);
+        }
+        tc_commit(smem_u32(&o_done[j & 1]));
+        tc_commit(smem_u32(&empty[j % STAGES]));
+      };
+      int issued_qk = 0, issued_pv = 0;
+      for (int j = 0; j <= ntiles; ++j) {
+        if (j < ntiles) {
+          if (!tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
+          if (j >= 2 && !tc_wait(smem_u32(&s_free[j & 1]), ((j - 2) >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
+          const uint32_t dst = tm + (j & 1) * GMAX;
+#pragma unroll
+          for (int ks = 0; ks < kTcD / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * LY::kHalf + (ks & 3) * 32;
+            const uint32_t qoff = (ks >> 2) * 2048 + (ks & 3) * 32;
+            const uint64_t adesc = tc_desc(kb + koff, 0, 1024);
+            tc_mma(dst, adesc, tc_desc(sma + LY::kQ + qoff, 0, 1024), idesc_qk, ks > 0);
+            if (QF32) tc_mma(dst, adesc, tc_desc(sma + LY::kQlo + qoff, 0, 1024), idesc_qk, 1);
+          }
+          tc_commit(smem_u32(&s_full[j & 1]));
+          ++issued_qk;
+        }
+        if (j >= 1) {
+          if (!tc_wait(smem_u32(&p_full[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          issue_pv(j - 1);
+          ++issued_pv;
+        }
+      }
+      if (*abort_flag) {   // let issued tensor-core work finish before TMEM is released
+        volatile int no_abort = 0;
+        if (issued_pv > 0)
+          tc_wait(smem_u32(&o_done[(issued_pv - 1) & 1]), ((issued_pv - 1) >> 1) & 1, &no_abort);
+        if (issued_qk > 0)
+          tc_wait(smem_u32(&s_full[(issued_qk - 1) & 1]), ((issued_qk - 1) >> 1) & 1, &no_abort);
+      }
     }
-    // (7) P^T(i) -> smem (bf16 hi + lo); V rows without cache data -> 0
-    if (tok_lane) {
+  } else {
+    // ------------------------- softmax warps 0-3 ------------------------------
+    const uint32_t lane_q = static_cast<uint32_t>(warp * 32) << 16;
+    const bool tok_lane = lane < 16;
+    const int tloc = 16 * warp + lane;   // token row of the M=64 accumulator layout
+    float lpart[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      m[h] = -CUDART_INF_F;
+      lpart[h] = 0.f;
+    }
+    const float sl2 = p.qk_scale_log2;
+    bool alive = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int tb = t_begin + j * kTcTile + tloc;
+      const bool filled = tok_lane && tb < ctx && sbt[(tb >> p.bs_log2) - lb0] >= 0;
+      if (!tc_wait(smem_u32(&s_full[j & 1]), (j >> 1) & 1, abort_flag)) alive = false;
+      tc_fence_after();
+      float sv[GMAX];
+      tc_ld16(tm + lane_q + (j & 1) * GMAX, sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
+      float mx[GMAX];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
-        if (h < G) {
-          const __nv_bfloat16 hv = __float2bfloat16_rn(sv[h]);
-          const __nv_bfloat16 lv = __float2bfloat16_rn(sv[h] - __bfloat162float(hv));
-          const uint32_t off = h * 128 + ((((tloc >> 3) ^ (h & 7))) << 4) + (tloc & 7) * 2;
-          *reinterpret_cast<__nv_bfloat16*>(sm + LY::kP + off) = hv;
-          *reinterpret_cast<__nv_bfloat16*>(sm + LY::kPlo + off) = lv;
+        sv[h] = (filled && h < G) ? sv[h] * sl2 : -CUDART_INF_F;
+        mx[h] = sv[h];
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) red[j & 1][warp][h] = mx[h];
+      }
+      alive = softmax_bar_all(alive);   // also publishes red[][] to all softmax warps
+      if (!alive) break;
+      bool resc = false;
+      float alpha[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        const float mt = fmaxf(fmaxf(red[j & 1][0][h], red[j & 1][1][h]),
+                               fmaxf(red[j & 1][2][h], red[j & 1][3][h]));
+        alpha[h] = 1.f;
+        if (h < G && mt > m[h] + 8.f) {
+          if (m[h] != -CUDART_INF_F) {
+            alpha[h] = exp2f(m[h] - mt);
+            resc = true;
+          }
+          m[h] = mt;
+        }
+        const float pr = (h < G && filled) ? exp2f(sv[h] - m[h]) : 0.f;
+        lpart[h] = lpart[h] * alpha[h] + pr;
+        sv[h] = pr;
+      }
+      // P^T buffer j%2 is free once PV(j-2) is done; a rescale needs PV(j-1) done.
+      // A failed wait only clears `alive`; the next vote ends the loop for all.
+      if (j >= 2 && !tc_wait(smem_u32(&o_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag))
+        alive = false;
+      if (resc) {   // same decision in every softmax thread
+        if (!tc_wait(smem_u32(&o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag))
+          alive = false;
+        tc_fence_after();
+        float o[GMAX];
+        tc_ld16(tmO + lane_q, o);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) o[h] *= alpha[h];
+        tc_st16(tmO + lane_q, o);
+      }
+      uint8_t* pb = sm + LY::kP + (j & 1) * LY::kPBuf;
+      if (tok_lane) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          if (h < G) {
+            const __nv_bfloat16 hv = __float2bfloat16_rn(sv[h]);
+            const __nv_bfloat16 lv = __float2bfloat16_rn(sv[h] - __bfloat162float(hv));
+            const uint32_t off = h * 128 + ((((tloc >> 3) ^ (h & 7))) << 4) + (tloc & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16*>(pb + off) = hv;
+            *reinterpret_cast<__nv_bfloat16*>(pb + LY::kPlo + off) = lv;
+          }
+        }
+        if (!filled) {   // V rows without cache data must not reach the products
+          uint8_t* vrow =
+              sm + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kHalf + tloc * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            *reinterpret_cast<uint4*>(vrow + (u << 4)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + LY::kHalf + (u << 4)) = make_uint4(0, 0, 0, 0);
+          }
         }
       }
-      if (!filled) {
-        uint8_t* vrow = sm + LY::kStages + (i % STAGES) * LY::kStage + 2 * LY::kHalf + tloc * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          *reinterpret_cast<uint4*>(vrow + (u << 4)) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + LY::kHalf + (u << 4)) = make_uint4(0, 0, 0, 0);
-        }
-      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
     }
-    fence_proxy_async();
-    tc_fence_before();
-    if (!__syncthreads_and(alive)) {
-      alive = false;
-      break;
-    }
-    // (8) O^T += V^T P^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t vb = sma + LY::kStages + (i % STAGES) * LY::kStage + 2 * LY::kHalf;
-#pragma unroll
-      for (int kk = 0; kk < kTcTile / 16; ++kk) {
-        const uint64_t adesc = tc_desc(vb + kk * 2048, LY::kHalf, 1024);
-        tc_mma(tmO, adesc, tc_desc(sma + LY::kP + kk * 32, 0, 1024), idesc_pv, (i > 0 || kk > 0));
-        tc_mma(tmO, adesc, tc_desc(sma + LY::kPlo + kk * 32, 0, 1024), idesc_pv, 1);
-      }
-      tc_commit(smem_u32(&bar_o));
-    }
-    ++pv_issued;
-  }
-
-  // ---- epilogue: O^T (lane d) / l[h] ------------------------------------------------
-  float ov[GMAX];
-  bool have = false;
-  if (alive && pv_issued > 0) {
-    have = __syncthreads_and(mbar_wait(smem_u32(&bar_o), (pv_issued - 1) & 1));
-    if (have) {
+    // epilogue: O^T (lane d) and the sum l per head
+    alive = softmax_bar_all(alive);
+    const bool last_ok =
+        alive && tc_wait(smem_u32(&o_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1, abort_flag);
+    if (__all_sync(0xffffffffu, last_ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
       tc_ld16(tmO + lane_q, ov);
+      have_out = 1;
     }
-  }
-  if (!alive || !have) {
-    if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
-    if (pv_issued > 0) mbar_wait(smem_u32(&bar_o), (pv_issued - 1) & 1);
-    if (qk_issued > 0) mbar_wait(smem_u32(&bar_s[(qk_issued - 1) & 1]), ((qk_issued - 1) >> 1) & 1);
-  }
-  // l[h]: sum of the token threads' partial sums
-  __syncthreads();
 #pragma unroll
-  for (int h = 0; h < GMAX; ++h) {
-    float v = tok_lane ? lpart[h] : 0.f;
+    for (int h = 0; h < GMAX; ++h) {
+      float v = tok_lane ? lpart[h] : 0.f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) red[warp][h] = v;
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) lred[warp][h] = v;
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;\n" ::"r"(tm) : "memory");
-  const bool ok_out = alive && have;
+  if (warp >= 4) return;
+  const bool ok_out = have_out && !*abort_flag;
+  if (tid == 0 && *abort_flag) flag_status(p.status, PKV_DEV_TIMEOUT);
   const int d = tid;   // O^T lane = dimension
   const int64_t sh0 = static_cast<int64_t>(s) * p.num_q_heads + hq0;
   for (int h = 0; h < G; ++h) {
-    const float L = red[0][h] + red[1][h] + red[2][h] + red[3][h];
+    const float L = lred[0][h] + lred[1][h] + lred[2][h] + lred[3][h];
     const float o = ok_out ? ov[h] : 0.f;
     if (nparts == 1) {
       p.out[(sh0 + h) * kTcD + d] = ok_out ? o / L : 0.f;
