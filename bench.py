@@ -218,6 +218,10 @@ def decode_kernel_name(w) -> str:
         return "paged_decode_kernel"
     if forced == "tc" and w.kv_dtype == "bf16" and w.head_dim == 128:
         return "paged_decode_tc_kernel"
+    if forced != "mma" and w.group <= 8 and (
+            (w.kv_dtype == "bf16" and w.head_dim in (64, 128))
+            or (w.kv_dtype == "fp8_e4m3" and w.head_dim == 128)):
+        return "paged_decode_mma2_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
         return "paged_decode_mma_kernel"
     if w.kv_dtype == "fp8_e4m3" and w.head_dim == 128:

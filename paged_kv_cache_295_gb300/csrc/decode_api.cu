@@ -31,11 +31,12 @@ namespace {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
-// Kernel choice.  Unset, the mma.sync tensor-core kernels run wherever they
-// apply (the fastest measured so far), else the CUDA-core kernel.
-// PKV_DECODE_PATH=tc selects the tcgen05 kernel where it applies,
-// PKV_DECODE_PATH=simt forces the CUDA-core kernel; the tests check every
-// kernel on the same inputs.
+// Kernel choice.  Unset: the transposed mma.sync kernel (decode_mma2.cuh) for
+// groups of up to 8 heads, the heads-as-rows mma.sync kernel (decode_mma.cuh)
+// for groups of up to 16, else the CUDA-core kernel - the fastest measured
+// order.  PKV_DECODE_PATH=mma skips the transposed kernel, =tc selects the
+// tcgen05 kernel where it applies, =simt forces the CUDA-core kernel; the tests
+// check every kernel on the same inputs.
 bool force_path(const char* name) {
   const char* v = std::getenv("PKV_DECODE_PATH");
   return v && std::strcmp(v, name) == 0;
@@ -149,10 +150,12 @@ extern "C" pkv_status paged_attention_decode(
   const int G = num_q_heads / num_kv_heads;
   const bool use_tc =
       force_path("tc") && tc_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
-  const bool use_mma =
-      !use_tc && !force_simt() && mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
+  const bool use_mma2 = !use_tc && !force_simt() && !force_path("mma") &&
+                        mma2_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
+  const bool use_mma = !use_tc && !use_mma2 && !force_simt() &&
+                       mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   LaunchFn fn = pick(kv_dtype, head_dim, G);
-  if (!use_tc && !use_mma && !fn) return PKV_ERR_UNSUPPORTED;
+  if (!use_tc && !use_mma2 && !use_mma && !fn) return PKV_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
@@ -198,6 +201,9 @@ extern "C" pkv_status paged_attention_decode(
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc) return launch_decode_tc(a, k_cache, v_cache, num_blocks, q_dtype == PKV_F32);
+  if (use_mma2)
+    return launch_decode_mma2(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
+                              kv_dtype == PKV_FP8_E4M3);
   if (use_mma)
     return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
                              kv_dtype == PKV_FP8_E4M3);

@@ -392,6 +392,11 @@ bool mma_path_supported(int32_t kv_dtype, int head_dim, int group, int block_siz
                         int64_t num_blocks);
 pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
                              int head_dim, int64_t num_blocks, bool q_f32, bool fp8);
+// Transposed mma.sync path (heads as the mma N columns); see decode_mma2.cuh.
+bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
+                         int64_t num_blocks);
+pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
+                              int head_dim, int64_t num_blocks, bool q_f32, bool fp8);
 // 5th-generation tensor-core (tcgen05 + TMEM) path; see decode_tc.cuh.
 bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                        int64_t num_blocks);

@@ -1,0 +1,420 @@
+// PagedAttention decode, tensor-core path with the contractions transposed
+// (mma.sync m16n8k16; 16-bit and FP8 caches; query groups of up to 8 heads).
+//
+// Same work split and staging as decode_mma.cuh (one CTA per sequence x KV
+// head x split-KV partition; each warp streams every NW-th 16-token chunk
+// through its own TMA ring), but the operands are laid out so the group's
+// query heads ride in the mma's N=8 columns instead of its 16 rows:
+//
+//   S^T[t][h]  = sum_d K[t][d] q_h[d]     A = K chunk (16 tokens x 16 dims),
+//                                         B = q^T (16 dims x 8 heads)
+//   O^T[d][h] += sum_t V[t][d] P[h][t]    A = V^T chunk (16 dims x 16 tokens),
+//                                         B = P^T (16 tokens x 8 heads)
+//
+// A 16-token chunk then takes 8 mma for QK and 8 per P part for PV, whatever
+// the group size up to 8, half of what the heads-as-rows form needs ("LLM
+// inference tutorial" section 4.4: all G heads of a KV head share every K/V
+// byte).  The lane that holds S^T for heads 2*tig, 2*tig+1 also holds O^T for
+// the same two heads, so the online-softmax rescale is lane-local.  P^T moves
+// from the accumulator layout to the B-fragment layout through 512 bytes of
+// per-warp shared memory.
+//
+// 16-bit caches: fragments come from the swizzled tiles with ldmatrix
+// (ldmatrix.trans for V^T); P is split into bf16 hi + lo parts.  FP8 caches:
+// E4M3 bytes are converted in registers to fp16 (exact) using a dimension
+// permutation shared by q and K (QK) and an output-dimension permutation (PV)
+// so each lane loads contiguous 16-byte slices; P is fp16.
+#pragma once
+
+#include "decode_mma_fp8.cuh"
+
+namespace pkv {
+
+template <typename KV, int D, int NW, int STAGES>
+struct Mma2Smem {
+  static constexpr int kBoxes = D * KV::kBytes / 128;             // 128-byte TMA boxes per row
+  static constexpr int kBoxBytes = kMmaChunk * 128;               // [16 rows][128 B]
+  static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;      // K + V
+  static constexpr int kScratch = 512;                            // P^T hi + lo (8 x 16 x 2 B each)
+  static constexpr int kWarpBytes = STAGES * kStageBytes + 1024;  // + scratch, 1 KiB aligned
+  static_assert(STAGES * kStageBytes >= 8 * (D + 2) * 4, "combine area fits a warp ring");
+  static size_t bytes(int table_entries) {
+    return 1024 + static_cast<size_t>(NW) * kWarpBytes + static_cast<size_t>(table_entries) * 4;
+  }
+};
+
+template <typename KV, int D, bool QF32, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_mma2_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const MmaParams mp) {
+  using SM = Mma2Smem<KV, D, NW, STAGES>;
+  constexpr bool F8 = KV::kBytes == 1;
+  static_assert(!F8 || D == 128, "FP8 path is built for head_dim 128");
+  constexpr int H = SM::kBoxes;
+  constexpr int KSTEPS = D / 16;   // QK k-steps
+  constexpr int MT = D / 16;       // PV m-tiles (16 output dims each)
+  const DecodeParams& p = mp.p;
+  const int G = p.num_q_heads / p.num_kv_heads;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[NW][STAGES];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+
+  const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int P = p.partition_tokens;
+
+  int ctx = __ldg(p.context_lens + s);
+  const int cap = context_cap(p);
+  if (ctx < 0 || ctx > cap) {
+    if (part == 0 && threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  const int nparts = (ctx + P - 1) / P;
+  if (part >= (nparts > 0 ? nparts : 1)) return;
+  const int hq0 = g * G;
+  if (ctx == 0) {
+    for (int i = threadIdx.x; i < G * D; i += NW * 32)
+      p.out[(static_cast<int64_t>(s) * p.num_q_heads + hq0) * D + i] = 0.f;
+    return;
+  }
+  const int t_begin = part * P;
+  const int t_end = min(t_begin + P, ctx);
+
+  int32_t* sbt = reinterpret_cast<int32_t*>(smem + NW * SM::kWarpBytes);
+  const int lb0 = t_begin >> p.bs_log2;
+  const int nlb = ((t_end - 1) >> p.bs_log2) - lb0 + 1;
+  const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
+  for (int i = threadIdx.x; i < nlb; i += NW * 32) {
+    int32_t b = __ldg(bt_row + lb0 + i);
+    if (b < 0 || b >= p.num_blocks) {
+      flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      b = -1;
+    }
+    sbt[i] = b;
+  }
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  // q^T as B fragments: b0 = q[gid][k 2tig..], b1 = q[gid][k 2tig+8..] of each k-step
+  // (FP8: logical k 2tig+e (+8) of k-step ks <-> dim 32*tig + 4*ks + e (+2)).
+  uint32_t qb[KSTEPS][2];
+  uint32_t qblo[QF32 ? KSTEPS : 1][2];
+  {
+    const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + hq0 + gid;
+    const bool real = gid < G;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int col = F8 ? 32 * tig + 4 * ks + 2 * half : 16 * ks + 8 * half + 2 * tig;
+        float x0 = 0.f, x1 = 0.f;
+        if (real) {
+          if (QF32) {
+            const float* qf = static_cast<const float*>(p.q) + row * D + col;
+            x0 = qf[0];
+            x1 = qf[1];
+          } else {
+            const __nv_bfloat16* qh = static_cast<const __nv_bfloat16*>(p.q) + row * D + col;
+            x0 = __bfloat162float(qh[0]);
+            x1 = __bfloat162float(qh[1]);
+          }
+        }
+        uint32_t hi, lo;
+        if (F8) {
+          hi = pack_f16(x0, x1);
+          const __half2 hv = *reinterpret_cast<const __half2*>(&hi);
+          lo = pack_f16(x0 - __low2float(hv), x1 - __high2float(hv));
+        } else {
+          hi = pack_bf16(x0, x1);
+          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hi);
+          lo = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
+        }
+        qb[ks][half] = hi;
+        if (QF32) qblo[QF32 ? ks : 0][half] = lo;
+      }
+    }
+  }
+
+  float o[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  // softmax state of heads 2*tig and 2*tig+1
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
+  const float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
+
+  uint8_t* ring = smem + warp * SM::kWarpBytes;
+  uint8_t* scratch = ring + STAGES * SM::kStageBytes;      // P^T hi [8][16], lo [8][16]
+  const uint32_t ring_a = smem_u32(ring);
+  const int nchunks = (t_end - t_begin + kMmaChunk - 1) / kMmaChunk;
+  const int my_n = warp < nchunks ? (nchunks - warp + NW - 1) / NW : 0;
+  const int box_rows = mp.box_rows;
+  const int nbox = kMmaChunk / box_rows;
+  bool alive = true;
+
+  auto issue = [&](int it) {
+    if (it >= my_n || lane != 0) return;
+    const int stage = it % STAGES;
+    const int t0 = t_begin + (warp + it * NW) * kMmaChunk;
+    const uint32_t bar = smem_u32(&bars[warp][stage]);
+    uint32_t bytes = 0;
+    for (int bx = 0; bx < nbox; ++bx) {
+      const int tb = t0 + bx * box_rows;
+      if (tb >= ctx) break;
+      if (sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 2 * H * box_rows * 128;
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+    const uint32_t sbase = ring_a + stage * SM::kStageBytes;
+    for (int bx = 0; bx < nbox; ++bx) {
+      const int tb = t0 + bx * box_rows;
+      if (tb >= ctx) break;
+      const int32_t b = sbt[(tb >> p.bs_log2) - lb0];
+      if (b < 0) continue;
+      const int z = (b << p.bs_log2) + (tb & ((1 << p.bs_log2) - 1));
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh) {
+        const uint32_t off = hh * SM::kBoxBytes + bx * box_rows * 128;
+        tma_load_3d(sbase + off, &tmap_k, hh * (128 / KV::kBytes), g, z, bar);
+        tma_load_3d(sbase + H * SM::kBoxBytes + off, &tmap_v, hh * (128 / KV::kBytes), g, z, bar);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int st = 0; st < STAGES - 1; ++st) issue(st);
+
+  for (int it = 0; it < my_n; ++it) {
+    issue(it + STAGES - 1);
+    const int stage = it % STAGES;
+    const bool landed =
+        __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[warp][stage]), (it / STAGES) & 1));
+    if (!landed) {
+      if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+      alive = false;
+      for (int k = it + 1; k < min(my_n, it + STAGES); ++k)
+        mbar_wait(smem_u32(&bars[warp][k % STAGES]), (k / STAGES) & 1);
+      break;
+    }
+    const int t0 = t_begin + (warp + it * NW) * kMmaChunk;
+    const int valid = min(kMmaChunk, ctx - t0);
+    uint8_t* kb = ring + stage * SM::kStageBytes;
+    uint8_t* vb = kb + H * SM::kBoxBytes;
+    bool hole = valid < kMmaChunk;
+    if (!hole) {
+      for (int bx = 0; bx < nbox; ++bx)
+        if (sbt[((t0 + bx * box_rows) >> p.bs_log2) - lb0] < 0) hole = true;
+    }
+    if (hole) {   // rows the TMA did not fill become zero
+      for (int i = lane; i < kMmaChunk * 8 * H * 2; i += 32) {
+        const int r = (i >> 3) % kMmaChunk;
+        const int rest = i / (8 * kMmaChunk);
+        const int bx = r / box_rows;
+        const bool filled = r < valid && sbt[((t0 + bx * box_rows) >> p.bs_log2) - lb0] >= 0;
+        if (!filled) {
+          uint8_t* base = (rest < H ? kb : vb) + (rest % H) * SM::kBoxBytes;
+          *reinterpret_cast<uint4*>(base + r * 128 + ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      __syncwarp();
+    }
+    const uint32_t kb_a = smem_u32(kb), vb_a = smem_u32(vb);
+
+    // ---- S^T = K q^T: tokens gid, gid+8 x heads 2tig, 2tig+1 -------------------
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (F8) {
+      uint32_t wa[8], wb[8];   // 32-byte slices [32*tig, +32) of token rows gid, gid+8
+      {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(kb + swz(gid, 2 * tig));
+        const uint4 a1 = *reinterpret_cast<const uint4*>(kb + swz(gid, 2 * tig + 1));
+        const uint4 b0 = *reinterpret_cast<const uint4*>(kb + swz(gid + 8, 2 * tig));
+        const uint4 b1 = *reinterpret_cast<const uint4*>(kb + swz(gid + 8, 2 * tig + 1));
+        wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
+        wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+        wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
+        wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const uint32_t a[4] = {e4m3x2_to_f16x2(wa[ks]), e4m3x2_to_f16x2(wb[ks]),
+                               e4m3x2_to_f16x2(wa[ks] >> 16), e4m3x2_to_f16x2(wb[ks] >> 16)};
+        mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
+        if (QF32) mma_f16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int i = lane >> 3, r = (i & 1) * 8 + (lane & 7);
+        const int hh = (16 * ks) / 64;
+        const int u = ((16 * ks) % 64) / 8 + (i >> 1);
+        uint32_t a[4];
+        ldsm_x4(kb_a + hh * SM::kBoxBytes + swz(r, u), a[0], a[1], a[2], a[3]);
+        mma_bf16(sacc, a, qb[ks][0], qb[ks][1]);
+        if (QF32) mma_bf16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
+      }
+    }
+    // ---- online softmax (columns = heads 2tig, 2tig+1; rows = tokens gid, gid+8) ----
+    const bool t0ok = gid < valid, t1ok = gid + 8 < valid;
+    sacc[0] = (t0ok && h0ok) ? sacc[0] * sl2 : -CUDART_INF_F;
+    sacc[1] = (t0ok && h1ok) ? sacc[1] * sl2 : -CUDART_INF_F;
+    sacc[2] = (t1ok && h0ok) ? sacc[2] * sl2 : -CUDART_INF_F;
+    sacc[3] = (t1ok && h1ok) ? sacc[3] * sl2 : -CUDART_INF_F;
+    float mx0 = fmaxf(sacc[0], sacc[2]), mx1 = fmaxf(sacc[1], sacc[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
+      const float a0 = h0ok ? exp2f(m0 - mn0) : 1.f;   // m = -inf first: exp2(-inf) = 0
+      const float a1 = h1ok ? exp2f(m1 - mn1) : 1.f;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      m0 = mn0;
+      m1 = mn1;
+    }
+    const float p00 = h0ok && t0ok ? exp2f(sacc[0] - m0) : 0.f;   // (token gid, head 2tig)
+    const float p01 = h1ok && t0ok ? exp2f(sacc[1] - m1) : 0.f;
+    const float p10 = h0ok && t1ok ? exp2f(sacc[2] - m0) : 0.f;   // (token gid+8, head 2tig)
+    const float p11 = h1ok && t1ok ? exp2f(sacc[3] - m1) : 0.f;
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    // P^T to B fragments via scratch: [head][token] (hi; lo for 16-bit caches)
+    {
+      auto put = [&](int off, float v) {
+        if (F8) {
+          *reinterpret_cast<__half*>(scratch + off) = __float2half_rn(v);
+        } else {
+          const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+          *reinterpret_cast<__nv_bfloat16*>(scratch + off) = hv;
+          *reinterpret_cast<__nv_bfloat16*>(scratch + 256 + off) =
+              __float2bfloat16_rn(v - __bfloat162float(hv));
+        }
+      };
+      put(((2 * tig) * 16 + gid) * 2, p00);
+      put(((2 * tig + 1) * 16 + gid) * 2, p01);
+      put(((2 * tig) * 16 + gid + 8) * 2, p10);
+      put(((2 * tig + 1) * 16 + gid + 8) * 2, p11);
+    }
+    __syncwarp();
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(scratch + (gid * 16 + 2 * tig) * 2);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(scratch + (gid * 16 + 2 * tig + 8) * 2);
+    uint32_t pl0 = 0, pl1 = 0;
+    if (!F8) {
+      pl0 = *reinterpret_cast<const uint32_t*>(scratch + 256 + (gid * 16 + 2 * tig) * 2);
+      pl1 = *reinterpret_cast<const uint32_t*>(scratch + 256 + (gid * 16 + 2 * tig + 8) * 2);
+    }
+
+    // ---- O^T += V^T P^T -----------------------------------------------------------
+    if (F8) {
+      // lane owns output dims 16*gid + 2*mt + (0 | 1); tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+      const uint4 va = *reinterpret_cast<const uint4*>(vb + swz(2 * tig, gid));
+      const uint4 vv = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 1, gid));
+      const uint4 vc = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 8, gid));
+      const uint4 vd = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 9, gid));
+      const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vv.x, vv.y, vv.z, vv.w};
+      const uint32_t Cw[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t lo01 = __byte_perm(A[w], B[w], 0x5140);   // bytes 4w, 4w+1 of 2tig / 2tig+1
+        const uint32_t hi01 = __byte_perm(A[w], B[w], 0x7362);   // bytes 4w+2, 4w+3
+        const uint32_t lo89 = __byte_perm(Cw[w], Dw[w], 0x5140);
+        const uint32_t hi89 = __byte_perm(Cw[w], Dw[w], 0x7362);
+        const uint32_t aA[4] = {e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo01 >> 16),
+                                e4m3x2_to_f16x2(lo89), e4m3x2_to_f16x2(lo89 >> 16)};
+        const uint32_t aB[4] = {e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi01 >> 16),
+                                e4m3x2_to_f16x2(hi89), e4m3x2_to_f16x2(hi89 >> 16)};
+        mma_f16(o[2 * w], aA, pb0, pb1);
+        mma_f16(o[2 * w + 1], aB, pb0, pb1);
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int i = lane >> 3, r = (i >> 1) * 8 + (lane & 7);
+        const int hh = (16 * mt) / 64;
+        const int u = ((16 * mt) % 64) / 8 + (i & 1);
+        uint32_t a[4];
+        ldsm_x4_t(vb_a + hh * SM::kBoxBytes + swz(r, u), a[0], a[1], a[2], a[3]);
+        mma_bf16(o[mt], a, pb0, pb1);
+        mma_bf16(o[mt], a, pl0, pl1);
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+  }
+
+  // ---- warp epilogue: l summed over the 8 token-row lanes; rows into the idle ring ----
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  if (!alive) {
+    m0 = m1 = -CUDART_INF_F;
+    l0 = l1 = 0.f;
+  }
+  __syncwarp();
+  float* wres = reinterpret_cast<float*>(ring);   // [8][D] acc, then m[8], l[8]
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int h = 2 * tig + e;
+    if (h < G) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int d_lo = F8 ? 16 * gid + 2 * mt : 16 * mt + gid;
+        const int d_hi = F8 ? 16 * gid + 2 * mt + 1 : 16 * mt + gid + 8;
+        wres[h * D + d_lo] = alive ? o[mt][e] : 0.f;
+        wres[h * D + d_hi] = alive ? o[mt][2 + e] : 0.f;
+      }
+      if (gid == 0) {
+        wres[8 * D + h] = e ? m1 : m0;
+        wres[8 * D + 8 + h] = e ? l1 : l0;
+      }
+    }
+  }
+  __syncthreads();
+
+  const float vsc = F8 ? __ldg(p.v_scale + g) : 1.f;
+  const bool single = nparts == 1;
+  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+    const int h = i / D, d = i % D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + w * SM::kWarpBytes)[8 * D + h]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float* r = reinterpret_cast<const float*>(smem + w * SM::kWarpBytes);
+      const float c = exp2f(r[8 * D + h] - M);
+      L = fmaf(r[8 * D + 8 + h], c, L);
+      O = fmaf(r[h * D + d], c, O);
+    }
+    const int64_t sh = static_cast<int64_t>(s) * p.num_q_heads + hq0 + h;
+    if (single) {
+      p.out[sh * D + d] = O / L * vsc;
+    } else {
+      const int64_t pi = sh * p.max_parts + part;
+      p.part_o[pi * D + d] = O * vsc;
+      if (d == 0) {
+        p.part_ml[pi * 2 + 0] = M;
+        p.part_ml[pi * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+}  // namespace pkv

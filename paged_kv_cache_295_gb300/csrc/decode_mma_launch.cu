@@ -7,6 +7,7 @@
 #include "decode_mma.cuh"
 #include "decode_mma_fp8.cuh"
 #include "decode_tc.cuh"
+#include "decode_mma2.cuh"
 
 namespace pkv {
 
@@ -127,7 +128,78 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
   return PKV_OK;
 }
 
+// Transposed mma.sync kernel: 4 warps, rings of 16-token chunks (8 KiB stages
+// three deep for 16-bit head_dim 128, 4 KiB stages six deep otherwise).
+template <typename KV, int D, bool QF32>
+pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
+                       int num_seqs, cudaStream_t stream) {
+  constexpr int NW = 4;
+  constexpr int STAGES = (D * KV::kBytes == 256) ? 3 : 6;
+  using SM = Mma2Smem<KV, D, NW, STAGES>;
+  const int bs = 1 << mp.p.bs_log2;
+  const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
+  const size_t smem = SM::bytes(table_entries);
+  auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES>;
+  static int configured = 0;
+  if (static_cast<int>(smem) > configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured = static_cast<int>(smem);
+  }
+  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
 }  // namespace
+
+bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
+                         int64_t num_blocks) {
+  if (kv_dtype == PKV_BF16) {
+    if (head_dim != 64 && head_dim != 128) return false;
+  } else if (kv_dtype == PKV_FP8_E4M3) {
+    if (head_dim != 128) return false;
+  } else {
+    return false;
+  }
+  if (group < 1 || group > 8) return false;
+  if (block_size < 8) return false;
+  if (num_blocks * block_size > 0x7fffffffLL) return false;
+  return encode_fn() != nullptr;
+}
+
+pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
+                              int head_dim, int64_t num_blocks, bool q_f32, bool fp8) {
+  const DecodeParams& p = a.p;
+  const int bs = 1 << p.bs_log2;
+  MmaParams mp{p, bs < kMmaChunk ? bs : kMmaChunk};
+  CUtensorMap tk, tv;
+  const int64_t rows = num_blocks * bs;
+  if (!make_map(&tk, k_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8) ||
+      !make_map(&tv, v_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8))
+    return PKV_ERR_CUDA;
+  pkv_status st;
+  if (fp8)
+    st = q_f32 ? launch_mma2<FP8, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
+               : launch_mma2<FP8, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
+  else if (head_dim == 128)
+    st = q_f32 ? launch_mma2<BF16, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
+               : launch_mma2<BF16, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
+  else
+    st = q_f32 ? launch_mma2<BF16, 64, true>(tk, tv, mp, a.num_seqs, a.stream)
+               : launch_mma2<BF16, 64, false>(tk, tv, mp, a.num_seqs, a.stream);
+  if (st != PKV_OK) return st;
+  if (p.max_parts > 1) {
+    if (head_dim == 128)
+      paged_decode_reduce_kernel<128><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
+    else
+      paged_decode_reduce_kernel<64><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
 
 bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                        int64_t num_blocks) {

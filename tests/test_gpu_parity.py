@@ -76,11 +76,12 @@ SMALL = {
 }
 
 
-@pytest.fixture(params=["auto", "tc", "simt"])
+@pytest.fixture(params=["auto", "mma", "tc", "simt"])
 def decode_path(request, monkeypatch):
-    """'auto' = the library's own kernel choice (mma.sync where it applies);
-    'tc' selects the tcgen05 kernel where it applies; 'simt' forces the
-    CUDA-core kernel everywhere."""
+    """'auto' = the library's own kernel choice (transposed mma.sync kernel for
+    groups up to 8); 'mma' skips it for the heads-as-rows mma.sync kernel; 'tc'
+    selects the tcgen05 kernel where it applies; 'simt' forces the CUDA-core
+    kernel everywhere."""
     if request.param == "auto":
         monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
     else:
