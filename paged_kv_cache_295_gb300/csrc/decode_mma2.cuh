@@ -158,19 +158,23 @@ __global__ void __launch_bounds__(NW * 32)
   const int nbox = kMmaChunk / box_rows;
   bool alive = true;
 
+  // Lane 0 arms the stage's barrier and loads K, lane 1 loads V (in parallel).
   auto issue = [&](int it) {
-    if (it >= my_n || lane != 0) return;
+    if (it >= my_n || lane > 1) return;
     const int stage = it % STAGES;
     const int t0 = t_begin + (warp + it * NW) * kMmaChunk;
     const uint32_t bar = smem_u32(&bars[warp][stage]);
-    uint32_t bytes = 0;
-    for (int bx = 0; bx < nbox; ++bx) {
-      const int tb = t0 + bx * box_rows;
-      if (tb >= ctx) break;
-      if (sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 2 * H * box_rows * 128;
+    if (lane == 0) {
+      uint32_t bytes = 0;
+      for (int bx = 0; bx < nbox; ++bx) {
+        const int tb = t0 + bx * box_rows;
+        if (tb >= ctx) break;
+        if (sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 2 * H * box_rows * 128;
+      }
+      mbar_arrive_expect_tx(bar, bytes);
     }
-    mbar_arrive_expect_tx(bar, bytes);
-    const uint32_t sbase = ring_a + stage * SM::kStageBytes;
+    const uint32_t sbase = ring_a + stage * SM::kStageBytes + lane * H * SM::kBoxBytes;
+    const CUtensorMap* map = lane ? &tmap_v : &tmap_k;
     for (int bx = 0; bx < nbox; ++bx) {
       const int tb = t0 + bx * box_rows;
       if (tb >= ctx) break;
@@ -178,11 +182,9 @@ __global__ void __launch_bounds__(NW * 32)
       if (b < 0) continue;
       const int z = (b << p.bs_log2) + (tb & ((1 << p.bs_log2) - 1));
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) {
-        const uint32_t off = hh * SM::kBoxBytes + bx * box_rows * 128;
-        tma_load_3d(sbase + off, &tmap_k, hh * (128 / KV::kBytes), g, z, bar);
-        tma_load_3d(sbase + H * SM::kBoxBytes + off, &tmap_v, hh * (128 / KV::kBytes), g, z, bar);
-      }
+      for (int hh = 0; hh < H; ++hh)
+        tma_load_3d(sbase + hh * SM::kBoxBytes + bx * box_rows * 128, map,
+                    hh * (128 / KV::kBytes), g, z, bar);
     }
   };
 
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(NW * 32)
           *reinterpret_cast<uint4*>(base + r * 128 + ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
         }
       }
+      fence_proxy_async();   // these generic writes precede the TMA refill of the stage
       __syncwarp();
     }
     const uint32_t kb_a = smem_u32(kb), vb_a = smem_u32(vb);
@@ -352,8 +355,7 @@ __global__ void __launch_bounds__(NW * 32)
         mma_bf16(o[mt], a, pl0, pl1);
       }
     }
-    fence_proxy_async();
-    __syncwarp();
+    __syncwarp();   // every lane is done with this stage before it is refilled
   }
 
   // ---- warp epilogue: l summed over the 8 token-row lanes; rows into the idle ring ----

@@ -128,13 +128,15 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
   return PKV_OK;
 }
 
-// Transposed mma.sync kernel: 4 warps, rings of 16-token chunks (8 KiB stages
-// three deep for 16-bit head_dim 128, 4 KiB stages six deep otherwise).
+// Transposed mma.sync kernel, rings of 16-token chunks three deep per warp:
+// 16-bit head_dim 128 (8 KiB stages) runs 4 warps per CTA; rows of 128 bytes
+// (FP8, or 16-bit head_dim 64; 4 KiB stages) run 8 warps, so an SM keeps 16
+// warps busy on the per-chunk work that dominates small rows.
 template <typename KV, int D, bool QF32>
 pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
                        int num_seqs, cudaStream_t stream) {
-  constexpr int NW = 4;
-  constexpr int STAGES = (D * KV::kBytes == 256) ? 3 : 6;
+  constexpr int NW = (D * KV::kBytes == 256) ? 4 : 8;
+  constexpr int STAGES = 3;
   using SM = Mma2Smem<KV, D, NW, STAGES>;
   const int bs = 1 << mp.p.bs_log2;
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
