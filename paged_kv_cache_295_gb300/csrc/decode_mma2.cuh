@@ -244,8 +244,9 @@ __global__ void __launch_bounds__(NW * 32)
       }
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
-        const uint32_t a[4] = {e4m3x2_to_f16x2(wa[ks]), e4m3x2_to_f16x2(wb[ks]),
-                               e4m3x2_to_f16x2(wa[ks] >> 16), e4m3x2_to_f16x2(wb[ks] >> 16)};
+        uint32_t a[4];   // {row gid k, row gid+8 k, row gid k+8, row gid+8 k+8}
+        e4m3x4_to_f16x2x2(wa[ks], a[0], a[2]);
+        e4m3x4_to_f16x2x2(wb[ks], a[1], a[3]);
         mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
         if (QF32) mma_f16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
       }
@@ -336,10 +337,11 @@ __global__ void __launch_bounds__(NW * 32)
         const uint32_t hi01 = __byte_perm(A[w], B[w], 0x7362);   // bytes 4w+2, 4w+3
         const uint32_t lo89 = __byte_perm(Cw[w], Dw[w], 0x5140);
         const uint32_t hi89 = __byte_perm(Cw[w], Dw[w], 0x7362);
-        const uint32_t aA[4] = {e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo01 >> 16),
-                                e4m3x2_to_f16x2(lo89), e4m3x2_to_f16x2(lo89 >> 16)};
-        const uint32_t aB[4] = {e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi01 >> 16),
-                                e4m3x2_to_f16x2(hi89), e4m3x2_to_f16x2(hi89 >> 16)};
+        uint32_t aA[4], aB[4];   // m-tiles 2w and 2w+1
+        e4m3x4_to_f16x2x2(lo01, aA[0], aA[1]);
+        e4m3x4_to_f16x2x2(lo89, aA[2], aA[3]);
+        e4m3x4_to_f16x2x2(hi01, aB[0], aB[1]);
+        e4m3x4_to_f16x2x2(hi89, aB[2], aB[3]);
         mma_f16(o[2 * w], aA, pb0, pb1);
         mma_f16(o[2 * w + 1], aB, pb0, pb1);
       }

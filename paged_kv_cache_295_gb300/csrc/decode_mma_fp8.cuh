@@ -41,6 +41,16 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Four E4M3 codes in a 32-bit word -> two f16x2 registers: `lo` holds bytes 0
+// and 1 (byte 0 in the low half), `hi` bytes 2 and 3.  One conversion
+// instruction per register, no repacking.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // Two E4M3 codes (low byte first) -> f16x2 with the low byte in the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu),
