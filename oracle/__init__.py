@@ -22,6 +22,10 @@ architecture" (intelliparadigm 2014318), "TGI architecture" (intelliparadigm
                   contiguous K/V, then softmax(q K^T * scale) V in float64
                   ("LLM inference tutorial", sections 4.1, 4.2 get_kv, 4.4
                   MHA/GQA/MQA forward).
+* ``prefill``   - paged (chunked) prefill attention: a chunk of query tokens,
+                  the last positions of their context, attends causally over
+                  the gathered cache ("LLM inference tutorial", sections 1.2
+                  prefill phase, 4.4 forward, 6.2 chunked prefill).
 
 Every float computation here is float64 unless a step is defined by a narrower
 type (FP8 dequantisation is one float32 multiply, as stated in ``attention``).
