@@ -44,7 +44,8 @@ import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
-WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA}
+PREFILL_METRIC = "paged prefill attention: TFLOP/s (% bf16 tensor peak), prefill tokens/s"
+WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL}
 DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
@@ -83,15 +84,15 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs", fallback=None):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
             d = json.load(open(p))
-            return float(d["hbm_gbs"]), "measured"
+            return float(d[key]), "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback"
+    return (FALLBACK_HBM_GBS if fallback is None else fallback), "fallback"
 
 
 # ---------------------------------------------------------------- clocks ---
@@ -504,6 +505,256 @@ def run_e2e(st, args, dev, world):
             "timer": "host wall clock, one stream sync per step"}
 
 
+# ---------------------------------------------------------- prefill arm ---
+def prefill_alg_flops(n, ctx, num_q_heads, head_dim, causal=True) -> int:
+    """Flops of the two contractions of one prefill launch: 4 * head_dim per
+    (query token, query head, visible key) - 2 D for q.k and 2 D for p.v."""
+    n = np.asarray(n, dtype=np.int64)
+    ctx = np.asarray(ctx, dtype=np.int64)
+    keys = (n * (ctx - n) + n * (n + 1) // 2) if causal else n * ctx
+    return int(keys.sum()) * num_q_heads * 4 * head_dim
+
+
+class PrefillStep:
+    """A chunked-prefill step of ``w`` resident on one GPU: append the chunk's
+    K/V rows, then prefill attention over each sequence's paged context."""
+
+    def __init__(self, w, device, keep_src=False):
+        import torch
+        import paged_kv_cache_295_gb300 as pkv
+        from paged_kv_cache_295_gb300.engine import PagedKVCache
+        self.w, self.device = w, device
+        self.n, self.lens = W.prefill_lens(w)
+        S, hq, hkv, d, bs = len(self.n), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+        nb = W.prefill_num_blocks(w, self.lens)
+        self.eng = eng = PagedKVCache(1, hkv, d, bs, nb, pkv.BF16, device=device,
+                                      initial_free_order=W.free_order(w, nb))
+        pre, chk = [], []
+        for s in range(S):
+            eng.pool.seq_create(s)
+            pre.append(eng.pool.append_tokens(s, int(self.lens[s] - self.n[s])))
+            chk.append(eng.pool.append_tokens(s, int(self.n[s])))
+        mb = int(max(len(eng.pool.block_table(s)) for s in range(S)))
+        tables, lens_pool = eng.pool.batch_tables(list(range(S)), mb)
+        assert np.array_equal(lens_pool, self.lens)
+        self.tables_h = tables
+        self.max_q, self.max_ctx = int(self.n.max()), int(self.lens.max())
+        off = np.concatenate([[0], np.cumsum(self.lens)])
+        pre_idx = np.concatenate([np.arange(off[s], off[s + 1] - self.n[s]) for s in range(S)])
+        chk_idx = np.concatenate([np.arange(off[s + 1] - self.n[s], off[s + 1])
+                                  for s in range(S)])
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 1000)
+        U, T = int(self.lens.sum()), int(self.n.sum())
+        k_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        v_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        self.q = torch.randn((T, hq, d), generator=gen, device=device).to(torch.bfloat16)
+        pre_i = torch.from_numpy(pre_idx).to(device)
+        if pre_idx.size:
+            eng.append(0, k_src[pre_i], v_src[pre_i],
+                       torch.from_numpy(np.concatenate(pre)).to(device))
+        chk_i = torch.from_numpy(chk_idx).to(device)
+        self.kn, self.vn = k_src[chk_i].contiguous(), v_src[chk_i].contiguous()
+        self.slots = torch.from_numpy(np.concatenate(chk)).to(device)
+        self.src = (k_src, v_src, off) if keep_src else None
+        del k_src, v_src
+        self.qs_h = np.concatenate([[0], np.cumsum(self.n)]).astype(np.int32)
+        self.qs = torch.from_numpy(self.qs_h).to(device)
+        self.tables = torch.from_numpy(tables).to(device)
+        self.ctx = torch.from_numpy(self.lens.astype(np.int32)).to(device)
+        self.out = torch.empty((T, hq, d), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def run(self, ev=None):
+        self.eng.append(0, self.kn, self.vn, self.slots, device_status=self.status)
+        if ev is not None:
+            ev[0].record()
+        self.eng.prefill(0, self.q, self.qs, self.tables, self.ctx, self.max_q, self.max_ctx,
+                         out=self.out, device_status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+
+def prefill_config(w, n, lens, nb):
+    return {"workload": w.name, "num_layers": w.num_layers, "num_seqs": int(len(n)),
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+            "q_dtype": w.q_dtype, "out_dtype": "f32", "causal": True,
+            "chunk_tokens": int(n.max()), "query_tokens": int(n.sum()),
+            "cached_prefix": f"{w.chunk_tokens} x U{{0..{w.max_prefix_chunks}}} seed {w.seed}",
+            "sum_ctx": int(lens.sum()), "max_ctx": int(lens.max()), "num_blocks": int(nb),
+            "l2": f"inputs larger than L2: {int(lens.sum()) * 2 * w.num_kv_heads * w.head_dim * 2 / 1e9:.3f}"
+                  " GB of K/V per step vs 129 MB L2"}
+
+
+def run_prefill_e2e(st, args, dev, world):
+    """The prefill step through the public API from pinned host buffers: H2D of
+    q, the chunk's K/V rows, slots, query_start, tables and lengths; append +
+    prefill; D2H of the output; one stream sync."""
+    import torch
+    n = args.e2e_steps or min(args.steps, 50)
+    pin = dict(pin_memory=True)
+    host = {k: v.cpu().pin_memory() for k, v in (("q", st.q), ("kn", st.kn), ("vn", st.vn),
+                                                  ("slots", st.slots), ("qs", st.qs),
+                                                  ("tables", st.tables), ("ctx", st.ctx))}
+    devb = {k: torch.empty_like(getattr(st, k)) for k in host}
+    out_h = torch.empty(st.out.shape, dtype=torch.float32, **pin)
+    bi = sum(t.numel() * t.element_size() for t in host.values())
+    bo = out_h.numel() * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        st.eng.append(0, devb["kn"], devb["vn"], devb["slots"])
+        st.eng.prefill(0, devb["q"], devb["qs"], devb["tables"], devb["ctx"], st.max_q,
+                       st.max_ctx, out=st.out)
+        out_h.copy_(st.out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = max_over_ranks(time.perf_counter() - t, world, dev)
+    flops = sum_over_ranks(prefill_alg_flops(st.n, st.lens, st.w.num_q_heads, st.w.head_dim) * n,
+                           world, dev)
+    return {"value": round(flops / dt / 1e12, 2), "unit": "TFLOP/s", "steps": n,
+            "ms_per_step": round(dt / n * 1e3, 5), "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo),
+            "prefill_tokens_per_s": round(world * int(st.n.sum()) * n / dt, 1),
+            "timer": "host wall clock, one stream sync per step"}
+
+
+def run_prefill(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be >= 3")
+    st = PrefillStep(w, dev)
+    for _ in range(Wm):
+        st.run()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        st.run(ev[i])
+    t1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    dt = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, dev)
+    attn = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    flops = prefill_alg_flops(st.n, st.lens, w.num_q_heads, w.head_dim)
+    value = sum_over_ranks(flops * K, world, dev) / dt / 1e12
+    attn_avg = statistics.fmean(attn)
+    peak, peak_src = measured_peaks("bf16_tflops", 1900.0)
+    achieved = flops / attn_avg / 1e12
+    e2e = run_prefill_e2e(st, args, dev, world)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args)
+    if rank != 0:
+        return
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": prefill_config(w, st.n, st.lens, st.eng.num_blocks),
+        "launch": {"parallelism": f"replicas x{world}", "query_rows_per_cta": 128,
+                   "keys_per_tile": 64},
+        "prefill_tokens_per_s": round(world * int(st.n.sum()) * K / dt, 1),
+        "attention_us": round(attn_avg * 1e6, 3),
+        "attention_us_median": round(statistics.median(attn) * 1e6, 3),
+        "append_plus_attention_us": round(dt / K * 1e6, 3),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                     if peak_src == "measured" else "fallback 1900 TFLOP/s",
+                     "kernel": "paged_prefill_tc_kernel", "alg_flops_per_launch": flops},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "device_status": int(st.status.item()),
+        "kernel_sources_sha": kernel_sources_sha(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+class OraclePrefillStep:
+    """One sequence of the prefill workload on the host for the oracle; a step
+    is one query row (every head) against its visible keys."""
+
+    def __init__(self, w):
+        from oracle import attention as OA
+        self.w = w
+        self.n, self.lens = W.prefill_lens(w)
+        s = int(np.argmax(self.lens))
+        self.s, L, hkv, d = s, int(self.lens[s]), w.num_kv_heads, w.head_dim
+        r = W.rng(w.seed, 900)
+        self.K = OA.to_f64(W.store(r.standard_normal((L, hkv, d), dtype=np.float32), "bf16"),
+                           "bf16")
+        self.V = OA.to_f64(W.store(r.standard_normal((L, hkv, d), dtype=np.float32), "bf16"),
+                           "bf16")
+        self.q = OA.to_f64(W.store(r.standard_normal((int(self.n[s]), w.num_q_heads, d),
+                                                     dtype=np.float32), "bf16"), "bf16")
+
+    def run(self, i):
+        from oracle import prefill as OPF
+        n, L = int(self.n[self.s]), int(self.lens[self.s])
+        row = i % n
+        OPF.attend_rows(self.q[row:row + 1], self.K, self.V, self.w.scale, [L - n + row])
+        return (L - n + row + 1) * self.w.num_q_heads * 4 * self.w.head_dim
+
+
+def run_prefill_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    st = OraclePrefillStep(w)
+    for i in range(Wm):
+        st.run(i)
+    fl, t = 0, time.perf_counter()
+    for i in range(K):
+        fl += st.run(Wm + i)
+    dt = time.perf_counter() - t
+    value = fl / dt / 1e12
+    nb = W.prefill_num_blocks(w, st.lens)
+    sample = (f"sequence {st.s} (context {int(st.lens[st.s])}), one query row (all heads) per "
+              f"step, {K} steps, numpy float64 oracle, 1 thread")
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 8),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": prefill_config(w, st.n, st.lens, nb),
+        "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 # ------------------------------------------------- reference arm (oracle) ---
 def workload_config(w, lens, nb):
     """The workload description both arms report (no launch details)."""
@@ -622,7 +873,8 @@ def run_reference(args):
 def cpu_baseline(args):
     """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
     w = WORKLOADS[args.workload]
-    lens = W.context_lens(w)
+    prefill = isinstance(w, W.PrefillWorkload)
+    lens = W.prefill_lens(w)[1] if prefill else W.context_lens(w)
     per_step = float(np.mean(lens)) * w.num_q_heads * 1.2e-6     # ~1.2 us per token-head
     steps = int(max(2, min(10 * w.num_seqs, args.cpu_seconds / per_step)))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
@@ -636,7 +888,8 @@ def cpu_baseline(args):
         cb["cpu_model"] = _cpu_model()
         return cb
     except Exception as e:   # the baseline is reported, never the target
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": "TFLOP/s" if prefill else "GB/s", "cores": 1,
+                "kind": "oracle",
                 "sample": f"failed: {type(e).__name__}: {e}"[:200]}
 
 
@@ -653,10 +906,11 @@ def _cpu_model():
 
 def main(argv=None):
     args = parse_args(argv)
+    prefill = isinstance(WORKLOADS[args.workload], W.PrefillWorkload)
     if args.impl == "reference":
-        run_reference(args)
+        (run_prefill_reference if prefill else run_reference)(args)
     else:
-        run_ours(args)
+        (run_prefill if prefill else run_ours)(args)
 
 
 if __name__ == "__main__":

@@ -239,6 +239,45 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   int32_t partition_tokens, int32_t* device_status,
                                   pkv_stream_t stream);
 
+/* Paged prefill attention: a chunk of query tokens per sequence attends,
+ * causally, over the sequence's whole paged context ("LLM inference tutorial"
+ * section 1.2 prefill phase; section 6.2 chunked prefill; section 4.4 MHA/GQA
+ * forward).  The chunk's K/V rows must already be in the cache
+ * (reshape_and_cache), so the chunk is the LAST n_s tokens of the context.
+ *   q            : device [num_tokens, num_q_heads, 128] bf16; the chunks of all
+ *                  sequences back to back.
+ *   query_start  : device [num_seqs + 1] int32, non-decreasing, query_start[0]
+ *                  = 0 and query_start[num_seqs] <= num_tokens; sequence s owns
+ *                  rows query_start[s] .. query_start[s+1]-1 (n_s of them, 0
+ *                  allowed) of q and out.
+ *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, 128] bf16.
+ *   block_tables : device [num_seqs, max_blocks_per_seq] int32 (as in decode).
+ *   context_lens : device [num_seqs] int32, the context INCLUDING the chunk;
+ *                  n_s <= context_lens[s] <= max_context_len.
+ *   max_query_len : host upper bound of n_s (sizes the grid).
+ *   causal       : 1 - query token i of sequence s (position
+ *                  context_lens[s] - n_s + i) sees keys 0 .. its position;
+ *                  0 - it sees all context_lens[s] keys.
+ *   out          : device [num_tokens, num_q_heads, 128] float32; rows outside
+ *                  every chunk are not written.
+ * Computes out[query_start[s]+i, h, :] = softmax(scale * q . K_g^T) V_g over
+ * the visible keys, g = h / G, with float32 accumulation.  Runs on tcgen05
+ * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).
+ * Supported: head_dim 128, bf16 q and caches, G = num_q_heads / num_kv_heads
+ * <= 16, block_size a power of two in [8, 4096], 16-byte aligned q, caches and
+ * out.  Device-side problems (a bad query_start or context, a bad block) are
+ * flagged in device_status; bad rows are skipped or zeroed. */
+pkv_status paged_attention_prefill(const void* q, const int32_t* query_start,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_blocks,
+                                   int32_t max_blocks_per_seq, int32_t max_context_len,
+                                   float scale, int32_t causal, int32_t q_dtype,
+                                   int32_t kv_dtype, float* out, int32_t* device_status,
+                                   pkv_stream_t stream);
+
 /* Size of the device scratch compiled into the library for
  * paged_attention_decode_noalloc (held on every GPU that loads the library,
  * until the process exits). */

@@ -1,0 +1,394 @@
+// Paged (chunked) prefill attention on the 5th-generation tensor cores
+// (tcgen05 + TMEM), bf16 q and caches, head_dim 128.
+//
+// Prefill is the compute-bound phase ("LLM inference tutorial" section 1.2);
+// a chunk of a prompt's tokens ("LLM inference tutorial" section 6.2 chunked
+// prefill) attends, causally, over every cached key of its sequence, which the
+// kernel reads through the block table ("nano-vLLM architecture" section 4.2).
+//
+// Work split: one CTA per (query tile, KV head, sequence).  A query tile is
+// 128 accumulator rows: TQ = 128 / G consecutive query tokens times the G
+// query heads that share the KV head ("LLM inference tutorial" section 4.4
+// GQA), row r = token (r / G), head (r % G), so every K/V byte a CTA loads
+// serves all G heads.  The CTA walks its keys in 64-token tiles:
+//
+//   S  = Q K^T      tcgen05.mma M=128 N=64  K=128   A = Q   (smem, K-major)
+//                                                   B = K tile (smem, K-major)
+//   P  = 2^(S*scale*log2e - m)  in the softmax warps, one TMEM lane = one row
+//   O += P V        tcgen05.mma M=128 N=128 K=64    A = P   (smem, K-major,
+//                                                        bf16 hi + lo parts)
+//                                                   B = V tile (smem, MN-major)
+//
+// S (two 64-column buffers) and O (128 columns) live in TMEM.  Warp roles:
+// warps 0-3 softmax (warp w owns TMEM lanes 32w..32w+31, i.e. rows), warp 4
+// TMA producer (lanes issue one tile's boxes in parallel, each box one block's
+// rows), warp 5 MMA issuer.  They talk only through mbarriers.  The running
+// max moves only when a tile's row max exceeds it by more than 2^8, so O is
+// rarely rescaled; a warp that must rescale loads its O lanes, scales and
+// stores them after PV(j-1) completed.  Every wait is bounded (2 s) and gives
+// up when another role has given up; TMEM is released before the CTA exits.
+#pragma once
+
+#include "decode_tc.cuh"
+
+namespace pkv {
+
+constexpr int kPfRows = 128;   // accumulator rows per CTA (M)
+constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
+constexpr int kPfD = 128;
+constexpr int kPfThreads = 192;
+constexpr int kPfStages = 3;
+
+struct PrefillParams {
+  const __nv_bfloat16* q;        // [T, Hq, D]
+  const int32_t* query_start;    // [S + 1]
+  const int32_t* block_tables;   // [S, max_blocks_per_seq]
+  const int32_t* context_lens;   // [S]
+  float* out;                    // [T, Hq, D]
+  int32_t* status;
+  int64_t num_blocks;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t max_blocks_per_seq;
+  int32_t bs_log2;
+  int32_t box_rows;              // min(block_size, 64)
+  int32_t tile_tokens;           // TQ = 128 / G
+  int32_t causal;
+  int32_t max_context_len;       // host bound: larger context_lens are flagged
+  int32_t num_tokens;            // T: rows of q and out
+  float qk_scale_log2;
+};
+
+struct PfLayout {
+  // [Q: 2 x 16 KB][P buffer 0: hi 16 KB, lo 16 KB][P buffer 1][stages: K 16 KB, V 16 KB]
+  static constexpr int kQHalf = kPfRows * 128;         // [128 rows][128 B]
+  static constexpr int kQ = 0;
+  static constexpr int kP = 2 * kQHalf;
+  static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
+  static constexpr int kPBuf = 2 * kPPart;             // hi + lo
+  static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
+  static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
+  static constexpr int kStages = kP + 2 * kPBuf;
+  static constexpr size_t bytes(int stages) {
+    return 1024 + static_cast<size_t>(kStages) + static_cast<size_t>(stages) * kStage;
+  }
+};
+
+// Valid-key mask of one 64-key tile: inside the context and in a block whose
+// table entry is a real block.  Bad entries are flagged once per CTA by the
+// producer.
+__device__ __forceinline__ uint64_t pf_tile_mask(const PrefillParams& p, const int32_t* bt_row,
+                                                 int k0, int ctx) {
+  uint64_t m = 0;
+  const int bs = 1 << p.bs_log2;
+  const int step = bs < kPfKeys ? bs : kPfKeys;
+  for (int c = 0; c < kPfKeys; c += step) {
+    const int kp = k0 + c;
+    if (kp >= ctx) break;
+    const int32_t b = __ldg(bt_row + (kp >> p.bs_log2));
+    if (b < 0 || b >= p.num_blocks) continue;
+    const int n = min(step, ctx - kp);
+    const uint64_t run = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+    m |= run << c;
+  }
+  return m;
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kPfThreads)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+  using LY = PfLayout;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int TQ = p.tile_tokens;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
+  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sma = smem_u32(sm);
+  volatile int* abort_flag = &abort_sh;
+
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int tile = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int q0 = __ldg(p.query_start + s);
+  const int q1 = __ldg(p.query_start + s + 1);
+  if (q0 < 0 || q1 < q0 || q1 > p.num_tokens) {   // rows outside q / out: touch nothing
+    if (blockIdx.x == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    return;
+  }
+  const int n = q1 - q0;
+  if (tile == 0 && tid == 0 && n > static_cast<int>(gridDim.x) * TQ)
+    flag_status(p.status, PKV_DEV_BAD_CONTEXT);   // more queries than max_query_len
+  const int tok0 = tile * TQ;
+  if (n <= 0 || tok0 >= n) return;
+  int ctx = __ldg(p.context_lens + s);
+  const int cap = min(p.max_context_len, p.max_blocks_per_seq << p.bs_log2);
+  if (ctx < n || ctx > cap) {   // queries must be the last n of a context the table covers
+    if (tile == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    const int ntok = min(TQ, n - tok0);
+    for (int i = tid; i < ntok * G * kPfD; i += kPfThreads) {
+      const int t = i / (G * kPfD), r = i % (G * kPfD);
+      p.out[(static_cast<int64_t>(q0 + tok0 + t) * p.num_q_heads + g * G) * kPfD + r] = 0.f;
+    }
+    return;
+  }
+  const int tok_end = min(tok0 + TQ, n);
+  const int nkeys = p.causal ? ctx - n + tok_end : ctx;
+  const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
+  const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
+
+  // Q (A operand of QK): row r = token tok0 + r / G, head g*G + r % G; 16-byte
+  // chunks into two 128-byte-swizzled halves.  Rows past the chunk are zero.
+  for (int i = tid; i < kPfRows * 16; i += kPfThreads) {
+    const int r = i >> 4, u = i & 15, hh = u >> 3, uu = u & 7;
+    const int t = tok0 + r / G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < TQ * G && t < n)
+      v = *reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(q0 + t) * p.num_q_heads + g * G + r % G) * kPfD + 8 * u);
+    *reinterpret_cast<uint4*>(sm + LY::kQ + hh * LY::kQHalf + swz(r, uu)) = v;
+  }
+  if (tid == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&empty[st]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&s_full[b]), 1);
+      mbar_init(smem_u32(&s_free[b]), 4);
+      mbar_init(smem_u32(&p_full[b]), 4);
+      mbar_init(smem_u32(&o_done[b]), 1);
+    }
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(
+                     smem_u32(&tmem_base_sh))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tmem_base_sh;   // S buffers at columns 0 / 64, O at 128
+  const uint32_t tmO = tm + 2 * kPfKeys;
+
+  if (warp == 4) {
+    // ------------------------------ TMA producer ------------------------------
+    const int box_rows = p.box_rows;
+    const int nbox = kPfKeys / box_rows;
+    bool flagged = false;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % STAGES;
+      if (j >= STAGES) {
+        bool ok = true;
+        if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      const int k0 = j * kPfKeys;
+      const uint32_t bar = smem_u32(&full[st]);
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int bx = 0; bx < nbox; ++bx) {
+          const int kb = k0 + bx * box_rows;
+          if (kb >= ctx) break;
+          const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
+          if (b >= 0 && b < p.num_blocks) {
+            bytes += 4 * box_rows * 128;
+          } else if (!flagged) {
+            flag_status(p.status, PKV_DEV_BAD_BLOCK);
+            flagged = true;
+          }
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+      }
+      __syncwarp();
+      const uint32_t sbase = sma + LY::kStages + st * LY::kStage;
+      for (int k = lane; k < 4 * nbox; k += 32) {   // (box, K/V, half) per lane
+        const int bx = k >> 2, kv = (k >> 1) & 1, hh = k & 1;
+        const int kb = k0 + bx * box_rows;
+        if (kb >= ctx) continue;
+        const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
+        if (b < 0 || b >= p.num_blocks) continue;
+        const int z = (b << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
+        const uint32_t off = kv * 2 * LY::kKVHalf + hh * LY::kKVHalf + bx * box_rows * 128;
+        tma_load_3d(sbase + off, kv ? &tmap_v : &tmap_k, hh * 64, g, z, bar);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, true);
+      const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
+      int issued_qk = 0, issued_pv = 0;
+      for (int j = 0; j <= ntiles; ++j) {
+        if (j < ntiles) {
+          if (!tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
+          if (j >= 2 && !tc_wait(smem_u32(&s_free[j & 1]), ((j - 2) >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
+          const uint32_t dst = tm + (j & 1) * kPfKeys;
+#pragma unroll
+          for (int ks = 0; ks < kPfD / 16; ++ks) {
+            const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
+            const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
+            tc_mma(dst, tc_desc(sma + LY::kQ + off_q, 0, 1024), tc_desc(kb + off_k, 0, 1024),
+                   idesc_qk, ks > 0);
+          }
+          tc_commit(smem_u32(&s_full[j & 1]));
+          ++issued_qk;
+        }
+        if (j >= 1) {
+          const int jp = j - 1;
+          if (!tc_wait(smem_u32(&p_full[jp & 1]), (jp >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t vb = sma + LY::kStages + (jp % STAGES) * LY::kStage + 2 * LY::kKVHalf;
+          const uint32_t pb = sma + LY::kP + (jp & 1) * LY::kPBuf;
+#pragma unroll
+          for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+            const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
+            tc_mma(tmO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (jp > 0 || kk > 0));
+            tc_mma(tmO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+          }
+          tc_commit(smem_u32(&o_done[jp & 1]));
+          tc_commit(smem_u32(&empty[jp % STAGES]));
+          ++issued_pv;
+        }
+      }
+      if (*abort_flag) {   // let issued tensor-core work finish before TMEM is released
+        volatile int no_abort = 0;
+        if (issued_pv > 0)
+          tc_wait(smem_u32(&o_done[(issued_pv - 1) & 1]), ((issued_pv - 1) >> 1) & 1, &no_abort);
+        if (issued_qk > 0)
+          tc_wait(smem_u32(&s_full[(issued_qk - 1) & 1]), ((issued_qk - 1) >> 1) & 1, &no_abort);
+      }
+    }
+  } else {
+    // ------------------------- softmax warps 0-3 ------------------------------
+    const int r = tid;                                  // accumulator row = TMEM lane
+    const uint32_t lane_q = static_cast<uint32_t>(warp * 32) << 16;
+    const int tl = r / G;
+    const bool row_ok = r < TQ * G && tok0 + tl < n;
+    const int qpos = ctx - n + tok0 + tl;               // this row's position
+    const int last = p.causal ? qpos : ctx - 1;         // last key it sees
+    const float sl2 = p.qk_scale_log2;
+    float m = -CUDART_INF_F, l = 0.f;
+    bool alive = true;
+    for (int j = 0; j < ntiles && alive; ++j) {
+      const int k0 = j * kPfKeys;
+      const uint64_t vmask = pf_tile_mask(p, bt_row, k0, ctx);
+      if (!tc_wait(smem_u32(&s_full[j & 1]), (j >> 1) & 1, abort_flag)) alive = false;
+      if (!__all_sync(0xffffffffu, alive)) break;
+      tc_fence_after();
+      float sv[kPfKeys];
+      tc_ld32(tm + lane_q + (j & 1) * kPfKeys, sv);
+      tc_ld32(tm + lane_q + (j & 1) * kPfKeys + 32, sv + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
+      float mt = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < kPfKeys; ++c) {
+        const bool ok = row_ok && ((vmask >> c) & 1ull) && (k0 + c <= last);
+        sv[c] = ok ? sv[c] * sl2 : -CUDART_INF_F;
+        mt = fmaxf(mt, sv[c]);
+      }
+      float alpha = 1.f;
+      bool resc = false;
+      if (mt > m + 8.f) {
+        if (m != -CUDART_INF_F) {
+          alpha = exp2f(m - mt);
+          resc = true;
+        }
+        m = mt;
+      }
+      float lt = 0.f;
+#pragma unroll
+      for (int c = 0; c < kPfKeys; ++c) {
+        const float pr = sv[c] == -CUDART_INF_F ? 0.f : exp2f(sv[c] - m);
+        lt += pr;
+        sv[c] = pr;
+      }
+      l = l * alpha + lt;
+      if (__any_sync(0xffffffffu, resc)) {   // PV(j-1) must be in O before scaling it
+        if (!tc_wait(smem_u32(&o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag))
+          alive = false;
+        if (!__all_sync(0xffffffffu, alive)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kPfD; c += 32) {
+          float o[32];
+          tc_ld32(tmO + lane_q + c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc_st32(tmO + lane_q + c, o);
+        }
+      }
+      // P buffer j%2 is free once PV(j-2) is done
+      if (j >= 2 && !tc_wait(smem_u32(&o_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag))
+        alive = false;
+      if (!__all_sync(0xffffffffu, alive)) break;
+      uint8_t* pb = sm + LY::kP + (j & 1) * LY::kPBuf;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = sv[8 * u + 2 * e], b = sv[8 * u + 2 * e + 1];
+          wh[e] = pack_bf16(a, b);
+          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&wh[e]);
+          wl[e] = pack_bf16(a - __low2float(hv), b - __high2float(hv));
+        }
+        *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
+            make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+      if (r < kPfKeys && !((vmask >> r) & 1ull)) {   // V rows without cache data -> 0
+        uint8_t* vrow = sm + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          *reinterpret_cast<uint4*>(vrow + (u << 4)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + LY::kKVHalf + (u << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
+    }
+    // epilogue: this warp's O rows / l
+    bool ok = alive && tc_wait(smem_u32(&o_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1,
+                               abort_flag);
+    if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + tl) * p.num_q_heads + g * G + r % G) *
+                                kPfD;
+#pragma unroll
+      for (int c = 0; c < kPfD; c += 32) {
+        float o[32];
+        tc_ld32(tmO + lane_q + c, o);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + c + e) =
+                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tm) : "memory");
+  if (tid == 0 && *abort_flag) flag_status(p.status, PKV_DEV_TIMEOUT);
+}
+
+}  // namespace pkv

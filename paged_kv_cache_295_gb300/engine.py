@@ -14,8 +14,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, FP8_E4M3, Pool, paged_attention_decode, reshape_and_cache,
-               workspace_bytes)
+from . import (BF16, F32, FP8_E4M3, Pool, paged_attention_decode, paged_attention_prefill,
+               reshape_and_cache, workspace_bytes)
 
 
 def _torch():
@@ -76,6 +76,13 @@ class PagedKVCache:
                                       k_scale=ks, v_scale=vs, workspace=workspace,
                                       partition=partition, device_status=device_status,
                                       stream=stream)
+
+    def prefill(self, layer, q, query_start, block_tables, context_lens, max_query_len,
+                max_context_len, causal=True, out=None, device_status=None, stream=None):
+        return paged_attention_prefill(q, query_start, self.k_cache(layer), self.v_cache(layer),
+                                       block_tables, context_lens, self.scale, max_query_len,
+                                       max_context_len, causal=causal, out=out,
+                                       device_status=device_status, stream=stream)
 
     def workspace_for(self, num_seqs, num_q_heads, max_context_len, partition=0, device="cuda"):
         torch = _torch()

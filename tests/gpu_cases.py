@@ -194,3 +194,77 @@ def run_gpu(case: SmallCase, partition=0, layers=None, tables=None):
         outs.append(out.cpu().numpy())
     torch.cuda.synchronize()
     return eng, outs, int(status.item())
+
+
+def make_prefill(w, chunk, prefix, seed=0, bad_block=None):
+    """A seeded chunked-prefill step: the oracle pool and the C pool hand out the
+    same slots; the cached prefix rows are placed by the oracle's append; the
+    chunk's rows are left for the GPU append.  Returns (device tensors, the
+    oracle's host arrays after the chunk's append, max chunk, max context)."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    n = np.asarray(chunk, dtype=np.int64)
+    ctx = n + np.asarray(prefix, dtype=np.int64)
+    S, hq, hkv, d, bs = len(n), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    nb = W.prefill_num_blocks(w, ctx) + 2
+    order = W.rng(w.seed + seed, 2).permutation(nb).astype(np.int32)
+    op = OP.Pool(1, hkv, d, bs, 2, nb, initial_free_order=order.tolist())
+    cp = pkv.Pool(1, hkv, d, bs, 1, num_blocks=nb, initial_free_order=order)
+    pre_slots, chunk_slots = [], []
+    for s in range(S):
+        op.seq_create(s)
+        cp.seq_create(s)
+        a = np.asarray(op.seq_append_tokens(s, int(ctx[s] - n[s])), dtype=np.int64)
+        b = np.asarray(op.seq_append_tokens(s, int(n[s])), dtype=np.int64)
+        assert np.array_equal(cp.append_tokens(s, int(ctx[s] - n[s])), a)
+        assert np.array_equal(cp.append_tokens(s, int(n[s])), b)
+        pre_slots.append(a)
+        chunk_slots.append(b)
+    mb = max(len(op.tables[s]) for s in range(S)) + 1
+    t_o, _ = op.padded_tables(list(range(S)), mb, pad=-1)
+    t_c, _ = cp.batch_tables(list(range(S)), mb)
+    tables = np.asarray(t_o, dtype=np.int32)
+    assert np.array_equal(tables, t_c)
+    if bad_block is not None:                  # (seq, logical block) -> out-of-range id
+        tables[bad_block] = nb + 5
+    r = W.rng(w.seed + seed, 3)
+    U = int(ctx.sum())
+    k_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
+    v_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
+    T = int(n.sum())
+    q = W.store(r.standard_normal((T, hq, d), dtype=np.float32), "bf16")
+    off = np.concatenate([[0], np.cumsum(ctx)])
+    pre_idx = np.concatenate([np.arange(off[s], off[s] + ctx[s] - n[s]) for s in range(S)])
+    chk_idx = np.concatenate([np.arange(off[s] + ctx[s] - n[s], off[s + 1]) for s in range(S)])
+    ps = np.concatenate(pre_slots) if pre_slots else np.zeros(0, np.int64)
+    cs = np.concatenate(chunk_slots)
+    kc = np.full((nb, bs, hkv, d), POISON["bf16"][1], dtype=np.uint16)
+    vc = kc.copy()
+    OA.reshape_and_cache(k_rows[pre_idx], v_rows[pre_idx], ps, kc, vc, "bf16", "bf16")
+    dev = {
+        "kc": to_torch(kc, "bf16"), "vc": to_torch(vc, "bf16"),
+        "kn": to_torch(k_rows[chk_idx], "bf16"), "vn": to_torch(v_rows[chk_idx], "bf16"),
+        "slots": torch.from_numpy(cs).cuda(), "q": to_torch(q, "bf16"),
+        "tables": torch.from_numpy(tables).cuda(),
+        "ctx": torch.from_numpy(ctx.astype(np.int32)).cuda(),
+        "qs": torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).cuda(),
+    }
+    OA.reshape_and_cache(k_rows[chk_idx], v_rows[chk_idx], cs, kc, vc, "bf16", "bf16")
+    host = {"kc": kc, "vc": vc, "q": q, "tables": tables, "ctx": ctx,
+            "qs": np.concatenate([[0], np.cumsum(n)])}
+    return dev, host, int(n.max()), int(ctx.max())
+
+
+def run_prefill_gpu(w, dev, max_q, max_ctx, causal=True, status=None):
+    """GPU append of the chunk rows, then paged_attention_prefill (float32 out)."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    pkv.reshape_and_cache(dev["kn"], dev["vn"], dev["slots"], dev["kc"], dev["vc"],
+                          device_status=status)
+    out = torch.full((dev["q"].shape[0], w.num_q_heads, w.head_dim), float("nan"),
+                     dtype=torch.float32, device="cuda")
+    pkv.paged_attention_prefill(dev["q"], dev["qs"], dev["kc"], dev["vc"], dev["tables"],
+                                dev["ctx"], w.scale, max_q, max_ctx, causal=causal, out=out,
+                                device_status=status)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()

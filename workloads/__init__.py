@@ -79,6 +79,65 @@ RAGGED_FP8_LAYER = DecodeWorkload("ragged_fp8_1layer", 256, 32, 32, 128, 16, FP8
 EXTRA = (RAGGED_FP8_LAYER,)
 
 
+@dataclass(frozen=True)
+class PrefillWorkload:
+    """One chunked-prefill step ("LLM inference tutorial" section 6.2: prompts
+    cut into chunks of ``chunk_size`` = 512 tokens, at most ``max_batch_tokens``
+    = 8192 tokens per batch).  Every sequence brings one chunk of
+    ``chunk_tokens`` new tokens; its earlier chunks (``chunk_tokens`` x
+    U{0 .. max_prefix_chunks}) are already in the cache."""
+    name: str
+    num_seqs: int
+    chunk_tokens: int
+    max_prefix_chunks: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    seed: int
+    kv_dtype: str = BF16
+    q_dtype: str = BF16
+    num_layers: int = 1
+    pool_slack: float = 1.5
+    chunk_fixed: tuple = ()           # per-sequence chunk lengths (small cases)
+    prefix_fixed: tuple = ()          # per-sequence cached prefix lengths
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+
+# 7B-shaped layer (32 heads x 128): 16 sequences x 512-token chunks = 8192 tokens.
+PREFILL_7B = PrefillWorkload("chunked_prefill_7b_bf16", 16, 512, 7, 32, 32, 128, 16, seed=5)
+# 70B-shaped GQA layer (64 query / 8 KV heads), blocks of 128 tokens, prompts to 8192.
+PREFILL_70B = PrefillWorkload("chunked_prefill_70b_gqa8_bf16", 16, 512, 15, 64, 8, 128, 128,
+                              seed=6)
+# Small ragged case the oracle finishes in seconds.
+PREFILL_TINY = PrefillWorkload("tiny_prefill_bf16", 3, 0, 0, 8, 2, 128, 16, seed=7,
+                               chunk_fixed=(5, 130, 64), prefix_fixed=(0, 37, 300))
+PREFILL = (PREFILL_TINY, PREFILL_7B, PREFILL_70B)
+
+
+def prefill_lens(w: PrefillWorkload):
+    """(chunk lengths, context lengths after the chunk) per sequence."""
+    if w.chunk_fixed:
+        n = np.asarray(w.chunk_fixed, dtype=np.int64)
+        pre = np.asarray(w.prefix_fixed, dtype=np.int64)
+    else:
+        n = np.full(w.num_seqs, w.chunk_tokens, dtype=np.int64)
+        pre = w.chunk_tokens * rng(w.seed, 1).integers(0, w.max_prefix_chunks + 1,
+                                                       size=w.num_seqs).astype(np.int64)
+    return n, pre + n
+
+
+def prefill_num_blocks(w: PrefillWorkload, ctx: np.ndarray) -> int:
+    return int(math.ceil(w.pool_slack * int(np.maximum(1, -(-ctx // w.block_size)).sum())))
+
+
 def rng(seed: int, stream: int = 0) -> np.random.Generator:
     """PCG64 generator for (workload seed, sub-stream)."""
     return np.random.default_rng([seed, stream])
