@@ -74,24 +74,34 @@ struct PfLayout {
   }
 };
 
-// Valid-key mask of one 64-key tile: inside the context and in a block whose
-// table entry is a real block.  Bad entries are flagged once per CTA by the
-// producer.
-__device__ __forceinline__ uint64_t pf_tile_mask(const PrefillParams& p, const int32_t* bt_row,
-                                                 int k0, int ctx) {
-  uint64_t m = 0;
-  const int bs = 1 << p.bs_log2;
-  const int step = bs < kPfKeys ? bs : kPfKeys;
-  for (int c = 0; c < kPfKeys; c += step) {
-    const int kp = k0 + c;
-    if (kp >= ctx) break;
-    const int32_t b = __ldg(bt_row + (kp >> p.bs_log2));
-    if (b < 0 || b >= p.num_blocks) continue;
-    const int n = min(step, ctx - kp);
-    const uint64_t run = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
-    m |= run << c;
-  }
-  return m;
+// 2^x with the MUFU instruction (relative error about 2^-22; 2^-inf = +0,
+// results below 2^-126 flush to 0, which only drops terms that small).
+__device__ __forceinline__ float pf_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 64 consecutive TMEM columns of this warp's 32 lanes -> 64 registers, with one
+// wait for both loads.
+__device__ __forceinline__ void pf_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+#define PKV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
+      : "r"(taddr));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : PKV_R8(32), PKV_R8(40), PKV_R8(48), PKV_R8(56)
+      : "r"(taddr + 32));
+#undef PKV_R8
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 template <int STAGES>
@@ -105,6 +115,7 @@ __global__ void __launch_bounds__(kPfThreads)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
   __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+  __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -182,44 +193,54 @@ __global__ void __launch_bounds__(kPfThreads)
 
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
+    // Lane i looks up box i's block (one round trip per tile, issued before the
+    // wait for the stage), lane 0 publishes the tile's key mask next to the
+    // stage and arms its barrier, and each lane with a real block issues its
+    // box's four copies (K and V, two 64-column halves).
     const int box_rows = p.box_rows;
     const int nbox = kPfKeys / box_rows;
     bool flagged = false;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % STAGES;
+      const int k0 = j * kPfKeys;
+      const int kb = k0 + lane * box_rows;
+      int32_t blk = -1;
+      if (lane < nbox && kb < ctx) {
+        const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
+        blk = (b >= 0 && b < p.num_blocks) ? b : -2;
+      }
+      const uint32_t valid = __ballot_sync(0xffffffffu, blk >= 0);
+      if (__ballot_sync(0xffffffffu, blk == -2) && !flagged) {
+        if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+        flagged = true;
+      }
       if (j >= STAGES) {
         bool ok = true;
         if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      const int k0 = j * kPfKeys;
       const uint32_t bar = smem_u32(&full[st]);
       if (lane == 0) {
-        uint32_t bytes = 0;
+        uint64_t m = 0;
         for (int bx = 0; bx < nbox; ++bx) {
-          const int kb = k0 + bx * box_rows;
-          if (kb >= ctx) break;
-          const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
-          if (b >= 0 && b < p.num_blocks) {
-            bytes += 4 * box_rows * 128;
-          } else if (!flagged) {
-            flag_status(p.status, PKV_DEV_BAD_BLOCK);
-            flagged = true;
-          }
+          if (!((valid >> bx) & 1u)) continue;
+          const int rows = min(box_rows, ctx - (k0 + bx * box_rows));
+          const uint64_t run = rows >= 64 ? ~0ull : ((1ull << rows) - 1ull);
+          m |= run << (bx * box_rows);
         }
-        mbar_arrive_expect_tx(bar, bytes);
+        key_mask[st] = m;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(valid)) * 4u * box_rows * 128u);
       }
       __syncwarp();
-      const uint32_t sbase = sma + LY::kStages + st * LY::kStage;
-      for (int k = lane; k < 4 * nbox; k += 32) {   // (box, K/V, half) per lane
-        const int bx = k >> 2, kv = (k >> 1) & 1, hh = k & 1;
-        const int kb = k0 + bx * box_rows;
-        if (kb >= ctx) continue;
-        const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
-        if (b < 0 || b >= p.num_blocks) continue;
-        const int z = (b << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
-        const uint32_t off = kv * 2 * LY::kKVHalf + hh * LY::kKVHalf + bx * box_rows * 128;
-        tma_load_3d(sbase + off, kv ? &tmap_v : &tmap_k, hh * 64, g, z, bar);
+      if (blk >= 0) {
+        const uint32_t sbase = sma + LY::kStages + st * LY::kStage + lane * box_rows * 128;
+        const int z = (blk << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // (K/V, half)
+          const int kv = k >> 1, hh = k & 1;
+          tma_load_3d(sbase + kv * 2 * LY::kKVHalf + hh * LY::kKVHalf, kv ? &tmap_v : &tmap_k,
+                      hh * 64, g, z, bar);
+        }
       }
     }
   } else if (warp == 5) {
@@ -283,40 +304,58 @@ __global__ void __launch_bounds__(kPfThreads)
     bool alive = true;
     for (int j = 0; j < ntiles && alive; ++j) {
       const int k0 = j * kPfKeys;
-      const uint64_t vmask = pf_tile_mask(p, bt_row, k0, ctx);
-      if (!tc_wait(smem_u32(&s_full[j & 1]), (j >> 1) & 1, abort_flag)) alive = false;
+      // S(j) ready implies the stage's copies landed; waiting on the stage's
+      // barrier as well makes the producer's key mask for it visible here.
+      if (!tc_wait(smem_u32(&s_full[j & 1]), (j >> 1) & 1, abort_flag) ||
+          !tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag))
+        alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
+      const uint64_t vmask = key_mask[j % STAGES];
+      // keys of this tile the row sees: those with cache data, up to `last`
+      const int lim = last - k0 + 1;
+      uint64_t rmask = lim >= kPfKeys ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1ull));
+      rmask = row_ok ? (rmask & vmask) : 0ull;
+      const bool dense = __all_sync(0xffffffffu, rmask == ~0ull);
       tc_fence_after();
       float sv[kPfKeys];
-      tc_ld32(tm + lane_q + (j & 1) * kPfKeys, sv);
-      tc_ld32(tm + lane_q + (j & 1) * kPfKeys + 32, sv + 32);
+      pf_ld64(tm + lane_q + (j & 1) * kPfKeys, sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
-      float mt = -CUDART_INF_F;
+      float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+      if (dense) {   // warp-uniform: no key of the tile is masked for any row
 #pragma unroll
-      for (int c = 0; c < kPfKeys; ++c) {
-        const bool ok = row_ok && ((vmask >> c) & 1ull) && (k0 + c <= last);
-        sv[c] = ok ? sv[c] * sl2 : -CUDART_INF_F;
-        mt = fmaxf(mt, sv[c]);
+        for (int c = 0; c < kPfKeys; ++c) {
+          sv[c] *= sl2;
+          mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+        }
+      } else {
+        const uint32_t mlo = static_cast<uint32_t>(rmask), mhi = static_cast<uint32_t>(rmask >> 32);
+#pragma unroll
+        for (int c = 0; c < kPfKeys; ++c) {
+          const bool ok = ((c < 32 ? mlo : mhi) >> (c & 31)) & 1u;
+          sv[c] = ok ? sv[c] * sl2 : -CUDART_INF_F;
+          mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+        }
       }
+      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       float alpha = 1.f;
       bool resc = false;
       if (mt > m + 8.f) {
         if (m != -CUDART_INF_F) {
-          alpha = exp2f(m - mt);
+          alpha = pf_ex2(m - mt);
           resc = true;
         }
         m = mt;
       }
-      float lt = 0.f;
+      const float mu = m == -CUDART_INF_F ? 0.f : m;   // rows with nothing seen yet: p = 0
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kPfKeys; ++c) {
-        const float pr = sv[c] == -CUDART_INF_F ? 0.f : exp2f(sv[c] - m);
-        lt += pr;
-        sv[c] = pr;
+        sv[c] = pf_ex2(sv[c] - mu);   // 2^-inf = 0 for masked keys
+        ls4[c & 3] += sv[c];
       }
-      l = l * alpha + lt;
+      l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
       if (__any_sync(0xffffffffu, resc)) {   // PV(j-1) must be in O before scaling it
         if (!tc_wait(smem_u32(&o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag))
           alive = false;
@@ -340,11 +379,11 @@ __global__ void __launch_bounds__(kPfThreads)
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; ++e) {   // bf16 hi part, then the bf16 of what it left
           const float a = sv[8 * u + 2 * e], b = sv[8 * u + 2 * e + 1];
           wh[e] = pack_bf16(a, b);
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&wh[e]);
-          wl[e] = pack_bf16(a - __low2float(hv), b - __high2float(hv));
+          wl[e] = pack_bf16(a - __uint_as_float(wh[e] << 16),
+                            b - __uint_as_float(wh[e] & 0xFFFF0000u));
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
