@@ -45,7 +45,8 @@ import workloads as W  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
 PREFILL_METRIC = "paged prefill attention: TFLOP/s (% bf16 tensor peak), prefill tokens/s"
-WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL}
+FORK_METRIC = "copy-on-write block copies of a beam fork: GB/s moved (% HBM peak)"
+WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL + W.FORK}
 DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
@@ -755,6 +756,191 @@ def run_prefill_reference(args):
     }), flush=True)
 
 
+# ------------------------------------------------------- beam-fork arm ---
+class ForkStep:
+    """Beam forks over a resident pool: prompts appended, each forked into
+    beams, one decode token per beam appended through the pool - the
+    copy-on-write pairs that produces are this step's copy_blocks work."""
+
+    def __init__(self, w, device):
+        import torch
+        import paged_kv_cache_295_gb300 as pkv
+        from paged_kv_cache_295_gb300.engine import PagedKVCache
+        self.w = w
+        lens = W.fork_prompt_lens(w)
+        bs = w.block_size
+        nb = int(math.ceil(w.pool_slack * (int((-(-lens // bs)).sum()) + w.num_prompts * w.beams)))
+        self.eng = eng = PagedKVCache(w.num_layers, w.num_kv_heads, w.head_dim, bs, nb, pkv.BF16,
+                                      device=device, initial_free_order=W.free_order(w, nb),
+                                      poison=False)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 1000)
+        for layer in range(w.num_layers):   # every block gets data (whole pool, one layer at a time)
+            eng.storage[layer].copy_(torch.randn(eng.storage[layer].shape, generator=gen,
+                                                 device=device).to(torch.bfloat16))
+        beams = []
+        for s, n in enumerate(lens):
+            eng.pool.seq_create(s)
+            eng.pool.append_tokens(s, int(n), want_slots=False)
+            beams.append(s)
+        nid = len(lens)
+        for s, n in enumerate(lens):
+            for _ in range(w.beams - 1):
+                eng.pool.seq_fork_prefix(nid, s, int(n))
+                beams.append(nid)
+                nid += 1
+        eng.pool.append_slots(beams)
+        self.pairs_h = eng.pool.take_copies()
+        self.pairs = torch.from_numpy(self.pairs_h).to(device)
+        self.lens = lens
+        plane = eng.storage[0, 0]
+        self.block_bytes = plane[0].numel() * plane.element_size()
+        self.planes = 2 * w.num_layers
+        self.nb = nb
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def moved_bytes(self) -> int:
+        """Read + written bytes of one copy_blocks launch."""
+        return 2 * int(self.pairs_h.shape[0]) * self.planes * self.block_bytes
+
+    def run(self):
+        import paged_kv_cache_295_gb300 as pkv
+        pkv.copy_blocks(self.eng.storage, self.pairs, device_status=self.status)
+
+
+def fork_config(w, lens, npairs, nb):
+    return {"workload": w.name, "num_layers": w.num_layers, "num_prompts": w.num_prompts,
+            "beams": w.beams, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+            "prompt_lens": f"uniform[{w.ctx_lo},{w.ctx_hi}] seed {w.seed}, no multiple of the "
+                           "block size", "copy_pairs": int(npairs), "planes": 2 * w.num_layers,
+            "num_blocks": int(nb),
+            "l2": "inputs larger than L2: each launch copies "
+                  f"{npairs * 2 * w.num_layers * w.block_size * w.num_kv_heads * w.head_dim * 2 / 1e9:.2f}"
+                  " GB vs 129 MB L2"}
+
+
+def run_fork(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be >= 3")
+    st = ForkStep(w, dev)
+    for _ in range(Wm):
+        st.run()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        ev[i][0].record()
+        st.run()
+        ev[i][1].record()
+    t1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    dt = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, dev)
+    ker = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    moved = st.moved_bytes()
+    value = sum_over_ranks(moved * K, world, dev) / dt / 1e9
+    peak, peak_src = measured_peaks()
+    achieved = moved / statistics.fmean(ker) / 1e9
+    # e2e: the pairs from pinned host memory, the copies, the status word back
+    pairs_h = torch.from_numpy(st.pairs_h).pin_memory()
+    pairs_d = torch.empty_like(st.pairs)
+    stat_h = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    import paged_kv_cache_295_gb300 as pkv
+    stream = torch.cuda.current_stream(dev)
+    n_e2e = args.e2e_steps or min(K, 200)
+
+    def one():
+        pairs_d.copy_(pairs_h, non_blocking=True)
+        pkv.copy_blocks(st.eng.storage, pairs_d, device_status=st.status)
+        stat_h.copy_(st.status, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one()
+    barrier(world)
+    t = time.perf_counter()
+    for _ in range(n_e2e):
+        one()
+    dte = max_over_ranks(time.perf_counter() - t, world, dev)
+    e2e = {"value": round(sum_over_ranks(moved * n_e2e, world, dev) / dte / 1e9, 2),
+           "unit": "GB/s", "steps": n_e2e, "ms_per_step": round(dte / n_e2e * 1e3, 5),
+           "h2d_bytes_per_step": int(pairs_h.numel() * 4), "d2h_bytes_per_step": 4,
+           "timer": "host wall clock, one stream sync per step"}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args)
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": FORK_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": fork_config(w, st.lens, st.pairs_h.shape[0], st.nb),
+        "launch": {"parallelism": f"replicas x{world}", "ctas": int(st.pairs_h.shape[0]) * st.planes},
+        "copy_us": round(statistics.fmean(ker) * 1e6, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "copy_blocks_kernel", "alg_bytes_per_launch": moved},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
+        "device_status": int(st.status.item()), "kernel_sources_sha": kernel_sources_sha(),
+    }), flush=True)
+
+
+def run_fork_reference(args):
+    """The oracle's copy_blocks on a host pool of the workload's plane shape:
+    each step copies the pairs of one prompt's beams (beams - 1 blocks)."""
+    from oracle import attention as OA
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    nb = 2 * w.beams
+    pool = W.store(W.rng(w.seed, 900).standard_normal(
+        (w.num_layers, 2, nb, w.block_size, w.num_kv_heads, w.head_dim), dtype=np.float32),
+        "bf16")
+    pairs = [(0, 1 + i) for i in range(w.beams - 1)]
+    for _ in range(Wm):
+        OA.copy_blocks(pool, pairs)
+    t = time.perf_counter()
+    for _ in range(K):
+        OA.copy_blocks(pool, pairs)
+    dt = time.perf_counter() - t
+    moved = 2 * len(pairs) * 2 * w.num_layers * pool[0, 0, 0].nbytes * K
+    value = moved / dt / 1e9
+    sample = (f"{len(pairs)} block copies (one prompt's beams) x {2 * w.num_layers} planes per "
+              f"step, {K} steps, numpy, 1 thread")
+    print(json.dumps({
+        "impl": "reference", "metric": FORK_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": fork_config(w, W.fork_prompt_lens(w), w.num_prompts * (w.beams - 1), 0),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 # ------------------------------------------------- reference arm (oracle) ---
 def workload_config(w, lens, nb):
     """The workload description both arms report (no launch details)."""
@@ -874,9 +1060,12 @@ def cpu_baseline(args):
     """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
     w = WORKLOADS[args.workload]
     prefill = isinstance(w, W.PrefillWorkload)
-    lens = W.prefill_lens(w)[1] if prefill else W.context_lens(w)
-    per_step = float(np.mean(lens)) * w.num_q_heads * 1.2e-6     # ~1.2 us per token-head
-    steps = int(max(2, min(10 * w.num_seqs, args.cpu_seconds / per_step)))
+    if isinstance(w, W.ForkWorkload):
+        steps = 200
+    else:
+        lens = W.prefill_lens(w)[1] if prefill else W.context_lens(w)
+        per_step = float(np.mean(lens)) * w.num_q_heads * 1.2e-6     # ~1.2 us per token-head
+        steps = int(max(2, min(10 * w.num_seqs, args.cpu_seconds / per_step)))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                RANK="0", WORLD_SIZE="1", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
@@ -906,11 +1095,14 @@ def _cpu_model():
 
 def main(argv=None):
     args = parse_args(argv)
-    prefill = isinstance(WORKLOADS[args.workload], W.PrefillWorkload)
-    if args.impl == "reference":
-        (run_prefill_reference if prefill else run_reference)(args)
+    w = WORKLOADS[args.workload]
+    if isinstance(w, W.PrefillWorkload):
+        arms = (run_prefill_reference, run_prefill)
+    elif isinstance(w, W.ForkWorkload):
+        arms = (run_fork_reference, run_fork)
     else:
-        (run_prefill if prefill else run_ours)(args)
+        arms = (run_reference, run_ours)
+    arms[0 if args.impl == "reference" else 1](args)
 
 
 if __name__ == "__main__":

@@ -126,17 +126,23 @@ pkv_status kv_pool_free_list(const pkv_pool* pool, int32_t* out, int64_t cap, in
 /* Sequences.  seq_create takes one block at once and starts at length 0, as
  * allocate_sequence in [TUT 4.2]; INVALID_ARG if seq_id exists. */
 pkv_status seq_create(pkv_pool* pool, int64_t seq_id);
-/* New sequence dst sharing src's first ntok tokens: ntok must be a positive
- * multiple of block_size and <= src's length; each shared block gets one more
- * reference [TUT 4.3].  dst's next token opens a private block, so no shared
- * block is ever written. */
+/* New sequence dst sharing src's first ntok tokens, 1 <= ntok <= src's
+ * length: the ceil(ntok / block_size) blocks holding them get one more
+ * reference each [TUT 4.3].  A partly filled last block is shared too; the
+ * first write into it by either sequence is copied on write (below).
+ * ntok = src's length forks a whole beam [TUT 4.2, copy-on-write for beam
+ * search]. */
 pkv_status seq_fork_prefix(pkv_pool* pool, int64_t dst, int64_t src, int32_t ntok);
 /* Append ONE token to each of n distinct sequences.  For the token at
  * position p: logical block p / block_size, offset p % block_size; a new block
  * is taken from the free list when that logical block is not in the table;
  * slot_mapping_out[i] = table[p / block_size] * block_size + p % block_size
- * [TUT 4.2 append_token].  All-or-nothing: NO_FREE_BLOCK / INVALID_ARG leave
- * the pool unchanged.  slot_mapping_out is a host array of n int64. */
+ * [TUT 4.2 append_token].  Copy-on-write: when that block is in the table but
+ * shared (reference count > 1), the sequence takes a new block from the
+ * free-list front in its place, drops its reference on the shared one and a
+ * (shared, new) pair is queued for pool_take_copies; the slot is in the new
+ * block.  All-or-nothing: NO_FREE_BLOCK / INVALID_ARG leave the pool
+ * unchanged.  slot_mapping_out is a host array of n int64. */
 pkv_status seq_append_slots(pkv_pool* pool, const int64_t* seq_ids, int32_t n,
                             int64_t* slot_mapping_out);
 /* Append n tokens to one sequence (a prompt).  Same rule and all-or-nothing
@@ -156,6 +162,45 @@ pkv_status seq_batch_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_
 /* Drop one reference on each block of the table, in table order (blocks that
  * reach 0 go to the free-list tail), and forget the sequence. */
 pkv_status seq_free(pkv_pool* pool, int64_t seq_id);
+
+/* Copy-on-write queue [TUT 4.2].  Writes the pending (source, destination)
+ * block pairs, oldest first, to pairs[0 .. 2 * *n) and clears the queue;
+ * *n = the number of pairs.  INVALID_ARG (queue kept) if cap < *n.  Drain it
+ * after every call that appends and run copy_blocks on the pairs before the
+ * device writes the appended tokens: within one such batch every destination
+ * is a fresh block that is nobody's source. */
+pkv_status pool_take_copies(pkv_pool* pool, int32_t* pairs, int32_t cap, int32_t* n);
+
+/* Prefix cache [TUT 4.3 PrefixCacheManager].  Entries are keyed by the token
+ * ids themselves (host int32 arrays; a hash only speeds the search and a hit
+ * is confirmed token by token).
+ *   prefix_cache_insert: remember the blocks holding seq_id's first n tokens
+ *     (ceil(n / block_size) of them; each gains a reference held by the
+ *     cache) under tokens[0 .. n), with count 1 (cache_prefix).  INVALID_ARG
+ *     if n < 1, n > the sequence's length or the prefix is already cached.
+ *   prefix_cache_lookup: the longest cached prefix of tokens[0 .. n), trying
+ *     lengths from n down (get_cached_prefix); *matched = its length (0 if
+ *     none), *nblocks = its block count and, when blocks is not NULL, the
+ *     blocks (INVALID_ARG if cap < *nblocks, count unchanged).  A hit adds one
+ *     to the entry's count.
+ *   seq_create_from_prefix: a new sequence seq_id starting with the longest
+ *     cached prefix of tokens[0 .. n) (its blocks gain a reference, the
+ *     entry's count one more; *matched its length), or a plain seq_create
+ *     when nothing matches (*matched = 0).  A partly filled last block is
+ *     copied on the first write into it.
+ *   prefix_cache_release: one fewer on the entry cached for exactly
+ *     tokens[0 .. n) (release_prefix); at zero the entry is dropped and its
+ *     blocks lose the cache's reference.  INVALID_ARG if not cached.
+ *   prefix_cache_count: that entry's count, 0 if not cached. */
+pkv_status prefix_cache_insert(pkv_pool* pool, const int32_t* tokens, int32_t n, int64_t seq_id);
+pkv_status prefix_cache_lookup(pkv_pool* pool, const int32_t* tokens, int32_t n,
+                               int32_t* matched, int32_t* blocks, int32_t cap,
+                               int32_t* nblocks);
+pkv_status seq_create_from_prefix(pkv_pool* pool, int64_t seq_id, const int32_t* tokens,
+                                  int32_t n, int32_t* matched);
+pkv_status prefix_cache_release(pkv_pool* pool, const int32_t* tokens, int32_t n);
+pkv_status prefix_cache_count(const pkv_pool* pool, const int32_t* tokens, int32_t n,
+                              int32_t* count);
 
 /* ------------------------------------------------------------------------ */
 /* Device: cache append [TUT 4.2 append_token, write half; TOPG 3.3].        */
@@ -238,6 +283,22 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   void* workspace, size_t workspace_bytes,
                                   int32_t partition_tokens, int32_t* device_status,
                                   pkv_stream_t stream);
+
+/* Copy-on-write block copies [TUT 4.2]: for each (src, dst) pair of
+ * pairs[0 .. 2n) (device int32), every plane's block dst becomes a copy of its
+ * block src.  A plane is one (layer, K or V) slice of the pool tensor
+ * [num_layers, 2, num_blocks, block_size, num_kv_heads, head_dim]:
+ * plane i's block b starts at base + i * plane_stride_bytes + b * block_bytes,
+ * so the whole pool has num_planes = 2 * num_layers, plane_stride_bytes =
+ * num_blocks * block_bytes and block_bytes = block_size * num_kv_heads *
+ * head_dim * element size.  Destinations must be distinct and no destination
+ * may be another pair's source (true of one pool_take_copies batch).  Pairs
+ * with an id outside [0, num_blocks) are skipped and flagged
+ * PKV_DEV_BAD_BLOCK.  base 16-byte aligned; block_bytes and
+ * plane_stride_bytes multiples of 16. */
+pkv_status copy_blocks(void* base, int32_t num_planes, int64_t plane_stride_bytes,
+                       int64_t block_bytes, int64_t num_blocks, const int32_t* pairs, int32_t n,
+                       int32_t* device_status, pkv_stream_t stream);
 
 /* Paged prefill attention: a chunk of query tokens per sequence attends,
  * causally, over the sequence's whole paged context ("LLM inference tutorial"

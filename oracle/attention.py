@@ -85,6 +85,15 @@ def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, src_dtype: s
                 raise ValueError(f"unsupported append {src_dtype}->{cache_dtype}")
 
 
+# -- copy-on-write: section 4.2 class docstring --------------------------------
+def copy_blocks(pool, pairs):
+    """``pool [num_layers, 2, num_blocks, ...]`` (in place): for each (src,
+    dst) pair in order, every layer's K and V rows of block ``dst`` become
+    those of block ``src``."""
+    for src, dst in pairs:
+        pool[:, :, int(dst)] = pool[:, :, int(src)]
+
+
 # -- gather: section 4.2 get_kv ------------------------------------------------
 def gather_sequence(cache, table, seq_len: int):
     """Concatenate the first ``seq_len`` rows of the table's blocks, in order."""

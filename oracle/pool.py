@@ -22,6 +22,20 @@ Follows "LLM inference tutorial" (xurj.top Tutorial/Detail/167):
   reference; this oracle keeps the count per physical block and frees a block
   when its count reaches zero (the page leaves "keep or free" open at zero;
   freeing is the reading taken);
+* section 4.2, the class docstring: copy-on-write for beam search.  A fork
+  shares the source's blocks, including a partly filled last block; the first
+  write into a block whose count is above one first moves the writer to a
+  fresh block (front of the free list) and records (old, new) in a list of
+  pending block copies, which the caller executes on the device before it
+  writes the token (``take_copies``);
+* section 4.3, ``PrefixCacheManager``: ``cache_prefix`` remembers the blocks of
+  a token prefix with count 1 (here the cache also holds one reference on each
+  of those blocks, so they outlive the sequence that wrote them);
+  ``get_cached_prefix`` tries the query's prefixes from the longest down and a
+  hit adds one to the count; ``release_prefix`` takes one off, and at zero the
+  entry is dropped together with its block references (the "free" reading of
+  the page's "keep or free").  Entries are keyed by the token tuple itself, so
+  there are no hash collisions to resolve;
 * "nano-vLLM architecture", section 4.3: ``block_bytes = 2 * num_layers *
   block_size * num_kv_heads * head_dim * dtype_size`` and ``available_blocks =
   free_memory // block_bytes``.
@@ -80,6 +94,8 @@ class Pool:
     ref: list[int] = field(init=False)
     tables: dict = field(init=False, default_factory=dict)
     lens: dict = field(init=False, default_factory=dict)
+    copies: list = field(init=False, default_factory=list)
+    prefix: dict = field(init=False, default_factory=dict)
 
     def __post_init__(self):
         if self.num_blocks <= 0 or self.block_size <= 0:
@@ -92,6 +108,8 @@ class Pool:
         self.ref = [0] * self.num_blocks
         self.tables = {}
         self.lens = {}
+        self.copies = []
+        self.prefix = {}
 
     # -- blocks (section 4.2 free list, section 4.3 reference counts) --------
     def block_alloc(self) -> int:
@@ -130,38 +148,53 @@ class Pool:
     def seq_fork_prefix(self, dst: int, src: int, ntok: int):
         """New sequence ``dst`` sharing the first ``ntok`` tokens of ``src``.
 
-        Only whole blocks are shared (``ntok`` a multiple of the block size),
-        so the next token of ``dst`` opens a private block and no block is
-        ever written through two tables (copy-on-write is not needed).
+        The ``ceil(ntok / block_size)`` blocks holding them gain a reference;
+        a partly filled last block is shared too and copied on the first
+        write into it (by either sequence).  ``ntok == len(src)`` is a full
+        fork (a beam).
         """
         if dst in self.tables or src not in self.tables:
             raise PoolError(INVALID_ARG, "bad fork ids")
-        if ntok <= 0 or ntok % self.block_size or ntok > self.lens[src]:
-            raise PoolError(INVALID_ARG, "fork length must be whole blocks of src")
-        shared = self.tables[src][: ntok // self.block_size]
+        if ntok <= 0 or ntok > self.lens[src]:
+            raise PoolError(INVALID_ARG, "fork length must be 1 .. len(src)")
+        shared = self.tables[src][: -(-ntok // self.block_size)]
         for b in shared:
             self.block_ref(b)
         self.tables[dst] = list(shared)
         self.lens[dst] = ntok
 
+    def _shared_target(self, sid: int) -> bool:
+        """The block the next token of ``sid`` goes to exists and is shared."""
+        blk = self.lens[sid] // self.block_size
+        t = self.tables[sid]
+        return blk < len(t) and self.ref[t[blk]] > 1
+
     def _needs_block(self, sid: int, extra: int) -> bool:
         n = self.lens[sid] + extra
-        return n // self.block_size >= len(self.tables[sid])
+        return n // self.block_size >= len(self.tables[sid]) or (
+            extra == 0 and self._shared_target(sid))
 
     def _append_one(self, sid: int) -> int:
         n = self.lens[sid]
         blk, off = divmod(n, self.block_size)
-        if blk >= len(self.tables[sid]):
-            self.tables[sid].append(self.block_alloc())
-        slot = self.tables[sid][blk] * self.block_size + off
+        t = self.tables[sid]
+        if blk >= len(t):
+            t.append(self.block_alloc())
+        elif self.ref[t[blk]] > 1:          # copy-on-write
+            new = self.block_alloc()
+            self.copies.append((t[blk], new))
+            self.block_free(t[blk])
+            t[blk] = new
+        slot = t[blk] * self.block_size + off
         self.lens[sid] = n + 1
         return slot
 
     def seq_append_slots(self, sids: list[int]) -> list[int]:
         """Append one token to each listed sequence; return the slot of each.
 
-        All-or-nothing: if the free list cannot cover every new block the
-        call fails before changing anything.  Repeated ids are refused.
+        All-or-nothing: if the free list cannot cover every new or
+        copied-on-write block the call fails before changing anything.
+        Repeated ids are refused.
         """
         if len(set(sids)) != len(sids):
             raise PoolError(INVALID_ARG, "repeated sequence id")
@@ -181,9 +214,74 @@ class Pool:
             raise PoolError(INVALID_ARG, "negative count")
         have = len(self.tables[sid]) * self.block_size
         need = max(0, -(-(self.lens[sid] + n - have) // self.block_size))
+        if n > 0 and self._shared_target(sid):
+            need += 1
         if need > len(self.free):
             raise PoolError(NO_FREE_BLOCK, f"need {need}, have {len(self.free)}")
         return [self._append_one(sid) for _ in range(n)]
+
+    def take_copies(self) -> list[tuple[int, int]]:
+        """The pending (source block, new block) copies, oldest first; clears them."""
+        out, self.copies = self.copies, []
+        return out
+
+    # -- prefix cache (section 4.3 PrefixCacheManager) ------------------------
+    def prefix_insert(self, tokens, sid: int):
+        """``cache_prefix``: the blocks holding ``sid``'s first ``len(tokens)``
+        tokens are remembered under ``tokens`` with count 1."""
+        key = tuple(int(t) for t in tokens)
+        if sid not in self.tables or not key or len(key) > self.lens[sid] or key in self.prefix:
+            raise PoolError(INVALID_ARG, "bad prefix insert")
+        blocks = self.tables[sid][: -(-len(key) // self.block_size)]
+        for b in blocks:
+            self.block_ref(b)
+        self.prefix[key] = {"blocks": list(blocks), "count": 1}
+
+    def prefix_lookup(self, tokens):
+        """``get_cached_prefix``: (blocks, length) of the longest cached prefix
+        of ``tokens``, trying lengths from the longest down, or None.  A hit
+        adds one to that entry's count."""
+        key = tuple(int(t) for t in tokens)
+        for length in range(len(key), 0, -1):
+            e = self.prefix.get(key[:length])
+            if e is not None:
+                e["count"] += 1
+                return list(e["blocks"]), length
+        return None
+
+    def seq_create_from_prefix(self, sid: int, tokens) -> int:
+        """New sequence whose first tokens come from the longest cached prefix
+        of ``tokens`` (its blocks gain a reference); without a hit, a plain
+        ``seq_create``.  Returns the number of tokens taken from the cache."""
+        if sid in self.tables:
+            raise PoolError(INVALID_ARG, f"sequence {sid} exists")
+        hit = self.prefix_lookup(tokens)
+        if hit is None:
+            self.seq_create(sid)
+            return 0
+        blocks, length = hit
+        for b in blocks:
+            self.block_ref(b)
+        self.tables[sid] = blocks
+        self.lens[sid] = length
+        return length
+
+    def prefix_release(self, tokens):
+        """``release_prefix``: one fewer; at zero the entry and its block
+        references go."""
+        key = tuple(int(t) for t in tokens)
+        e = self.prefix.get(key)
+        if e is None:
+            raise PoolError(INVALID_ARG, "prefix not cached")
+        e["count"] -= 1
+        if e["count"] == 0:
+            del self.prefix[key]
+            for b in e["blocks"]:
+                self.block_free(b)
+
+    def prefix_count(self, tokens) -> int:
+        e = self.prefix.get(tuple(int(t) for t in tokens))
+        return 0 if e is None else e["count"]
 
     def seq_free(self, sid: int):
         if sid not in self.tables:

@@ -68,6 +68,13 @@ _SIGS = {
     "seq_block_table": (I32, [P, I64, P, I32, C.POINTER(I32)]),
     "seq_batch_tables": (I32, [P, P, I32, I32, P, P]),
     "seq_free": (I32, [P, I64]),
+    "pool_take_copies": (I32, [P, P, I32, C.POINTER(I32)]),
+    "prefix_cache_insert": (I32, [P, P, I32, I64]),
+    "prefix_cache_lookup": (I32, [P, P, I32, C.POINTER(I32), P, I32, C.POINTER(I32)]),
+    "seq_create_from_prefix": (I32, [P, I64, P, I32, C.POINTER(I32)]),
+    "prefix_cache_release": (I32, [P, P, I32]),
+    "prefix_cache_count": (I32, [P, P, I32, C.POINTER(I32)]),
+    "copy_blocks": (I32, [P, I32, I64, I64, I64, P, I32, P, P]),
     "reshape_and_cache": (I32, [P, P, P, P, P, I32, I32, I32, I32, I64, I32, I32, P, P, P, P]),
     "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32]),
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
@@ -227,6 +234,53 @@ class Pool:
     def seq_free(self, sid: int):
         _check(library().seq_free(self._h, sid), "seq_free")
 
+    def take_copies(self) -> np.ndarray:
+        """Pending copy-on-write pairs ``[k, 2]`` int32 (source, new block); clears them."""
+        n = C.c_int32()
+        st = library().pool_take_copies(self._h, None, 0, C.byref(n))
+        if st != 0 and n.value == 0:
+            _check(st, "pool_take_copies")
+        buf = np.empty((max(n.value, 1), 2), dtype=np.int32)
+        _check(library().pool_take_copies(self._h, _np_ptr(buf), buf.shape[0], C.byref(n)),
+               "pool_take_copies")
+        return buf[: n.value]
+
+    @staticmethod
+    def _tokens(tokens):
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        return t, (_np_ptr(t) if t.size else None)
+
+    def prefix_insert(self, tokens, sid: int):
+        t, ptr = self._tokens(tokens)
+        _check(library().prefix_cache_insert(self._h, ptr, t.size, sid), "prefix_cache_insert")
+
+    def prefix_lookup(self, tokens):
+        """(matched length, blocks) of the longest cached prefix; a hit counts."""
+        t, ptr = self._tokens(tokens)
+        m, nb = C.c_int32(), C.c_int32()
+        buf = np.empty(max(1, -(-t.size // self.block_size)), dtype=np.int32)
+        _check(library().prefix_cache_lookup(self._h, ptr, t.size, C.byref(m), _np_ptr(buf),
+                                             buf.size, C.byref(nb)), "prefix_cache_lookup")
+        return m.value, buf[: nb.value].tolist()
+
+    def seq_create_from_prefix(self, sid: int, tokens) -> int:
+        t, ptr = self._tokens(tokens)
+        m = C.c_int32()
+        _check(library().seq_create_from_prefix(self._h, sid, ptr, t.size, C.byref(m)),
+               "seq_create_from_prefix")
+        return m.value
+
+    def prefix_release(self, tokens):
+        t, ptr = self._tokens(tokens)
+        _check(library().prefix_cache_release(self._h, ptr, t.size), "prefix_cache_release")
+
+    def prefix_count(self, tokens) -> int:
+        t, ptr = self._tokens(tokens)
+        c = C.c_int32()
+        _check(library().prefix_cache_count(self._h, ptr, t.size, C.byref(c)),
+               "prefix_cache_count")
+        return c.value
+
 
 # ---------------------------------------------------------------------------
 # Device calls (torch tensors in, async on the current stream).
@@ -354,6 +408,19 @@ def paged_attention_prefill(q, query_start, k_cache, v_cache, block_tables, cont
         _dev(device_status, "device_status"), _stream(stream))
     _check(st, "paged_attention_prefill")
     return out
+
+
+def copy_blocks(pool_tensor, pairs, device_status=None, stream=None):
+    """Copy-on-write copies on the pool tensor ``[L, 2, NB, bs, Hkv, D]``:
+    ``pairs`` is a device int32 ``[k, 2]`` of (source, destination) blocks."""
+    L, two, nb = pool_tensor.shape[:3]
+    plane = pool_tensor[0, 0]
+    bb = plane[0].numel() * plane.element_size()
+    k = pairs.shape[0] if pairs.dim() else 0
+    st = library().copy_blocks(_dev(pool_tensor, "pool"), L * two, nb * bb, bb, nb,
+                               _dev(pairs, "pairs") if k else None, k,
+                               _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "copy_blocks")
 
 
 def copy_kernel(src, dst, stream=None):

@@ -10,10 +10,27 @@
 //
 // The free list is a ring buffer of capacity num_blocks: a block id is in it
 // at most once, so it never overflows and both ends are O(1).
+//
+// Copy-on-write ("LLM inference tutorial" section 4.2, the class docstring:
+// beam search): forks share blocks, including a partly filled last block; the
+// first write into a block whose count is above one moves the writer to a new
+// block from the free-list front and records (old, new) in a pending-copy list
+// that the caller drains (pool_take_copies) and executes on the device
+// (copy_blocks) before writing the token.
+//
+// Prefix cache (section 4.3, PrefixCacheManager): entries map a token prefix
+// to the blocks holding it, with a count that starts at 1 (cache_prefix),
+// rises on every hit of the longest-prefix lookup (get_cached_prefix) and
+// falls on release (release_prefix); at zero the entry is dropped together
+// with the block references it held.  Lookup hashes every prefix of the query
+// in one pass (a 64-bit mix per token) and probes from the longest down; a
+// probe hit is confirmed by comparing the tokens, so collisions cannot match.
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
+#include <utility>
 #include <vector>
 
 #include "pagedkv.h"
@@ -34,6 +51,28 @@ struct Seq {
   int32_t len = 0;
 };
 
+struct PrefixEntry {
+  std::vector<int32_t> tokens;
+  std::vector<int32_t> blocks;
+  int32_t count = 0;
+};
+
+// Hash of every prefix of tokens[0..n): out[k] covers the first k+1 tokens.
+void prefix_hashes(const int32_t* tokens, int32_t n, std::vector<uint64_t>& out) {
+  out.resize(n);
+  uint64_t h = 0x243F6A8885A308D3ull;
+  for (int32_t i = 0; i < n; ++i) {
+    uint64_t x = h ^ (static_cast<uint64_t>(static_cast<uint32_t>(tokens[i])) + 0x9E3779B97F4A7C15ull);
+    x ^= x >> 30;
+    x *= 0xBF58476D1CE4E5B9ull;
+    x ^= x >> 27;
+    x *= 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    h = x;
+    out[i] = h;
+  }
+}
+
 }  // namespace
 
 struct pkv_pool {
@@ -45,6 +84,19 @@ struct pkv_pool {
   int64_t count = 0;           // number of free blocks
   std::vector<int32_t> ref;    // reference count per block (0 = free)
   std::unordered_map<int64_t, Seq> seqs;
+  std::vector<std::pair<int32_t, int32_t>> copies;   // pending copy-on-write (src, dst)
+  std::unordered_map<uint64_t, std::vector<PrefixEntry>> prefix;   // prefix hash -> entries
+
+  // The entry cached for exactly tokens[0..n) (hash h), or nullptr.
+  PrefixEntry* find_prefix(uint64_t h, const int32_t* tokens, int32_t n) {
+    auto it = prefix.find(h);
+    if (it == prefix.end()) return nullptr;
+    for (PrefixEntry& e : it->second)
+      if (static_cast<int32_t>(e.tokens.size()) == n &&
+          std::equal(e.tokens.begin(), e.tokens.end(), tokens))
+        return &e;
+    return nullptr;
+  }
 
   int32_t pop_front() {
     int32_t b = ring[head];
@@ -61,18 +113,34 @@ struct pkv_pool {
 
 namespace {
 
+// The block the sequence's next token goes to exists and is shared.
+bool shared_target(const pkv_pool* p, const Seq& s) {
+  const int64_t blk = s.len / p->cfg.block_size;
+  return blk < static_cast<int64_t>(s.table.size()) && p->ref[s.table[blk]] > 1;
+}
+
 bool seq_needs_block(const pkv_pool* p, const Seq& s) {
-  return static_cast<int64_t>(s.len / p->cfg.block_size) >= static_cast<int64_t>(s.table.size());
+  return static_cast<int64_t>(s.len / p->cfg.block_size) >=
+             static_cast<int64_t>(s.table.size()) ||
+         shared_target(p, s);
 }
 
 // Advance a sequence by one token, taking a block from the free-list front
-// when the token's logical block is not in the table yet.
+// when the token's logical block is not in the table yet, or when it is
+// shared (copy-on-write: the pending copy is recorded).  Capacity for the
+// table entry and the copy record is reserved by the callers.
 void append_one(pkv_pool* p, Seq& s) {
   const int32_t blk = s.len / p->cfg.block_size;
   if (blk >= static_cast<int32_t>(s.table.size())) {
     const int32_t b = p->pop_front();
     p->ref[b] = 1;
     s.table.push_back(b);
+  } else if (p->ref[s.table[blk]] > 1) {
+    const int32_t b = p->pop_front();
+    p->ref[b] = 1;
+    p->copies.emplace_back(s.table[blk], b);
+    --p->ref[s.table[blk]];
+    s.table[blk] = b;
   }
   ++s.len;
 }
@@ -228,10 +296,10 @@ pkv_status seq_fork_prefix(pkv_pool* p, int64_t dst, int64_t src, int32_t ntok) 
   auto it = p->seqs.find(src);
   if (it == p->seqs.end() || p->seqs.count(dst)) return PKV_ERR_INVALID_ARG;
   const int32_t bs = p->cfg.block_size;
-  if (ntok <= 0 || ntok % bs != 0 || ntok > it->second.len) return PKV_ERR_INVALID_ARG;
+  if (ntok <= 0 || ntok > it->second.len) return PKV_ERR_INVALID_ARG;
   try {
     Seq s;
-    s.table.assign(it->second.table.begin(), it->second.table.begin() + ntok / bs);
+    s.table.assign(it->second.table.begin(), it->second.table.begin() + (ntok + bs - 1) / bs);
     s.len = ntok;
     for (int32_t b : s.table) ++p->ref[b];
     p->seqs.emplace(dst, std::move(s));
@@ -260,6 +328,7 @@ pkv_status seq_append_slots(pkv_pool* p, const int64_t* ids, int32_t n, int64_t*
       Seq& s = *v[i];
       if (seq_needs_block(p, s)) s.table.reserve(s.table.size() + 1);
     }
+    p->copies.reserve(p->copies.size() + static_cast<size_t>(need));
   } catch (const std::bad_alloc&) {
     return PKV_ERR_HOST_MEMORY;
   }
@@ -280,11 +349,13 @@ pkv_status seq_append_tokens(pkv_pool* p, int64_t sid, int32_t n, int64_t* slots
   const int64_t bs = p->cfg.block_size;
   const int64_t have = static_cast<int64_t>(s.table.size()) * bs;
   const int64_t over = static_cast<int64_t>(s.len) + n - have;
-  const int64_t need = over > 0 ? (over + bs - 1) / bs : 0;
+  const int64_t cow = (n > 0 && shared_target(p, s)) ? 1 : 0;
+  const int64_t need = (over > 0 ? (over + bs - 1) / bs : 0) + cow;
   if (need > p->count) return PKV_ERR_NO_FREE_BLOCK;
   if (static_cast<int64_t>(s.len) + n > INT32_MAX) return PKV_ERR_INVALID_ARG;
   try {
     s.table.reserve(s.table.size() + need);
+    p->copies.reserve(p->copies.size() + static_cast<size_t>(cow));
   } catch (const std::bad_alloc&) {
     return PKV_ERR_HOST_MEMORY;
   }
@@ -344,6 +415,143 @@ pkv_status seq_free(pkv_pool* p, int64_t sid) {
     if (--p->ref[b] == 0) p->push_back(b);
   }
   p->seqs.erase(it);
+  return PKV_OK;
+}
+
+pkv_status pool_take_copies(pkv_pool* p, int32_t* pairs, int32_t cap, int32_t* n) {
+  if (!p || !n || cap < 0) return PKV_ERR_INVALID_ARG;
+  const int64_t k = static_cast<int64_t>(p->copies.size());
+  if (k > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  *n = static_cast<int32_t>(k);
+  if (cap < k || (!pairs && k > 0)) return PKV_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < k; ++i) {
+    pairs[2 * i] = p->copies[i].first;
+    pairs[2 * i + 1] = p->copies[i].second;
+  }
+  p->copies.clear();
+  return PKV_OK;
+}
+
+pkv_status prefix_cache_insert(pkv_pool* p, const int32_t* tokens, int32_t n, int64_t sid) {
+  if (!p || n <= 0 || !tokens) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end() || n > it->second.len) return PKV_ERR_INVALID_ARG;
+  try {
+    std::vector<uint64_t> h;
+    prefix_hashes(tokens, n, h);
+    if (p->find_prefix(h[n - 1], tokens, n)) return PKV_ERR_INVALID_ARG;
+    const int32_t bs = p->cfg.block_size;
+    PrefixEntry e;
+    e.tokens.assign(tokens, tokens + n);
+    e.blocks.assign(it->second.table.begin(), it->second.table.begin() + (n + bs - 1) / bs);
+    e.count = 1;
+    auto& bucket = p->prefix[h[n - 1]];
+    bucket.reserve(bucket.size() + 1);
+    for (int32_t b : e.blocks) ++p->ref[b];
+    bucket.push_back(std::move(e));
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+namespace {
+
+// Longest cached prefix of tokens[0..n): its entry and length, or nullptr.
+PrefixEntry* longest_prefix(pkv_pool* p, const int32_t* tokens, int32_t n, int32_t* len) {
+  std::vector<uint64_t> h;
+  prefix_hashes(tokens, n, h);
+  for (int32_t k = n; k >= 1; --k) {
+    if (PrefixEntry* e = p->find_prefix(h[k - 1], tokens, k)) {
+      *len = k;
+      return e;
+    }
+  }
+  *len = 0;
+  return nullptr;
+}
+
+}  // namespace
+
+pkv_status prefix_cache_lookup(pkv_pool* p, const int32_t* tokens, int32_t n, int32_t* matched,
+                               int32_t* blocks, int32_t cap, int32_t* nblocks) {
+  if (!p || n < 0 || (n > 0 && !tokens) || !matched || !nblocks || cap < 0)
+    return PKV_ERR_INVALID_ARG;
+  try {
+    int32_t len = 0;
+    PrefixEntry* e = n > 0 ? longest_prefix(p, tokens, n, &len) : nullptr;
+    *matched = len;
+    *nblocks = e ? static_cast<int32_t>(e->blocks.size()) : 0;
+    if (!e) return PKV_OK;
+    if (blocks && cap < *nblocks) return PKV_ERR_INVALID_ARG;
+    if (blocks) std::memcpy(blocks, e->blocks.data(), e->blocks.size() * sizeof(int32_t));
+    ++e->count;
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_create_from_prefix(pkv_pool* p, int64_t sid, const int32_t* tokens, int32_t n,
+                                  int32_t* matched) {
+  if (!p || n < 0 || (n > 0 && !tokens) || !matched) return PKV_ERR_INVALID_ARG;
+  if (p->seqs.count(sid)) return PKV_ERR_INVALID_ARG;
+  try {
+    int32_t len = 0;
+    PrefixEntry* e = n > 0 ? longest_prefix(p, tokens, n, &len) : nullptr;
+    *matched = 0;
+    if (!e) return seq_create(p, sid);
+    Seq s;
+    s.table = e->blocks;
+    s.len = len;
+    p->seqs.emplace(sid, std::move(s));
+    for (int32_t b : e->blocks) ++p->ref[b];
+    ++e->count;
+    *matched = len;
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+pkv_status prefix_cache_release(pkv_pool* p, const int32_t* tokens, int32_t n) {
+  if (!p || n <= 0 || !tokens) return PKV_ERR_INVALID_ARG;
+  try {
+    std::vector<uint64_t> h;
+    prefix_hashes(tokens, n, h);
+    auto it = p->prefix.find(h[n - 1]);
+    if (it == p->prefix.end()) return PKV_ERR_INVALID_ARG;
+    auto& bucket = it->second;
+    for (size_t i = 0; i < bucket.size(); ++i) {
+      PrefixEntry& e = bucket[i];
+      if (static_cast<int32_t>(e.tokens.size()) != n ||
+          !std::equal(e.tokens.begin(), e.tokens.end(), tokens))
+        continue;
+      if (--e.count == 0) {
+        for (int32_t b : e.blocks)
+          if (--p->ref[b] == 0) p->push_back(b);
+        bucket.erase(bucket.begin() + static_cast<std::ptrdiff_t>(i));
+        if (bucket.empty()) p->prefix.erase(it);
+      }
+      return PKV_OK;
+    }
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_ERR_INVALID_ARG;
+}
+
+pkv_status prefix_cache_count(const pkv_pool* p, const int32_t* tokens, int32_t n,
+                              int32_t* count) {
+  if (!p || n <= 0 || !tokens || !count) return PKV_ERR_INVALID_ARG;
+  try {
+    std::vector<uint64_t> h;
+    prefix_hashes(tokens, n, h);
+    const PrefixEntry* e = const_cast<pkv_pool*>(p)->find_prefix(h[n - 1], tokens, n);
+    *count = e ? e->count : 0;
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
   return PKV_OK;
 }
 

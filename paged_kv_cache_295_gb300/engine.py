@@ -14,8 +14,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, FP8_E4M3, Pool, paged_attention_decode, paged_attention_prefill,
-               reshape_and_cache, workspace_bytes)
+from . import (BF16, F32, FP8_E4M3, Pool, copy_blocks, paged_attention_decode,
+               paged_attention_prefill, reshape_and_cache, workspace_bytes)
 
 
 def _torch():
@@ -66,6 +66,16 @@ class PagedKVCache:
         vs = None if self.v_scale is None else self.v_scale[layer]
         reshape_and_cache(k_new, v_new, slot_mapping, self.k_cache(layer), self.v_cache(layer),
                           ks, vs, device_status=device_status, stream=stream)
+
+    def run_copies(self, device_status=None, stream=None):
+        """Drain the pool's copy-on-write queue and copy those blocks (every
+        layer, K and V) on the device; returns the pairs (host ``[k, 2]``)."""
+        torch = _torch()
+        pairs = self.pool.take_copies()
+        if pairs.shape[0]:
+            d = torch.from_numpy(pairs).to(self.storage.device, non_blocking=False)
+            copy_blocks(self.storage, d, device_status=device_status, stream=stream)
+        return pairs
 
     def attend(self, layer, q, block_tables, context_lens, max_context_len, out=None,
                workspace=None, partition=0, device_status=None, stream=None):

@@ -80,8 +80,9 @@ def test_c_pool_replays_oracle_bit_exact(lib, seed):
     o = OP.Pool(1, 2, 16, bs, 2, nb, initial_free_order=order)
     c = lib.Pool(1, 2, 16, bs, lib.BF16, num_blocks=nb, initial_free_order=order)
     live, nid = [], 0
+    prompts = {}                       # token ids of a few cached prefixes
     for _ in range(600):
-        op = int(r.integers(0, 7))
+        op = int(r.integers(0, 10))
         if op == 0 or not live:
             a = _status_of(lambda: o.seq_create(nid))
             b = _c_status_of(lib, lambda: c.seq_create(nid))
@@ -109,7 +110,7 @@ def test_c_pool_replays_oracle_bit_exact(lib, seed):
                 assert res_o["v"] == res_c["v"].tolist()
         elif op == 4:
             src = int(r.choice(live))
-            ntok = bs * int(r.integers(0, 3))
+            ntok = int(r.integers(0, o.lens[src] + 2))       # 0 and len+1 are refused
             a = _status_of(lambda: o.seq_fork_prefix(nid, src, ntok))
             b = _c_status_of(lib, lambda: c.seq_fork_prefix(nid, src, ntok))
             assert a == b
@@ -121,6 +122,41 @@ def test_c_pool_replays_oracle_bit_exact(lib, seed):
             o.seq_free(s)
             c.seq_free(s)
             live.remove(s)
+        elif op == 7:                    # the copy-on-write queue, drained on both
+            assert [tuple(x) for x in o.take_copies()] == [tuple(x) for x in
+                                                           c.take_copies().tolist()]
+        elif op == 8:                    # cache a prefix of a live sequence
+            s = int(r.choice(live))
+            if o.lens[s]:
+                toks = r.integers(0, 4, size=int(r.integers(1, o.lens[s] + 1))).tolist()
+                a = _status_of(lambda: o.prefix_insert(toks, s))
+                b = _c_status_of(lib, lambda: c.prefix_insert(toks, s))
+                assert a == b
+                if a == OP.OK:
+                    prompts[tuple(toks)] = True
+        elif op == 9 and prompts:        # look up / start from / release a prefix
+            key = list(list(prompts)[int(r.integers(0, len(prompts)))])
+            q = key + r.integers(0, 4, size=int(r.integers(0, 3))).tolist()
+            kind = int(r.integers(0, 3))
+            if kind == 0:
+                hit = o.prefix_lookup(q)
+                assert c.prefix_lookup(q) == ((hit[1], hit[0]) if hit else (0, []))
+            elif kind == 1:
+                res_o, res_c = {}, {}
+                a = _status_of(lambda: res_o.setdefault("v", o.seq_create_from_prefix(nid, q)))
+                b = _c_status_of(lib, lambda: res_c.setdefault("v",
+                                                              c.seq_create_from_prefix(nid, q)))
+                assert a == b and res_o.get("v") == res_c.get("v")
+                if a == OP.OK:
+                    live.append(nid)
+                nid += 1
+            else:
+                a = _status_of(lambda: o.prefix_release(key))
+                b = _c_status_of(lib, lambda: c.prefix_release(key))
+                assert a == b
+                if o.prefix_count(key) == 0:
+                    prompts.pop(tuple(key), None)
+            assert o.prefix_count(key) == c.prefix_count(key)
         else:
             b_id = int(r.integers(-1, nb + 1))
             if r.integers(0, 2):

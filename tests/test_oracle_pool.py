@@ -106,9 +106,10 @@ def test_errors():
     with pytest.raises(P.PoolError) as e:
         pool.block_ref(1)
     assert e.value.status == P.REFCOUNT
-    with pytest.raises(P.PoolError) as e:
-        pool.seq_fork_prefix(3, 0, 3)            # not whole blocks
-    assert e.value.status == P.INVALID_ARG
+    for bad in (0, 5):                           # nothing to share / beyond the length
+        with pytest.raises(P.PoolError) as e:
+            pool.seq_fork_prefix(3, 0, bad)
+        assert e.value.status == P.INVALID_ARG
     with pytest.raises(P.PoolError) as e:
         pool.seq_append_slots([0, 0])
     assert e.value.status == P.INVALID_ARG
@@ -155,3 +156,147 @@ def test_brute_force_slots_against_position_rule():
         st = pool.stats()
         assert st["used_blocks"] + st["free_blocks"] == nb
         assert st["used_blocks"] == sum(len(pool.tables[s]) for s in live)
+
+
+def test_copy_on_write_trace():
+    """Hand-derived: a beam fork shares a partly filled block; the first write
+    into it moves the writer to the free-list front and queues (old, new)."""
+    pool = P.Pool(1, 1, 8, 4, 2, 8)
+    pool.seq_create(0)                                   # block 0
+    assert pool.seq_append_tokens(0, 6) == [0, 1, 2, 3, 4, 5]   # block 1 opened at token 4
+    pool.seq_fork_prefix(1, 0, 6)                        # full fork: [0, 1], len 6
+    assert pool.ref[0] == 2 and pool.ref[1] == 2
+    assert pool.seq_append_slots([1]) == [2 * 4 + 2]     # block 1 shared -> copy into 2
+    assert pool.block_table(1) == [0, 2] and pool.ref[1] == 1 and pool.ref[2] == 1
+    assert pool.seq_append_slots([0]) == [1 * 4 + 2]     # block 1 is 0's alone now
+    assert pool.take_copies() == [(1, 2)] and pool.take_copies() == []
+    assert pool.seq_append_tokens(1, 2) == [11, 12]      # block 2 offset 3, then block 3
+    pool.seq_free(0)
+    assert pool.ref[0] == 1 and pool.ref[1] == 0 and list(pool.free)[-1] == 1
+
+
+def test_copy_on_write_counts_in_all_or_nothing():
+    pool = P.Pool(1, 1, 8, 4, 2, 3)
+    pool.seq_create(0)
+    pool.seq_append_tokens(0, 2)
+    pool.seq_fork_prefix(1, 0, 2)
+    pool.seq_create(2)                                   # last free block
+    with pytest.raises(P.PoolError) as e:                # both would copy: one block short
+        pool.seq_append_slots([0, 1])
+    assert e.value.status == P.NO_FREE_BLOCK and pool.lens[0] == 2 and pool.copies == []
+    with pytest.raises(P.PoolError) as e:
+        pool.seq_append_tokens(1, 3)                     # 1 copy + 1 new block, 1 free
+    assert e.value.status == P.NO_FREE_BLOCK and pool.lens[1] == 2
+    pool.seq_free(2)
+    assert pool.seq_append_tokens(1, 3) and pool.lens[1] == 5 and len(pool.copies) == 1
+
+
+def _check_beams(seed, bs, nb, steps, drain=True):
+    """Random forks, appends and frees with a cache of token values; after every
+    append the copy queue is executed before the writes.  Returns the largest
+    mismatch between each live sequence's gathered cache and its own history."""
+    from oracle import attention as A
+    r = np.random.default_rng(seed)
+    pool = P.Pool(1, 1, 1, bs, 4, nb, initial_free_order=r.permutation(nb).tolist())
+    cache = np.full((1, 2, nb, bs, 1, 1), np.nan)
+    hist, nid, val = {}, 0, 0.0
+    for _ in range(steps):
+        op = r.integers(0, 6)
+        live = sorted(hist)
+        try:
+            if op == 0 or not live:
+                pool.seq_create(nid)
+                hist[nid] = []
+                nid += 1
+            elif op == 1:                                 # fork (beam or prefix)
+                src = int(r.choice(live))
+                if hist[src]:
+                    ntok = int(r.integers(1, len(hist[src]) + 1))
+                    pool.seq_fork_prefix(nid, src, ntok)
+                    hist[nid] = hist[src][:ntok]
+                    nid += 1
+            elif op in (2, 3, 4):
+                sids = r.choice(live, size=int(r.integers(1, len(live) + 1)),
+                                replace=False).tolist()
+                slots = pool.seq_append_slots(sids)
+                if drain:
+                    A.copy_blocks(cache, pool.take_copies())
+                for sid, sl in zip(sids, slots):
+                    val += 1.0
+                    cache[0, :, sl // bs, sl % bs] = val
+                    hist[sid].append(val)
+            else:
+                sid = int(r.choice(live))
+                pool.seq_free(sid)
+                del hist[sid]
+        except P.PoolError as e:
+            assert e.status == P.NO_FREE_BLOCK
+    worst = 0.0
+    for sid, h in hist.items():
+        for kv in (0, 1):
+            got = A.gather_sequence(cache[0, kv], pool.tables[sid], len(h))[:, 0, 0]
+            d = np.abs(got - np.asarray(h)) if h else np.zeros(1)
+            worst = max(worst, float(np.nan_to_num(d, nan=1e9).max()))
+    return worst
+
+
+@pytest.mark.parametrize("seed,bs", [(0, 4), (1, 1), (2, 16), (3, 3)])
+def test_beams_read_back_their_own_history(seed, bs):
+    """Every sequence gathers exactly the tokens it appended, whatever was
+    forked from it or written by its beams later (copy-on-write invariant)."""
+    assert _check_beams(seed, bs, 64, 800) == 0.0
+
+
+def test_skipping_the_copies_is_caught():
+    assert _check_beams(0, 4, 64, 800, drain=False) > 0.0
+
+
+def test_prefix_cache_trace():
+    """Section 4.3: insert with count 1, longest-prefix lookup adds one per hit,
+    release takes one off; at zero the entry and its block references go."""
+    pool = P.Pool(1, 1, 8, 4, 2, 16)
+    toks = [5, 6, 7, 8, 9, 10]
+    pool.seq_create(0)
+    pool.seq_append_tokens(0, 6)                          # blocks 0, 1
+    pool.prefix_insert(toks[:4], 0)                       # block 0
+    pool.prefix_insert(toks, 0)                           # blocks 0, 1
+    assert pool.ref[0] == 3 and pool.ref[1] == 2
+    assert pool.prefix_count(toks[:4]) == 1 and pool.prefix_count(toks) == 1
+    assert pool.prefix_lookup(toks + [11, 12]) == ([0, 1], 6)
+    assert pool.prefix_lookup([5, 6, 7, 8, 0]) == ([0], 4)
+    assert pool.prefix_lookup([5, 6, 7]) is None and pool.prefix_lookup([1]) is None
+    assert pool.prefix_count(toks) == 2 and pool.prefix_count(toks[:4]) == 2
+    assert pool.seq_create_from_prefix(1, toks + [42]) == 6
+    assert pool.block_table(1) == [0, 1] and pool.lens[1] == 6 and pool.ref[1] == 3
+    assert pool.seq_append_slots([1]) == [2 * 4 + 2]      # partly filled block 1: copied
+    assert pool.take_copies() == [(1, 2)]
+    assert pool.seq_create_from_prefix(2, [99]) == 0 and pool.block_table(2) == [3]
+    pool.seq_free(0)
+    for _ in range(3):
+        pool.prefix_release(toks)                         # 3 -> 0: entry dropped
+    assert pool.prefix_count(toks) == 0 and pool.ref[1] == 0 and pool.ref[0] == 2   # [:4] entry + seq 1
+    with pytest.raises(P.PoolError):
+        pool.prefix_release(toks)
+    with pytest.raises(P.PoolError):
+        pool.prefix_insert(toks[:4], 1)                   # already cached
+
+
+def test_prefix_lookup_equals_brute_force_scan():
+    """The longest cached prefix found by the page's descending loop equals a
+    direct scan of every entry."""
+    r = np.random.default_rng(5)
+    pool = P.Pool(1, 1, 8, 4, 2, 256)
+    pool.seq_create(0)
+    pool.seq_append_tokens(0, 40)
+    entries = set()
+    for _ in range(30):
+        n = int(r.integers(1, 12))
+        e = tuple(int(x) for x in r.integers(0, 3, size=n))
+        if e not in entries:
+            pool.prefix_insert(list(e), 0)
+            entries.add(e)
+    for _ in range(300):
+        q = [int(x) for x in r.integers(0, 3, size=int(r.integers(0, 15)))]
+        best = max((len(e) for e in entries if tuple(q[:len(e)]) == e), default=0)
+        hit = pool.prefix_lookup(q)
+        assert (hit[1] if hit else 0) == best

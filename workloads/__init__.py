@@ -225,3 +225,38 @@ def fp8_scale_from_absmax(absmax: np.ndarray) -> np.ndarray:
     """Static per-head FP8 scale absmax / 448 (symmetric rule, qmax = 448)."""
     a = np.asarray(absmax, dtype=np.float32)
     return np.where(a > 0, a / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+
+
+@dataclass(frozen=True)
+class ForkWorkload:
+    """Beam search over a pool ("LLM inference tutorial" section 4.2: blocks
+    shared copy-on-write between beams): ``num_prompts`` prompts of U[ctx_lo,
+    ctx_hi] tokens, each forked into ``beams`` beams, then one decode token per
+    beam; every shared, partly filled last block is copied on write."""
+    name: str
+    num_prompts: int
+    beams: int
+    num_layers: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    seed: int
+    ctx_lo: int
+    ctx_hi: int
+    kv_dtype: str = BF16
+    pool_slack: float = 1.5
+
+
+# 32 layers of the 7B shape, 64 prompts x 4 beams: 192 block copies x 64 planes.
+BEAM_FORK_7B = ForkWorkload("beam_fork_cow_7b_bf16", 64, 4, 32, 32, 128, 16, seed=8,
+                            ctx_lo=64, ctx_hi=512)
+FORK = (BEAM_FORK_7B,)
+
+
+def fork_prompt_lens(w: ForkWorkload) -> np.ndarray:
+    """Prompt lengths, none a multiple of the block size (the fork shares a
+    partly filled block, as a beam fork mid-block does)."""
+    lens = rng(w.seed, 1).integers(w.ctx_lo, w.ctx_hi + 1, size=w.num_prompts)
+    lens = np.where(lens % w.block_size == 0, lens + 1, lens)
+    return lens.astype(np.int64)
+
