@@ -45,7 +45,7 @@ import workloads as W  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
 PREFILL_METRIC = "paged prefill attention: TFLOP/s (% bf16 tensor peak), prefill tokens/s"
-FORK_METRIC = "copy-on-write block copies of a beam fork: GB/s moved (% HBM peak)"
+FORK_METRIC = "copy-on-write block copies of a beam fork: GB/s (distinct sources read + copies written; % HBM peak)"
 WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL + W.FORK}
 DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
@@ -801,8 +801,11 @@ class ForkStep:
         torch.cuda.synchronize(device)
 
     def moved_bytes(self) -> int:
-        """Read + written bytes of one copy_blocks launch."""
-        return 2 * int(self.pairs_h.shape[0]) * self.planes * self.block_bytes
+        """Algorithmic bytes of one copy_blocks launch: every distinct source
+        block read once, every destination written (a prompt's partly filled
+        block is the source of beams - 1 copies)."""
+        srcs = len(set(self.pairs_h[:, 0].tolist()))
+        return (srcs + int(self.pairs_h.shape[0])) * self.planes * self.block_bytes
 
     def run(self):
         import paged_kv_cache_295_gb300 as pkv
@@ -924,7 +927,7 @@ def run_fork_reference(args):
     for _ in range(K):
         OA.copy_blocks(pool, pairs)
     dt = time.perf_counter() - t
-    moved = 2 * len(pairs) * 2 * w.num_layers * pool[0, 0, 0].nbytes * K
+    moved = (1 + len(pairs)) * 2 * w.num_layers * pool[0, 0, 0].nbytes * K   # one source
     value = moved / dt / 1e9
     sample = (f"{len(pairs)} block copies (one prompt's beams) x {2 * w.num_layers} planes per "
               f"step, {K} steps, numpy, 1 thread")

@@ -10,7 +10,9 @@ num_kv_heads, head_dim]``, i.e. one layer's K (or V) slice of the pool tensor
 * ``"f32"``      - numpy float32;
 * ``"bf16"``     - numpy uint16 holding bfloat16 bit patterns;
 * ``"fp8_e4m3"`` - numpy uint8 holding E4M3 codes, with one float32 scale
-                   per KV head (K and V separately).
+                   per KV head (K and V separately);
+* ``"int8"``     - numpy int8 holding symmetric 8-bit codes, with one float32
+                   scale per KV head (K and V separately).
 
 What the decode step computes is a plain definition: paging only decides where
 the bytes of a sequence live, and the page's ``get_kv`` (section 4.2) gathers
@@ -56,6 +58,26 @@ def fp8_dequant(codes: np.ndarray, scale_per_head: np.ndarray) -> np.ndarray:
     return (vals * s).astype(np.float64)
 
 
+def int8_encode(x_f32: np.ndarray, scale_per_head: np.ndarray) -> np.ndarray:
+    """"LLM inference tutorial" section 3.1 ``symmetric_quantize`` with bits =
+    8 and a given scale: ``round(x / scale)`` clamped to [-128, 127].  The
+    quotient is one IEEE float32 division and ``round`` is round-half-to-even
+    (torch.round).  A NaN quotient (the page leaves it open) encodes as 0.
+    ``x_f32 [..., num_kv_heads, head_dim]`` float32."""
+    s = np.asarray(scale_per_head, dtype=np.float32)[:, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.asarray(x_f32, dtype=np.float32) / s
+    q = np.where(np.isnan(q), np.float32(0), q)
+    return np.clip(np.rint(q), -128, 127).astype(np.int8)
+
+
+def int8_dequant(codes: np.ndarray, scale_per_head: np.ndarray) -> np.ndarray:
+    """INT8 cache rows -> float64 as ``f32(code) * f32(scale[head])`` (one
+    float32 multiply, section 3.1 dequantisation), then widened."""
+    s = np.asarray(scale_per_head, dtype=np.float32)[:, None]
+    return (np.asarray(codes, dtype=np.int8).astype(np.float32) * s).astype(np.float64)
+
+
 # -- append: section 4.2 append_token, write half ------------------------------
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, src_dtype: str,
                       cache_dtype: str, k_scale=None, v_scale=None):
@@ -66,7 +88,8 @@ def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, src_dtype: s
     offset ``s % block_size`` (section 4.2 ``append_token``); a negative slot
     skips the token.  Same source and cache type: the bytes are copied.  FP8
     cache: ``code = E4M3_rne_satfinite(f32(x) / f32(scale[head]))`` with the
-    quotient an IEEE float32 division (section 3.1 ``x / scale``).
+    quotient an IEEE float32 division (section 3.1 ``x / scale``).  INT8
+    cache: ``int8_encode``.
     """
     bs = k_cache.shape[1]
     for i, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64).tolist()):
@@ -81,6 +104,8 @@ def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, src_dtype: s
                 x = to_f64(row, src_dtype).astype(np.float32)   # exact widening
                 q = x / np.asarray(scale, dtype=np.float32)[:, None]
                 dst[blk, off] = fp8.encode_f32(q.astype(np.float32))
+            elif cache_dtype == "int8":
+                dst[blk, off] = int8_encode(to_f64(row, src_dtype).astype(np.float32), scale)
             else:
                 raise ValueError(f"unsupported append {src_dtype}->{cache_dtype}")
 
@@ -114,6 +139,8 @@ def gather_sequence(cache, table, seq_len: int):
 def decode_kv(rows, kv_dtype: str, scale=None) -> np.ndarray:
     if kv_dtype == "fp8_e4m3":
         return fp8_dequant(rows, scale)
+    if kv_dtype == "int8":
+        return int8_dequant(rows, scale)
     return to_f64(rows, kv_dtype)
 
 

@@ -54,7 +54,7 @@ NO_FREE_BLOCK = "no_free_block"
 BAD_BLOCK = "bad_block"
 REFCOUNT = "refcount"
 
-DTYPE_BYTES = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}
+DTYPE_BYTES = {"f32": 4, "bf16": 2, "fp8_e4m3": 1, "int8": 1}
 
 
 class PoolError(Exception):

@@ -19,8 +19,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-F32, BF16, FP8 = "f32", "bf16", "fp8_e4m3"
-ELEM_BYTES = {F32: 4, BF16: 2, FP8: 1}
+F32, BF16, FP8, INT8 = "f32", "bf16", "fp8_e4m3", "int8"
+ELEM_BYTES = {F32: 4, BF16: 2, FP8: 1, INT8: 1}
 
 
 @dataclass(frozen=True)
@@ -225,6 +225,13 @@ def fp8_scale_from_absmax(absmax: np.ndarray) -> np.ndarray:
     """Static per-head FP8 scale absmax / 448 (symmetric rule, qmax = 448)."""
     a = np.asarray(absmax, dtype=np.float32)
     return np.where(a > 0, a / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+
+
+def int8_scale_from_absmax(absmax: np.ndarray) -> np.ndarray:
+    """Static per-head INT8 scale absmax / 127 (section 3.1 symmetric rule,
+    qmax = 2^7 - 1)."""
+    a = np.asarray(absmax, dtype=np.float32)
+    return np.where(a > 0, a / np.float32(127.0), np.float32(1.0)).astype(np.float32)
 
 
 @dataclass(frozen=True)
