@@ -208,7 +208,7 @@ def attention_alg_bytes(w, lens) -> int:
 
 def append_alg_bytes(w) -> int:
     """Bytes of one append launch: the new rows read (source type) and written."""
-    src = 2 if w.kv_dtype in ("bf16", "fp8_e4m3") else 4
+    src = 2 if w.kv_dtype in ("bf16", "fp8_e4m3", "int8") else 4
     return w.num_seqs * 2 * w.num_kv_heads * w.head_dim * (src + W.ELEM_BYTES[w.kv_dtype]) + \
         w.num_seqs * 8
 
@@ -222,7 +222,7 @@ def decode_kernel_name(w) -> str:
         return "paged_decode_tc_kernel"
     if forced != "mma" and w.group <= 8 and (
             (w.kv_dtype == "bf16" and w.head_dim in (64, 128))
-            or (w.kv_dtype == "fp8_e4m3" and w.head_dim == 128)):
+            or (w.kv_dtype in ("fp8_e4m3", "int8") and w.head_dim == 128)):
         return "paged_decode_mma2_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
         return "paged_decode_mma_kernel"
@@ -241,7 +241,8 @@ class DeviceStep:
         from paged_kv_cache_295_gb300.engine import PagedKVCache, build_prompts
         self.w, self.device, self.partition = w, device, partition
         S, hq, hkv, d, bs = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
-        code = {"f32": pkv.F32, "bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3}[w.kv_dtype]
+        code = {"f32": pkv.F32, "bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3,
+                "int8": pkv.INT8}[w.kv_dtype]
         self.lens = W.context_lens(w)
         nb = W.num_blocks(w, self.lens)
         self.eng = eng = PagedKVCache(w.num_layers, hkv, d, bs, nb, code, device=device,
@@ -277,12 +278,13 @@ class DeviceStep:
                   for _ in range(nsets)]
             vn = [torch.randn((S, hkv, d), generator=gen, device=device).to(self.src_dt)
                   for _ in range(nsets)]
-            if code == pkv.FP8_E4M3:
-                # static per-head scale absmax / 448 over the layer's data
+            if code in (pkv.FP8_E4M3, pkv.INT8):
+                # static per-head scale absmax / qmax over the layer's data (448 E4M3, 127 INT8)
+                qmax = 448.0 if code == pkv.FP8_E4M3 else 127.0
                 ka = torch.maximum(ks.float().abs().amax((0, 2)), torch.stack(kn).float().abs().amax((0, 1, 3)))
                 va = torch.maximum(vs.float().abs().amax((0, 2)), torch.stack(vn).float().abs().amax((0, 1, 3)))
-                eng.k_scale[layer] = torch.where(ka > 0, ka / 448.0, torch.ones_like(ka))
-                eng.v_scale[layer] = torch.where(va > 0, va / 448.0, torch.ones_like(va))
+                eng.k_scale[layer] = torch.where(ka > 0, ka / qmax, torch.ones_like(ka))
+                eng.v_scale[layer] = torch.where(va > 0, va / qmax, torch.ones_like(va))
             if prompt.size:
                 eng.append(layer, ks, vs, prompt_d)
             if layer in keep_layers:   # kept for oracle checks of this layer
@@ -996,7 +998,8 @@ class OracleStep:
         op.append_slots(range(S))
         mb = max(len(op.p.tables[s]) for s in range(S))
         self.tables = np.asarray(op.p.padded_tables(list(range(S)), mb)[0], dtype=np.int64)
-        dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}[w.kv_dtype]
+        dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8,
+              "int8": np.int8}[w.kv_dtype]
         self.kc = np.zeros((self.nb, bs, hkv, d), dtype=dt)
         self.vc = np.zeros_like(self.kc)
         r = W.rng(w.seed, 900)
@@ -1017,6 +1020,8 @@ class OracleStep:
                         y = np.clip(x / sc[None, None, :, None], -448, 448).astype(np.float32)
                         cache[b] = torch.from_numpy(y[0]).to(torch.float8_e4m3fn).view(
                             torch.uint8).numpy()
+                    elif w.kv_dtype == "int8":     # codes drawn directly
+                        cache[b] = r.integers(-127, 128, size=(bs, hkv, d)).astype(np.int8)
                     else:
                         cache[b] = W.store(x[0], w.kv_dtype)
         self.q = W.store(r.standard_normal((S, w.num_q_heads, d), dtype=np.float32), w.q_dtype)

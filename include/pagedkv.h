@@ -61,7 +61,9 @@ typedef enum {
 #define PKV_DEV_TIMEOUT 0x8       /* an asynchronous copy did not land within 2 s; the CTA
                                      stopped early and its output is not valid */
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+/* Element types.  INT8 is the tutorial's section 3.1 symmetric 8-bit code
+ * (value = code * scale); FP8_E4M3 the OCP E4M3 code (value = e4m3 * scale). */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2, PKV_INT8 = 3 } pkv_dtype;
 
 /* Human-readable name of a status (static string). */
 const char* pkv_status_string(int32_t status);
@@ -219,6 +221,10 @@ pkv_status prefix_cache_count(const pkv_pool* pool, const int32_t* tokens, int32
  *     E4M3(round-to-nearest-even, saturate to +-448)(float(x) / k_scale[h])
  *     with an IEEE float32 division [TUT 3.1 symmetric rule, qmax = 448];
  *     k_scale / v_scale are device [num_kv_heads] float32.
+ *   cache_dtype == INT8 with src f32 or bf16: each element becomes
+ *     clamp(round_half_even(float(x) / k_scale[h]), -128, 127), the quotient
+ *     an IEEE float32 division, a NaN quotient 0 [TUT 3.1 symmetric_quantize,
+ *     bits = 8].
  * Requirements: all buffers 16-byte aligned; head_dim * elem_size a multiple of
  * 16 bytes.  UNSUPPORTED for other dtype pairs. */
 pkv_status reshape_and_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -248,7 +254,7 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
 /* One query token per sequence attends over its whole paged context.
  *   q            : device [num_seqs, num_q_heads, head_dim], q_dtype (f32|bf16).
  *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, head_dim],
- *                  kv_dtype (f32|bf16|fp8_e4m3); one layer's views.
+ *                  kv_dtype (f32|bf16|fp8_e4m3|int8); one layer's views.
  *   block_tables : device [num_seqs, max_blocks_per_seq] int32, row-major;
  *                  entry j of row s is the physical block of logical block j.
  *                  Entries at or beyond ceil(context_lens[s]/block_size) are
@@ -257,8 +263,9 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *                  token appended this step).  0 gives an output of 0.
  *   max_context_len : host upper bound of context_lens (sizes the grid).
  *   scale        : logit scale (1/sqrt(head_dim) in [TUT 4.4]).
- *   k_scale, v_scale : device [num_kv_heads] float32 dequant scales, FP8 only
- *                  (value = float(e4m3) * scale[kv_head]); else ignored.
+ *   k_scale, v_scale : device [num_kv_heads] float32 dequant scales, FP8 and
+ *                  INT8 only (value = float(code) * scale[kv_head]); else
+ *                  ignored.
  *   out          : device [num_seqs, num_q_heads, head_dim] float32.
  *   workspace    : device scratch of workspace_bytes >=
  *                  paged_attention_workspace_bytes(...) (may be NULL when that
@@ -271,8 +278,10 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * over t < context_lens[s], K/V gathered through the block table [TUT 4.2
  * get_kv], with float32 accumulation and a running (online) softmax.
  * Supported: head_dim in {64, 128, 256} with head_dim * kv_elem_size in
- * [64, 512] bytes; G in {1, 2, 4, 8}; block_size a power of two in [1, 4096];
- * 16-byte aligned buffers.  UNSUPPORTED / INVALID_ARG otherwise. */
+ * [64, 512] bytes; G in {1, 2, 4, 8}, and G up to 16 for bf16 and FP8 caches
+ * with head_dim 128 (bf16 also 64) and block_size >= 8; block_size a power of
+ * two in [1, 4096]; 16-byte aligned buffers.  UNSUPPORTED / INVALID_ARG
+ * otherwise. */
 pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_tables, const int32_t* context_lens,
                                   int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

@@ -17,8 +17,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
-F32, BF16, FP8_E4M3 = 0, 1, 2
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E4M3: "fp8_e4m3"}
+F32, BF16, FP8_E4M3, INT8 = 0, 1, 2, 3
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E4M3: "fp8_e4m3", INT8: "int8"}
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 STATUS = {0: "ok", 1: "invalid_arg", 2: "no_free_block", 3: "bad_block", 4: "refcount",
@@ -298,6 +298,8 @@ def _dtype_code(t) -> int:
         return BF16
     if t.dtype in (torch.uint8, torch.float8_e4m3fn):
         return FP8_E4M3
+    if t.dtype == torch.int8:
+        return INT8
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 

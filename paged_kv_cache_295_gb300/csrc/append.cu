@@ -3,7 +3,9 @@
 // append_token: physical block slot / block_size, offset slot % block_size).
 // The FP8 variant stores E4M3(float(x) / scale[head]) ("ToPG framework"
 // section 3.3 compressed FP8 cache; the tutorial's section 3.1 symmetric
-// x / scale rule).
+// x / scale rule); the INT8 variant stores clamp(round(x / scale[head]),
+// -128, 127) with round half to even (the tutorial's section 3.1
+// symmetric_quantize with bits = 8), a NaN quotient as 0.
 //
 // One thread writes one 16-byte segment of one destination row, so a warp
 // covers whole rows with coalesced 16-byte stores.  The work is tiny next to
@@ -68,9 +70,32 @@ __device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, fl
   }
 }
 
-// Quantising kernel: f32 / bf16 source -> E4M3 cache, per-head scale.
-template <typename Src>
-__global__ void append_fp8_kernel(const Src* __restrict__ k_new, const Src* __restrict__ v_new,
+// Four float32 quotients -> four cache bytes (low byte first).
+template <typename Q>
+__device__ __forceinline__ uint32_t quant4(const float* q);
+
+template <>
+__device__ __forceinline__ uint32_t quant4<FP8>(const float* q) {   // E4M3, RNE, saturating
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+template <>
+__device__ __forceinline__ uint32_t quant4<INT8>(const float* q) {   // RNE, clamp, NaN -> 0
+  uint32_t w = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    int v = __float2int_rn(q[b]);   // round half to even; NaN -> 0, +-inf saturate
+    v = v < -128 ? -128 : (v > 127 ? 127 : v);
+    w |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * b);
+  }
+  return w;
+}
+
+// Quantising kernel: f32 / bf16 source -> 8-bit cache (Q = FP8 or INT8), per-head scale.
+template <typename Src, typename Q>
+__global__ void append_quant_kernel(const Src* __restrict__ k_new, const Src* __restrict__ v_new,
                                   const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
                                   uint4* __restrict__ v_cache, const float* __restrict__ k_scale,
                                   const float* __restrict__ v_scale, int32_t num_tokens,
@@ -98,13 +123,11 @@ __global__ void append_fp8_kernel(const Src* __restrict__ k_new, const Src* __re
     const float s = __ldg((is_v ? v_scale : k_scale) + head);
     uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      // IEEE float32 division, then E4M3 round-to-nearest-even with saturation.
-      const float2 a = make_float2(__fdiv_rn(x[4 * k + 0], s), __fdiv_rn(x[4 * k + 1], s));
-      const float2 b = make_float2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s));
-      const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
-      w[k] = (lo & 0xFFFFu) | (hi << 16);
+    for (int k = 0; k < 4; ++k) {   // IEEE float32 division, then the 8-bit code
+      float q[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(x[4 * k + e], s);
+      w[k] = quant4<Q>(q);
     }
     const int64_t dst = (slot * num_kv_heads + head) * segs + seg;
     (is_v ? v_cache : k_cache)[dst] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -143,26 +166,30 @@ extern "C" pkv_status reshape_and_cache(const void* k_new, const void* v_new,
   const int64_t num_slots = num_blocks * block_size;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   constexpr int kThreads = 256;
-  if (src_dtype == cache_dtype && cache_dtype != PKV_FP8_E4M3) {
+  const bool quant = cache_dtype == PKV_FP8_E4M3 || cache_dtype == PKV_INT8;
+  if (src_dtype == cache_dtype && !quant) {
     const int32_t segs = head_dim * es_dst / 16;
     const int64_t work = 2LL * num_tokens * num_kv_heads * segs;
     append_copy_kernel<<<grid_for(work, kThreads), kThreads, 0, st>>>(
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, num_kv_heads, segs,
         num_slots, device_status);
-  } else if (cache_dtype == PKV_FP8_E4M3 && (src_dtype == PKV_F32 || src_dtype == PKV_BF16)) {
+  } else if (quant && (src_dtype == PKV_F32 || src_dtype == PKV_BF16)) {
     if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
     const int64_t work = 2LL * num_tokens * num_kv_heads * (head_dim / 16);
-    if (src_dtype == PKV_F32)
-      append_fp8_kernel<float><<<grid_for(work, kThreads), kThreads, 0, st>>>(
-          static_cast<const float*>(k_new), static_cast<const float*>(v_new), slot_mapping,
+    const int grid = grid_for(work, kThreads);
+    auto launch = [&](auto src_tag, auto q_tag) {
+      using Src = decltype(src_tag);
+      using Q = decltype(q_tag);
+      append_quant_kernel<Src, Q><<<grid, kThreads, 0, st>>>(
+          static_cast<const Src*>(k_new), static_cast<const Src*>(v_new), slot_mapping,
           static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), k_scale, v_scale,
           num_tokens, num_kv_heads, head_dim, num_slots, device_status);
+    };
+    if (cache_dtype == PKV_FP8_E4M3)
+      src_dtype == PKV_F32 ? launch(float{}, FP8{}) : launch(__nv_bfloat16{}, FP8{});
     else
-      append_fp8_kernel<__nv_bfloat16><<<grid_for(work, kThreads), kThreads, 0, st>>>(
-          static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
-          slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), k_scale,
-          v_scale, num_tokens, num_kv_heads, head_dim, num_slots, device_status);
+      src_dtype == PKV_F32 ? launch(float{}, INT8{}) : launch(__nv_bfloat16{}, INT8{});
   } else {
     return PKV_ERR_UNSUPPORTED;
   }

@@ -10,9 +10,9 @@
 
 namespace pkv {
 
-constexpr int kElemBytes[3] = {4, 2, 1};
+constexpr int kElemBytes[4] = {4, 2, 1, 1};
 
-inline int elem_bytes(int32_t dt) { return (dt >= 0 && dt <= 2) ? kElemBytes[dt] : 0; }
+inline int elem_bytes(int32_t dt) { return (dt >= 0 && dt <= 3) ? kElemBytes[dt] : 0; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -51,6 +51,11 @@ struct FP8 {
   static constexpr int kPerVec = 16;
 };
 
+struct INT8 {
+  static constexpr int kBytes = 1;
+  static constexpr int kPerVec = 16;
+};
+
 template <typename T>
 __device__ __forceinline__ void decode16(const uint4& v, float* x);
 
@@ -79,6 +84,17 @@ __device__ __forceinline__ void decode16<FP8>(const uint4& v, float* x) {
     float2 b = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
     x[4 * i + 0] = a.x; x[4 * i + 1] = a.y;
     x[4 * i + 2] = b.x; x[4 * i + 3] = b.y;
+  }
+}
+
+template <>
+__device__ __forceinline__ void decode16<INT8>(const uint4& v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      x[4 * i + b] = static_cast<float>(static_cast<int8_t>((w[i] >> (8 * b)) & 0xFFu));
   }
 }
 

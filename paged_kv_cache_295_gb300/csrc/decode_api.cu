@@ -96,6 +96,11 @@ LaunchFn pick(int32_t kv_dtype, int D, int G) {
       if (D == 128) return pick_group<BF16, 128>(G);
       if (D == 256) return pick_group<BF16, 256>(G);
       return nullptr;
+    case PKV_INT8:
+      if (D == 64) return pick_group<INT8, 64>(G);
+      if (D == 128) return pick_group<INT8, 128>(G);
+      if (D == 256) return pick_group<INT8, 256>(G);
+      return nullptr;
     case PKV_FP8_E4M3:
       if (D == 64) return pick_group<FP8, 64>(G);
       if (D == 128) return pick_group<FP8, 128>(G);
@@ -164,7 +169,8 @@ extern "C" pkv_status paged_attention_decode(
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_INVALID_ARG;
-  if (kv_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+  if ((kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) && (!k_scale || !v_scale))
+    return PKV_ERR_INVALID_ARG;
 
   const int32_t P = resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
   const int32_t parts = parts_for(max_context_len, P);
@@ -203,7 +209,7 @@ extern "C" pkv_status paged_attention_decode(
   if (use_tc) return launch_decode_tc(a, k_cache, v_cache, num_blocks, q_dtype == PKV_F32);
   if (use_mma2)
     return launch_decode_mma2(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
-                              kv_dtype == PKV_FP8_E4M3);
+                              kv_dtype);
   if (use_mma)
     return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
                              kv_dtype == PKV_FP8_E4M3);

@@ -396,7 +396,7 @@ pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const v
 bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                          int64_t num_blocks);
 pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                              int head_dim, int64_t num_blocks, bool q_f32, bool fp8);
+                              int head_dim, int64_t num_blocks, bool q_f32, int32_t kv_dtype);
 // 5th-generation tensor-core (tcgen05 + TMEM) path; see decode_tc.cuh.
 bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                        int64_t num_blocks);

@@ -1,5 +1,5 @@
 // PagedAttention decode, tensor-core path with the contractions transposed
-// (mma.sync m16n8k16; 16-bit and FP8 caches; query groups of up to 8 heads).
+// (mma.sync m16n8k16; 16-bit, FP8 and INT8 caches; query groups of up to 8 heads).
 //
 // Same work split and staging as decode_mma.cuh (one CTA per sequence x KV
 // head x split-KV partition; each warp streams every NW-th 16-token chunk
@@ -20,15 +20,27 @@
 // per-warp shared memory.
 //
 // 16-bit caches: fragments come from the swizzled tiles with ldmatrix
-// (ldmatrix.trans for V^T); P is split into bf16 hi + lo parts.  FP8 caches:
-// E4M3 bytes are converted in registers to fp16 (exact) using a dimension
+// (ldmatrix.trans for V^T); P is split into bf16 hi + lo parts.  8-bit caches
+// (FP8 E4M3 or INT8): the codes are converted in registers to fp16 (exact for
+// both) using a dimension
 // permutation shared by q and K (QK) and an output-dimension permutation (PV)
 // so each lane loads contiguous 16-byte slices; P is fp16.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma_fp8.cuh"
 
 namespace pkv {
+
+// Four 8-bit cache codes -> two f16x2 (bytes 0, 1 -> lo; 2, 3 -> hi), exactly.
+template <typename KV>
+__device__ __forceinline__ void byte4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (std::is_same<KV, INT8>::value)
+    s8x4_to_f16x2x2(w, lo, hi);
+  else
+    e4m3x4_to_f16x2x2(w, lo, hi);
+}
 
 template <typename KV, int D, int NW, int STAGES>
 struct Mma2Smem {
@@ -49,7 +61,7 @@ __global__ void __launch_bounds__(NW * 32)
                              const __grid_constant__ CUtensorMap tmap_v, const MmaParams mp) {
   using SM = Mma2Smem<KV, D, NW, STAGES>;
   constexpr bool F8 = KV::kBytes == 1;
-  static_assert(!F8 || D == 128, "FP8 path is built for head_dim 128");
+  static_assert(!F8 || D == 128, "the 8-bit path is built for head_dim 128");
   constexpr int H = SM::kBoxes;
   constexpr int KSTEPS = D / 16;   // QK k-steps
   constexpr int MT = D / 16;       // PV m-tiles (16 output dims each)
@@ -245,8 +257,8 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         uint32_t a[4];   // {row gid k, row gid+8 k, row gid k+8, row gid+8 k+8}
-        e4m3x4_to_f16x2x2(wa[ks], a[0], a[2]);
-        e4m3x4_to_f16x2x2(wb[ks], a[1], a[3]);
+        byte4_to_f16x2x2<KV>(wa[ks], a[0], a[2]);
+        byte4_to_f16x2x2<KV>(wb[ks], a[1], a[3]);
         mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
         if (QF32) mma_f16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
       }
@@ -338,10 +350,10 @@ __global__ void __launch_bounds__(NW * 32)
         const uint32_t lo89 = __byte_perm(Cw[w], Dw[w], 0x5140);
         const uint32_t hi89 = __byte_perm(Cw[w], Dw[w], 0x7362);
         uint32_t aA[4], aB[4];   // m-tiles 2w and 2w+1
-        e4m3x4_to_f16x2x2(lo01, aA[0], aA[1]);
-        e4m3x4_to_f16x2x2(lo89, aA[2], aA[3]);
-        e4m3x4_to_f16x2x2(hi01, aB[0], aB[1]);
-        e4m3x4_to_f16x2x2(hi89, aB[2], aB[3]);
+        byte4_to_f16x2x2<KV>(lo01, aA[0], aA[1]);
+        byte4_to_f16x2x2<KV>(lo89, aA[2], aA[3]);
+        byte4_to_f16x2x2<KV>(hi01, aB[0], aB[1]);
+        byte4_to_f16x2x2<KV>(hi89, aB[2], aB[3]);
         mma_f16(o[2 * w], aA, pb0, pb1);
         mma_f16(o[2 * w + 1], aB, pb0, pb1);
       }

@@ -51,6 +51,19 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
       : "r"(w));
 }
 
+// Four signed 8-bit codes -> two f16x2, bytes 0, 1 in lo and 2, 3 in hi (low
+// byte in the low half), exactly: with u = code + 128 in [0, 255], the binary16
+// whose bits are 0x6400 | u is 1024 + u (exponent 10, mantissa u), so
+// subtracting 1152 = 1024 + 128 (bits 0x6480) leaves the code.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 // Two E4M3 codes (low byte first) -> f16x2 with the low byte in the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu),

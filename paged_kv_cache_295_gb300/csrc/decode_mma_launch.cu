@@ -125,7 +125,7 @@ bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_si
                          int64_t num_blocks) {
   if (kv_dtype == PKV_BF16) {
     if (head_dim != 64 && head_dim != 128) return false;
-  } else if (kv_dtype == PKV_FP8_E4M3) {
+  } else if (kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) {
     if (head_dim != 128) return false;
   } else {
     return false;
@@ -137,19 +137,23 @@ bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_si
 }
 
 pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                              int head_dim, int64_t num_blocks, bool q_f32, bool fp8) {
+                              int head_dim, int64_t num_blocks, bool q_f32, int32_t kv_dtype) {
   const DecodeParams& p = a.p;
   const int bs = 1 << p.bs_log2;
   MmaParams mp{p, bs < kMmaChunk ? bs : kMmaChunk};
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * bs;
-  if (!make_map(&tk, k_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8) ||
-      !make_map(&tv, v_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, fp8))
+  const bool byte_codes = kv_dtype != PKV_BF16;
+  if (!make_map(&tk, k_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, byte_codes) ||
+      !make_map(&tv, v_cache, head_dim, p.num_kv_heads, rows, mp.box_rows, byte_codes))
     return PKV_ERR_CUDA;
   pkv_status st;
-  if (fp8)
+  if (kv_dtype == PKV_FP8_E4M3)
     st = q_f32 ? launch_mma2<FP8, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
                : launch_mma2<FP8, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
+  else if (kv_dtype == PKV_INT8)
+    st = q_f32 ? launch_mma2<INT8, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
+               : launch_mma2<INT8, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
   else if (head_dim == 128)
     st = q_f32 ? launch_mma2<BF16, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
                : launch_mma2<BF16, 128, false>(tk, tv, mp, a.num_seqs, a.stream);

@@ -42,6 +42,7 @@ int dtype_size(int32_t dt) {
     case PKV_F32: return 4;
     case PKV_BF16: return 2;
     case PKV_FP8_E4M3: return 1;
+    case PKV_INT8: return 1;
     default: return 0;
   }
 }

@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, FP8_E4M3, Pool, copy_blocks, paged_attention_decode,
+from . import (BF16, F32, FP8_E4M3, INT8, Pool, copy_blocks, paged_attention_decode,
                paged_attention_prefill, reshape_and_cache, workspace_bytes)
 
 
@@ -25,7 +25,8 @@ def _torch():
 
 def torch_kv_dtype(code):
     torch = _torch()
-    return {F32: torch.float32, BF16: torch.bfloat16, FP8_E4M3: torch.uint8}[code]
+    return {F32: torch.float32, BF16: torch.bfloat16, FP8_E4M3: torch.uint8,
+            INT8: torch.int8}[code]
 
 
 class PagedKVCache:
@@ -44,13 +45,15 @@ class PagedKVCache:
         if poison:   # unused slots hold NaN so a stray read shows in the output
             if kv_dtype == FP8_E4M3:
                 self.storage.fill_(0x7F)
+            elif kv_dtype == INT8:       # no NaN code: the largest one distorts a stray read
+                self.storage.fill_(127)
             else:
                 self.storage.fill_(float("nan"))
         # logit scale 1/sqrt(head_dim) as float32 ("LLM inference tutorial" 4.4)
         self.scale = float(np.float32(1.0 / np.sqrt(head_dim)))
         self.k_scale = None
         self.v_scale = None
-        if kv_dtype == FP8_E4M3:
+        if kv_dtype in (FP8_E4M3, INT8):
             self.k_scale = torch.ones((num_layers, num_kv_heads), dtype=torch.float32,
                                       device=device)
             self.v_scale = torch.ones_like(self.k_scale)

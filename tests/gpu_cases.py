@@ -11,9 +11,9 @@ from oracle import attention as OA
 from oracle import fp8 as OF8
 from oracle import pool as OP
 
-CODE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
+CODE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2, "int8": 3}
 POISON = {"f32": (np.float32, np.float32(np.nan)), "bf16": (np.uint16, 0x7FC0),
-          "fp8_e4m3": (np.uint8, 0x7F)}
+          "fp8_e4m3": (np.uint8, 0x7F), "int8": (np.int8, 127)}
 
 
 class OraclePool:
@@ -36,12 +36,13 @@ class OraclePool:
 
 
 def src_dtype(w):
-    return "bf16" if w.kv_dtype == "fp8_e4m3" else w.kv_dtype
+    return "bf16" if w.kv_dtype in ("fp8_e4m3", "int8") else w.kv_dtype
 
 
 def torch_dtype(code_name):
     import torch
-    return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[code_name]
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+            "int8": torch.int8}[code_name]
 
 
 def to_torch(a, name, device="cuda"):
@@ -127,11 +128,12 @@ def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None) -> tuple:
         kn.append(W.store(kn32, sd))
         vn.append(W.store(vn32, sd))
         qq.append(W.store(q32, w.q_dtype))
-        if w.kv_dtype == "fp8_e4m3":
+        if w.kv_dtype in ("fp8_e4m3", "int8"):
             ka = np.abs(np.concatenate([OA.to_f64(pk[-1], sd), OA.to_f64(kn[-1], sd)])).max((0, 2))
             va = np.abs(np.concatenate([OA.to_f64(pv[-1], sd), OA.to_f64(vn[-1], sd)])).max((0, 2))
-            ks_l.append(W.fp8_scale_from_absmax(ka))
-            vs_l.append(W.fp8_scale_from_absmax(va))
+            rule = W.fp8_scale_from_absmax if w.kv_dtype == "fp8_e4m3" else W.int8_scale_from_absmax
+            ks_l.append(rule(ka))
+            vs_l.append(rule(va))
         else:
             ks_l.append(None)
             vs_l.append(None)

@@ -1,7 +1,8 @@
 """GPU parity: the C-ABI library against the oracle on seeded small decode steps.
 
 Slots, tables and cache bytes must be bit-exact; attention outputs within the
-stated max-abs tolerances (2e-3 for bf16/f32 KV, 1e-2 for FP8 KV).
+stated max-abs tolerances (2e-3 for bf16/f32 KV, 1e-2 for FP8 and INT8 KV: the
+8-bit paths carry q * k_scale and P as fp16, like the FP8 bound).
 """
 import dataclasses
 
@@ -13,7 +14,7 @@ from tests import gpu_cases as GC
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2}
+TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2, "int8": 1e-2}
 
 
 @pytest.fixture(scope="module")
@@ -73,6 +74,12 @@ SMALL = {
                                                seed=17, ctx_law="fixed"), [2, 31, 900]),
     "d128_fp8_g16_bs8": (W.DecodeWorkload("fp8g16", 2, 32, 2, 128, 8, "fp8_e4m3", "bf16",
                                           seed=18, ctx_law="fixed"), [9, 1300]),
+    "d128_int8_mha_bs16": (W.DecodeWorkload("i8g1", 4, 4, 4, 128, 16, "int8", "bf16", seed=19,
+                                            ctx_law="fixed"), [1, 17, 300, 1000]),
+    "d128_int8_g8_bs32_qf32": (W.DecodeWorkload("i8g8", 3, 16, 2, 128, 32, "int8", "f32",
+                                                seed=20, ctx_law="fixed"), [2, 31, 900]),
+    "d64_int8_g4_bs8": (W.DecodeWorkload("i8d64", 3, 8, 2, 64, 8, "int8", "bf16", seed=21,
+                                         ctx_law="fixed"), [3, 64, 513]),
 }
 
 
@@ -241,3 +248,36 @@ def test_fp8_append_rounding_bit_exact(torch_cuda, scale):
     OA.reshape_and_cache(k, v, slots, okc, ovc, "f32", "fp8_e4m3", sc, sc)
     assert np.array_equal(kc.cpu().numpy(), okc)
     assert np.array_equal(vc.cpu().numpy(), ovc)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37])
+def test_int8_append_rounding_bit_exact(torch_cuda, scale):
+    """Every half-integer quotient in and beyond [-128, 127] (and its float32
+    neighbours), infinities and NaN through the INT8 quantising append."""
+    torch = torch_cuda
+    import paged_kv_cache_295_gb300 as pkv
+    from oracle import attention as OA
+    base = np.arange(-140, 141, dtype=np.float32) + np.float32(0.5)
+    x = np.concatenate([base, np.nextafter(base, np.float32(-1e9)),
+                        np.nextafter(base, np.float32(1e9)),
+                        np.array([0, 127, -128, 1e30, -1e30, np.inf, -np.inf, np.nan],
+                                 dtype=np.float32)]) * np.float32(scale)
+    hkv, d = 2, 16
+    n = -(-x.size // (hkv * d))
+    pad = np.zeros(n * hkv * d, np.float32)
+    pad[: x.size] = x
+    k = pad.reshape(n, hkv, d)
+    v = -k
+    slots = np.random.default_rng(1).permutation(n).astype(np.int64)
+    sc = np.array([scale, scale], np.float32)
+    kc = torch.zeros((n, 1, hkv, d), dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    pkv.reshape_and_cache(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                          torch.from_numpy(slots).cuda(), kc, vc, torch.from_numpy(sc).cuda(),
+                          torch.from_numpy(sc).cuda())
+    okc = np.zeros((n, 1, hkv, d), np.int8)
+    ovc = okc.copy()
+    OA.reshape_and_cache(k, v, slots, okc, ovc, "f32", "int8", sc, sc)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
+

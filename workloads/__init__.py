@@ -76,7 +76,10 @@ RAGGED_FP8_LAYER = DecodeWorkload("ragged_fp8_1layer", 256, 32, 32, 128, 16, FP8
                                   seed=4, num_layers=1, ctx_law="lognormal", ctx_lo=1,
                                   ctx_hi=16384, pool_slack=1.25, prefix_tokens=2048,
                                   prefix_seqs=128)
-EXTRA = (RAGGED_FP8_LAYER,)
+# The 7B layer with an INT8 cache (section 3.1 symmetric codes, per-head scale).
+LLAMA7B_LAYER_INT8 = DecodeWorkload("llama7b_layer_int8", 32, 32, 32, 128, 16, INT8, BF16,
+                                    seed=1, ctx_lo=512, ctx_hi=4096)
+EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8)
 
 
 @dataclass(frozen=True)
