@@ -409,6 +409,9 @@ def run_ours(args):
                if NCU_TRAFFIC.get("sources_sha") == sha and NCU_TRAFFIC.get("workload") == w.name
                else None)
 
+    graph = None
+    if w.graph:   # the same step replayed as one CUDA graph (buckets 1..S, padding)
+        graph, dt, value, dt_local = run_graph(st, K, Wm, world, dev, dt, kv_log)
     e2e = run_e2e(st, args, dev, world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -438,6 +441,7 @@ def run_ours(args):
                      "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4) if bw else None,
                      "frac_of_in_run_read": round(achieved / bw["read_gbs"], 4) if bw else None},
         "in_run_bandwidth_gbs": {k: round(v, 1) for k, v in bw.items()} if bw else None,
+        "graph": graph,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * st.launches_per_step(),
@@ -446,6 +450,49 @@ def run_ours(args):
         "kernel_sources_sha": sha,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_graph(st, K, Wm, world, dev, dt_eager, kv_log):
+    """Times the step as a replayed CUDA graph (decode_graph_*): returns the
+    graph report and the (dt, value, dt_local) that replace the eager ones."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    w = st.w
+    S = w.num_seqs
+    buckets = sorted({1 << i for i in range(S.bit_length()) if (1 << i) < S} | {S})
+    g = pkv.DecodeGraph(st.eng, w.num_q_heads, st.tables.shape[1], buckets,
+                        device_status=st.status)
+    L = w.num_layers
+    for l in range(L):
+        g.q[l, :S] = st.q[l][0]
+        g.k_new[l, :S] = st.kn[l][0]
+        g.v_new[l, :S] = st.vn[l][0]
+    g.slots[:S] = st.slots
+    g.tables[:S] = st.tables
+    g.lens[:S] = st.ctx
+    for _ in range(Wm):
+        g.launch(S)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(K):
+        g.launch(S)
+    t1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    dt_local = t0.elapsed_time(t1) * 1e-3
+    dt = max_over_ranks(dt_local, world, dev)
+    value = sum_over_ranks(kv_log * K, world, dev) / dt / 1e9
+    rep = {"buckets": buckets, "bucket_used": S, "ms_per_step": round(dt / K * 1e3, 5),
+           "eager_ms_per_step": round(dt_eager / K * 1e3, 5),
+           "speedup_vs_eager": round(dt_eager / dt, 3),
+           "partition_tokens": pkv.partition_tokens(S, w.num_kv_heads,
+                                                    st.tables.shape[1] * w.block_size),
+           "note": "value, ms_per_step and decode_tokens_per_s are the graph replay's"}
+    g.close()
+    return rep, dt, value, dt_local
 
 
 def run_e2e(st, args, dev, world):

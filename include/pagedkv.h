@@ -4,14 +4,17 @@
  *
  * Sources of the operations (web pages on LLM inference):
  *   [TUT]  "LLM inference tutorial" (xurj.top Tutorial/Detail/167)
- *          section 4.1 KVCache, 4.2 PagedAttention (class PagedKVCache),
- *          4.3 Prefix Caching (class PrefixCacheManager), 4.4 MHA/GQA/MQA,
- *          3.1 symmetric quantisation.
+ *          section 1.2 prefill and decode phases, 3.1 symmetric
+ *          quantisation, 4.1 KVCache, 4.2 PagedAttention (class
+ *          PagedKVCache, copy-on-write for beam search), 4.3 Prefix Caching
+ *          (class PrefixCacheManager), 4.4 MHA/GQA/MQA, 6.2 chunked prefill.
  *   [NANO] "nano-vLLM architecture" (intelliparadigm 2014318), section 4.2
  *          PagedAttention (logical -> physical block mapping, attention that
- *          reads through the mapping) and 4.3 memory-pool formula.
+ *          reads through the mapping), 4.3 memory-pool formula, 5 CUDA graph
+ *          capture and replay with batch-size buckets and padding.
  *   [TGI]  "TGI architecture" (intelliparadigm 2004249), section 3.2 paged
- *          blocks of 128-256 tokens shared between requests.
+ *          blocks of 128-256 tokens shared between requests; 5.1 CUDA graphs
+ *          recorded for common batch sizes at warm-up.
  *   [TOPG] "ToPG framework" (intelliparadigm 2232463), section 3.3: the KV
  *          cache stored compressed as FP8.
  *
@@ -27,6 +30,8 @@
  *     pointers; host buffers are owned by the caller and passed as host
  *     pointers.
  *   - A pool handle is not thread-safe: the caller serialises calls on it.
+ *   - decode_graph_create is the one device-side call that allocates (graph
+ *     objects and a private stream) and synchronises; it is a set-up call.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -347,6 +352,72 @@ pkv_status paged_attention_prefill(const void* q, const int32_t* query_start,
                                    float scale, int32_t causal, int32_t q_dtype,
                                    int32_t kv_dtype, float* out, int32_t* device_status,
                                    pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* CUDA-graph decode step with batch-size buckets and padding.               */
+/* ------------------------------------------------------------------------ */
+/* A whole decode step - for every layer, reshape_and_cache of the new token
+ * then paged_attention_decode - is captured once per batch-size bucket into a
+ * CUDA graph over fixed device buffers, and replayed; a batch of B sequences
+ * runs the smallest bucket >= B, its rows B .. bucket-1 padded as context 0
+ * (output 0) and slot -1 (no append) [NANO 5.1 record and replay, 5.2
+ * buckets: pick the nearest larger bucket, pad to it; TGI 5.1 graphs
+ * recorded for common batch sizes].  The buffer layout below is this
+ * library's own.
+ * Buffers (device, caller-owned, sized for the largest bucket Bmax):
+ *   q            : [num_layers][Bmax][num_q_heads][head_dim], q_dtype.
+ *   k_new, v_new : [num_layers][Bmax][num_kv_heads][head_dim], src_dtype.
+ *   slot_mapping : [Bmax] int64; block_tables [Bmax][max_blocks_per_seq]
+ *                  int32; context_lens [Bmax] int32 (shared by all layers).
+ *   out          : [num_layers][Bmax][num_q_heads][head_dim] float32.
+ *   workspace    : >= paged_attention_workspace_bytes(Bmax, num_q_heads,
+ *                  num_kv_heads, head_dim, max_blocks_per_seq * block_size, 0).
+ *   k_caches, v_caches : HOST arrays of num_layers device pointers, each a
+ *                  [num_blocks, block_size, num_kv_heads, head_dim] view.
+ *   k_scales, v_scales : HOST arrays of num_layers device [num_kv_heads]
+ *                  float32 pointers (8-bit caches; else NULL).
+ * The graphs keep every pointer; the caller writes a step's inputs into the
+ * buffers before decode_graph_launch and reads out after it.  Partitions are
+ * sized for a context of max_blocks_per_seq * block_size. */
+typedef struct {
+  int32_t num_layers, num_q_heads, num_kv_heads, head_dim, block_size;
+  int64_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t q_dtype, kv_dtype, src_dtype;
+  float scale;
+  void* const* k_caches;
+  void* const* v_caches;
+  const float* const* k_scales;
+  const float* const* v_scales;
+  void* q;
+  void* k_new;
+  void* v_new;
+  int64_t* slot_mapping;
+  int32_t* block_tables;
+  int32_t* context_lens;
+  float* out;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* device_status;
+  const int32_t* buckets;   /* host, ascending batch sizes; the last is Bmax */
+  int32_t num_buckets;
+} pkv_decode_graph_config;
+
+typedef struct pkv_decode_graph pkv_decode_graph;
+
+/* Captures one graph per bucket on a private stream of the current device.
+ * Before capturing, it runs each bucket's step once with every row padded
+ * (nothing is appended, so no cache changes) to load the kernels; this
+ * overwrites slot_mapping and context_lens.  Returns INVALID_ARG /
+ * UNSUPPORTED for arguments paged_attention_decode would refuse, CUDA if a
+ * capture fails. */
+pkv_status decode_graph_create(const pkv_decode_graph_config* cfg, pkv_decode_graph** out);
+/* Replays the step for a batch of 1 .. Bmax sequences on stream: pads rows
+ * batch .. bucket-1 (context 0, slot -1), then launches the bucket's graph.
+ * *bucket_out (nullable) receives the bucket used. */
+pkv_status decode_graph_launch(pkv_decode_graph* g, int32_t batch, int32_t* bucket_out,
+                               pkv_stream_t stream);
+void decode_graph_destroy(pkv_decode_graph* g);
 
 /* Size of the device scratch compiled into the library for
  * paged_attention_decode_noalloc (held on every GPU that loads the library,

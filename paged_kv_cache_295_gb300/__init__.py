@@ -47,6 +47,21 @@ class _PoolStats(C.Structure):
                 ("used_bytes", C.c_int64)]
 
 
+class _GraphConfig(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("num_q_heads", C.c_int32),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("block_size", C.c_int32), ("num_blocks", C.c_int64),
+                ("max_blocks_per_seq", C.c_int32), ("q_dtype", C.c_int32),
+                ("kv_dtype", C.c_int32), ("src_dtype", C.c_int32), ("scale", C.c_float),
+                ("k_caches", C.POINTER(C.c_void_p)), ("v_caches", C.POINTER(C.c_void_p)),
+                ("k_scales", C.POINTER(C.c_void_p)), ("v_scales", C.POINTER(C.c_void_p)),
+                ("q", C.c_void_p), ("k_new", C.c_void_p), ("v_new", C.c_void_p),
+                ("slot_mapping", C.c_void_p), ("block_tables", C.c_void_p),
+                ("context_lens", C.c_void_p), ("out", C.c_void_p), ("workspace", C.c_void_p),
+                ("workspace_bytes", C.c_size_t), ("device_status", C.c_void_p),
+                ("buckets", C.POINTER(C.c_int32)), ("num_buckets", C.c_int32)]
+
+
 _lib = None
 P, I32, I64, SZ, FL = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
 _SIGS = {
@@ -75,6 +90,9 @@ _SIGS = {
     "prefix_cache_release": (I32, [P, P, I32]),
     "prefix_cache_count": (I32, [P, P, I32, C.POINTER(I32)]),
     "copy_blocks": (I32, [P, I32, I64, I64, I64, P, I32, P, P]),
+    "decode_graph_create": (I32, [C.POINTER(_GraphConfig), C.POINTER(P)]),
+    "decode_graph_launch": (I32, [P, I32, C.POINTER(I32), P]),
+    "decode_graph_destroy": (None, [P]),
     "reshape_and_cache": (I32, [P, P, P, P, P, I32, I32, I32, I32, I64, I32, I32, P, P, P, P]),
     "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32]),
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
@@ -423,6 +441,82 @@ def copy_blocks(pool_tensor, pairs, device_status=None, stream=None):
                                _dev(pairs, "pairs") if k else None, k,
                                _dev(device_status, "device_status"), _stream(stream))
     _check(st, "copy_blocks")
+
+
+class DecodeGraph:
+    """A decode step (every layer: append + attention) captured as one CUDA
+    graph per batch-size bucket over fixed device buffers, replayed with the
+    batch padded to the nearest larger bucket.
+
+    ``engine`` is a ``PagedKVCache``; the buffers are allocated here for the
+    largest bucket: ``q [L, Bmax, Hq, D]``, ``k_new``/``v_new [L, Bmax, Hkv,
+    D]``, ``slots [Bmax]``, ``tables [Bmax, max_blocks]``, ``lens [Bmax]``,
+    ``out [L, Bmax, Hq, D]``.  Fill the first ``batch`` rows, call
+    ``launch(batch)``, read ``out[:, :batch]``.
+    """
+
+    def __init__(self, engine, num_q_heads, max_blocks, buckets, q_dtype=None, src_dtype=None,
+                 device_status=None):
+        torch = _torch()
+        e = engine
+        dev = e.storage.device
+        self.buckets = sorted(int(b) for b in buckets)
+        B, L = self.buckets[-1], e.num_layers
+        hq, hkv, d = num_q_heads, e.num_kv_heads, e.head_dim
+        q_dtype = torch.bfloat16 if q_dtype is None else q_dtype
+        if src_dtype is None:
+            src_dtype = torch.float32 if e.kv_dtype == F32 else torch.bfloat16
+        self.q = torch.zeros((L, B, hq, d), dtype=q_dtype, device=dev)
+        self.k_new = torch.zeros((L, B, hkv, d), dtype=src_dtype, device=dev)
+        self.v_new = torch.zeros_like(self.k_new)
+        self.slots = torch.full((B,), -1, dtype=torch.int64, device=dev)
+        self.tables = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
+        self.lens = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.out = torch.zeros((L, B, hq, d), dtype=torch.float32, device=dev)
+        max_ctx = max_blocks * e.block_size
+        need = workspace_bytes(B, hq, hkv, d, max_ctx, 0)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.status = device_status
+        kp = (C.c_void_p * L)(*[e.k_cache(l).data_ptr() for l in range(L)])
+        vp = (C.c_void_p * L)(*[e.v_cache(l).data_ptr() for l in range(L)])
+        ksp = vsp = None
+        if e.k_scale is not None:
+            ksp = (C.c_void_p * L)(*[e.k_scale[l].data_ptr() for l in range(L)])
+            vsp = (C.c_void_p * L)(*[e.v_scale[l].data_ptr() for l in range(L)])
+        bk = (C.c_int32 * len(self.buckets))(*self.buckets)
+        self._keep = (kp, vp, ksp, vsp, bk, e)
+        cfg = _GraphConfig(
+            L, hq, hkv, d, e.block_size, e.num_blocks, max_blocks,
+            _dtype_code(self.q), e.kv_dtype, _dtype_code(self.k_new), float(e.scale),
+            C.cast(kp, C.POINTER(C.c_void_p)), C.cast(vp, C.POINTER(C.c_void_p)),
+            C.cast(ksp, C.POINTER(C.c_void_p)) if ksp else None,
+            C.cast(vsp, C.POINTER(C.c_void_p)) if vsp else None,
+            self.q.data_ptr(), self.k_new.data_ptr(), self.v_new.data_ptr(),
+            self.slots.data_ptr(), self.tables.data_ptr(), self.lens.data_ptr(),
+            self.out.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+            device_status.data_ptr() if device_status is not None else None,
+            C.cast(bk, C.POINTER(C.c_int32)), len(self.buckets))
+        h = C.c_void_p()
+        _check(library().decode_graph_create(C.byref(cfg), C.byref(h)), "decode_graph_create")
+        self._h = h
+
+    def launch(self, batch, stream=None) -> int:
+        """Replay the step for ``batch`` rows; returns the bucket used."""
+        b = C.c_int32()
+        _check(library().decode_graph_launch(self._h, int(batch), C.byref(b), _stream(stream)),
+               "decode_graph_launch")
+        return b.value
+
+    def close(self):
+        if getattr(self, "_h", None):
+            library().decode_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def copy_kernel(src, dst, stream=None):

@@ -1,0 +1,194 @@
+// CUDA-graph decode step ("nano-vLLM architecture" section 5: record once,
+// replay; batch-size buckets with padding to the nearest larger bucket;
+// "TGI architecture" section 5.1: graphs recorded for common batch sizes).
+//
+// One graph per bucket holds, for every layer, the append of the step's new
+// K/V rows and the decode attention (with its split-KV reduce), captured from
+// the library's own entry points on a private stream.  A launch pads the rows
+// between the batch and the bucket (context 0, slot -1) with one small kernel
+// and replays the bucket's graph on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+struct pkv_decode_graph {
+  pkv_decode_graph_config cfg{};
+  std::vector<void*> k_caches, v_caches;
+  std::vector<const float*> k_scales, v_scales;
+  std::vector<int32_t> buckets;
+  std::vector<cudaGraphExec_t> execs;
+  int device = 0;
+};
+
+namespace pkv {
+namespace {
+
+__global__ void pad_rows_kernel(int32_t* context_lens, int64_t* slot_mapping, int32_t from,
+                                int32_t to) {
+  const int32_t i = from + blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < to) {
+    context_lens[i] = 0;
+    slot_mapping[i] = -1;
+  }
+}
+
+pkv_status pad_rows(const pkv_decode_graph_config& c, int32_t from, int32_t to, cudaStream_t st) {
+  if (to <= from) return PKV_OK;
+  const int32_t n = to - from;
+  pad_rows_kernel<<<(n + 255) / 256, 256, 0, st>>>(c.context_lens, c.slot_mapping, from, to);
+  return cuda_status(cudaGetLastError());
+}
+
+// The step for a batch of B rows: every layer's append, then its decode.
+pkv_status record_step(const pkv_decode_graph& g, int32_t B, cudaStream_t st) {
+  const pkv_decode_graph_config& c = g.cfg;
+  const int32_t Bmax = g.buckets.back();
+  const int64_t q_layer = static_cast<int64_t>(Bmax) * c.num_q_heads * c.head_dim;
+  const int64_t kv_layer = static_cast<int64_t>(Bmax) * c.num_kv_heads * c.head_dim;
+  const int qb = elem_bytes(c.q_dtype), sb = elem_bytes(c.src_dtype);
+  const int32_t max_ctx = c.max_blocks_per_seq * c.block_size;
+  for (int32_t l = 0; l < c.num_layers; ++l) {
+    const float* ks = g.k_scales.empty() ? nullptr : g.k_scales[l];
+    const float* vs = g.v_scales.empty() ? nullptr : g.v_scales[l];
+    pkv_status s = reshape_and_cache(
+        static_cast<const uint8_t*>(c.k_new) + l * kv_layer * sb,
+        static_cast<const uint8_t*>(c.v_new) + l * kv_layer * sb, c.slot_mapping, g.k_caches[l],
+        g.v_caches[l], B, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.src_dtype,
+        c.kv_dtype, ks, vs, c.device_status, reinterpret_cast<pkv_stream_t>(st));
+    if (s != PKV_OK) return s;
+    s = paged_attention_decode(
+        static_cast<const uint8_t*>(c.q) + l * q_layer * qb, g.k_caches[l], g.v_caches[l],
+        c.block_tables, c.context_lens, B, c.num_q_heads, c.num_kv_heads, c.head_dim,
+        c.block_size, c.num_blocks, c.max_blocks_per_seq, max_ctx, c.scale, c.q_dtype, c.kv_dtype,
+        ks, vs, c.out + l * q_layer, c.workspace, c.workspace_bytes, 0, c.device_status,
+        reinterpret_cast<pkv_stream_t>(st));
+    if (s != PKV_OK) return s;
+  }
+  return PKV_OK;
+}
+
+void release(pkv_decode_graph* g) {
+  if (!g) return;
+  for (cudaGraphExec_t e : g->execs)
+    if (e) cudaGraphExecDestroy(e);
+  delete g;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status decode_graph_create(const pkv_decode_graph_config* cfg,
+                                          pkv_decode_graph** out) {
+  using namespace pkv;
+  if (!cfg || !out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const pkv_decode_graph_config& c = *cfg;
+  if (c.num_layers <= 0 || c.num_buckets <= 0 || !c.buckets || !c.k_caches || !c.v_caches ||
+      !c.q || !c.k_new || !c.v_new || !c.slot_mapping || !c.block_tables || !c.context_lens ||
+      !c.out || c.max_blocks_per_seq <= 0 || c.block_size <= 0 || c.head_dim <= 0 ||
+      c.num_q_heads <= 0 || c.num_kv_heads <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (elem_bytes(c.q_dtype) == 0 || elem_bytes(c.src_dtype) == 0) return PKV_ERR_UNSUPPORTED;
+  const bool scaled = c.kv_dtype == PKV_FP8_E4M3 || c.kv_dtype == PKV_INT8;
+  if (scaled && (!c.k_scales || !c.v_scales)) return PKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < c.num_buckets; ++i)
+    if (c.buckets[i] <= 0 || (i > 0 && c.buckets[i] <= c.buckets[i - 1]))
+      return PKV_ERR_INVALID_ARG;
+  const int64_t max_ctx = static_cast<int64_t>(c.max_blocks_per_seq) * c.block_size;
+  if (max_ctx > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+  const int32_t Bmax = c.buckets[c.num_buckets - 1];
+  const size_t need = paged_attention_workspace_bytes(Bmax, c.num_q_heads, c.num_kv_heads,
+                                                      c.head_dim, static_cast<int32_t>(max_ctx), 0);
+  for (int32_t i = 0; i < c.num_buckets; ++i)   // every bucket's partials fit the workspace
+    if (paged_attention_workspace_bytes(c.buckets[i], c.num_q_heads, c.num_kv_heads, c.head_dim,
+                                        static_cast<int32_t>(max_ctx), 0) > c.workspace_bytes)
+      return PKV_ERR_INVALID_ARG;
+  (void)need;
+
+  pkv_decode_graph* g = new (std::nothrow) pkv_decode_graph();
+  if (!g) return PKV_ERR_HOST_MEMORY;
+  try {
+    g->cfg = c;
+    g->k_caches.assign(c.k_caches, c.k_caches + c.num_layers);
+    g->v_caches.assign(c.v_caches, c.v_caches + c.num_layers);
+    if (scaled) {
+      g->k_scales.assign(c.k_scales, c.k_scales + c.num_layers);
+      g->v_scales.assign(c.v_scales, c.v_scales + c.num_layers);
+    }
+    g->buckets.assign(c.buckets, c.buckets + c.num_buckets);
+    g->execs.assign(c.num_buckets, nullptr);
+  } catch (const std::bad_alloc&) {
+    delete g;
+    return PKV_ERR_HOST_MEMORY;
+  }
+  g->cfg.k_caches = nullptr;   // the copies above are the ones kept
+  g->cfg.v_caches = nullptr;
+  g->cfg.k_scales = nullptr;
+  g->cfg.v_scales = nullptr;
+  g->cfg.buckets = nullptr;
+  cudaGetDevice(&g->device);
+
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    release(g);
+    return PKV_ERR_CUDA;
+  }
+  pkv_status status = PKV_OK;
+  // Load every kernel and set its attributes outside any capture: one run per
+  // bucket with all rows padded (nothing appended, outputs 0).
+  status = pad_rows(g->cfg, 0, Bmax, st);
+  for (int32_t i = 0; status == PKV_OK && i < c.num_buckets; ++i)
+    status = record_step(*g, g->buckets[i], st);
+  if (status == PKV_OK && cudaStreamSynchronize(st) != cudaSuccess) status = PKV_ERR_CUDA;
+  for (int32_t i = 0; status == PKV_OK && i < c.num_buckets; ++i) {
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      status = PKV_ERR_CUDA;
+      break;
+    }
+    const pkv_status rs = record_step(*g, g->buckets[i], st);
+    const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+    if (rs != PKV_OK || ec != cudaSuccess || !graph) {
+      status = rs != PKV_OK ? rs : PKV_ERR_CUDA;
+      if (graph) cudaGraphDestroy(graph);
+      break;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&g->execs[i], graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      g->execs[i] = nullptr;
+      status = PKV_ERR_CUDA;
+      break;
+    }
+  }
+  if (status == PKV_OK && cudaStreamSynchronize(st) != cudaSuccess) status = PKV_ERR_CUDA;
+  cudaStreamDestroy(st);
+  if (status != PKV_OK) {
+    cudaGetLastError();
+    release(g);
+    return status;
+  }
+  *out = g;
+  return PKV_OK;
+}
+
+extern "C" pkv_status decode_graph_launch(pkv_decode_graph* g, int32_t batch, int32_t* bucket_out,
+                                          pkv_stream_t stream) {
+  using namespace pkv;
+  if (!g || batch <= 0 || batch > g->buckets.back()) return PKV_ERR_INVALID_ARG;
+  const auto it = std::lower_bound(g->buckets.begin(), g->buckets.end(), batch);
+  const size_t i = static_cast<size_t>(it - g->buckets.begin());
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const pkv_status s = pad_rows(g->cfg, batch, *it, st);
+  if (s != PKV_OK) return s;
+  if (cudaGraphLaunch(g->execs[i], st) != cudaSuccess) return PKV_ERR_CUDA;
+  if (bucket_out) *bucket_out = *it;
+  return PKV_OK;
+}
+
+extern "C" void decode_graph_destroy(pkv_decode_graph* g) { pkv::release(g); }

@@ -46,6 +46,7 @@ class DecodeWorkload:
     k_head_scale: tuple = ()          # (lo, hi): K of head g scaled by linspace
     prefix_tokens: int = 0            # shared prompt prefix (whole blocks)
     prefix_seqs: int = 0              # sequences 0 .. prefix_seqs-1 share it
+    graph: bool = False               # time the step as a replayed CUDA graph
 
     @property
     def group(self) -> int:
@@ -79,7 +80,11 @@ RAGGED_FP8_LAYER = DecodeWorkload("ragged_fp8_1layer", 256, 32, 32, 128, 16, FP8
 # The 7B layer with an INT8 cache (section 3.1 symmetric codes, per-head scale).
 LLAMA7B_LAYER_INT8 = DecodeWorkload("llama7b_layer_int8", 32, 32, 32, 128, 16, INT8, BF16,
                                     seed=1, ctx_lo=512, ctx_hi=4096)
-EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8)
+# Small-batch decode of all 32 layers of the 7B shape with short contexts, where
+# launch cost matters: timed as a CUDA-graph replay (and eagerly, for contrast).
+LLAMA7B_B8_GRAPH = DecodeWorkload("llama7b_32layer_b8_graph", 8, 32, 32, 128, 16, BF16, BF16,
+                                  seed=9, num_layers=32, ctx_lo=256, ctx_hi=1024, graph=True)
+EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8, LLAMA7B_B8_GRAPH)
 
 
 @dataclass(frozen=True)
