@@ -119,6 +119,19 @@ def copy_blocks(pool, pairs):
         pool[:, :, int(dst)] = pool[:, :, int(src)]
 
 
+# -- swap: "ToPG framework" section 2.3 (pages beyond device memory) -----------
+def swap_blocks(pool, host, pairs, to_host: bool):
+    """``pool [num_layers, 2, num_blocks, ...]``, ``host [num_host_blocks,
+    num_layers, 2, ...]`` (in place): each (source, destination) pair copies a
+    whole block, every layer's K and V, from the pool to a host slot
+    (``to_host``) or from a host slot to the pool."""
+    for src, dst in pairs:
+        if to_host:
+            host[int(dst)] = pool[:, :, int(src)]
+        else:
+            pool[:, :, int(dst)] = host[int(src)]
+
+
 # -- gather: section 4.2 get_kv ------------------------------------------------
 def gather_sequence(cache, table, seq_len: int):
     """Concatenate the first ``seq_len`` rows of the table's blocks, in order."""

@@ -36,6 +36,15 @@ Follows "LLM inference tutorial" (xurj.top Tutorial/Detail/167):
   entry is dropped together with its block references (the "free" reading of
   the page's "keep or free").  Entries are keyed by the token tuple itself, so
   there are no hash collisions to resolve;
+* "ToPG framework", section 2.3: pages managed by an LRU policy, so contexts
+  can outgrow device memory.  Reading taken (the policy is not spelled out):
+  the pool orders resident sequences by their last append (least recently
+  used first, ties by id); a sequence swapped out moves its private blocks
+  (count 1) to host slots taken from a FIFO host free list, its shared blocks
+  stay on the device, and it takes no appends, forks or batch views until it
+  is swapped back in, when each host block gets a device block from the
+  free-list front.  Each swap returns the (source, destination) pairs the
+  caller copies on the device;
 * "nano-vLLM architecture", section 4.3: ``block_bytes = 2 * num_layers *
   block_size * num_kv_heads * head_dim * dtype_size`` and ``available_blocks =
   free_memory // block_bytes``.
@@ -96,6 +105,11 @@ class Pool:
     lens: dict = field(init=False, default_factory=dict)
     copies: list = field(init=False, default_factory=list)
     prefix: dict = field(init=False, default_factory=dict)
+    host_free: deque = field(init=False, default_factory=deque)
+    host_blocks: int = field(init=False, default=0)
+    on_host: dict = field(init=False, default_factory=dict)      # sid -> set of table indices
+    last_use: dict = field(init=False, default_factory=dict)
+    clock: int = field(init=False, default=0)
 
     def __post_init__(self):
         if self.num_blocks <= 0 or self.block_size <= 0:
@@ -110,6 +124,11 @@ class Pool:
         self.lens = {}
         self.copies = []
         self.prefix = {}
+        self.host_free = deque()
+        self.host_blocks = 0
+        self.on_host = {}
+        self.last_use = {}
+        self.clock = 0
 
     # -- blocks (section 4.2 free list, section 4.3 reference counts) --------
     def block_alloc(self) -> int:
@@ -138,12 +157,23 @@ class Pool:
             self.free.append(b)
 
     # -- sequences (section 4.2 allocate_sequence / append_token / free) -----
+    def _touch(self, sid: int):
+        self.clock += 1
+        self.last_use[sid] = self.clock
+
+    def _resident(self, sid: int):
+        if sid not in self.tables:
+            raise PoolError(INVALID_ARG, f"unknown sequence {sid}")
+        if sid in self.on_host:
+            raise PoolError(INVALID_ARG, f"sequence {sid} is swapped out")
+
     def seq_create(self, sid: int):
         if sid in self.tables:
             raise PoolError(INVALID_ARG, f"sequence {sid} exists")
         b = self.block_alloc()
         self.tables[sid] = [b]
         self.lens[sid] = 0
+        self._touch(sid)
 
     def seq_fork_prefix(self, dst: int, src: int, ntok: int):
         """New sequence ``dst`` sharing the first ``ntok`` tokens of ``src``.
@@ -153,7 +183,7 @@ class Pool:
         write into it (by either sequence).  ``ntok == len(src)`` is a full
         fork (a beam).
         """
-        if dst in self.tables or src not in self.tables:
+        if dst in self.tables or src not in self.tables or src in self.on_host:
             raise PoolError(INVALID_ARG, "bad fork ids")
         if ntok <= 0 or ntok > self.lens[src]:
             raise PoolError(INVALID_ARG, "fork length must be 1 .. len(src)")
@@ -162,6 +192,7 @@ class Pool:
             self.block_ref(b)
         self.tables[dst] = list(shared)
         self.lens[dst] = ntok
+        self._touch(dst)
 
     def _shared_target(self, sid: int) -> bool:
         """The block the next token of ``sid`` goes to exists and is shared."""
@@ -199,17 +230,19 @@ class Pool:
         if len(set(sids)) != len(sids):
             raise PoolError(INVALID_ARG, "repeated sequence id")
         for s in sids:
-            if s not in self.tables:
-                raise PoolError(INVALID_ARG, f"unknown sequence {s}")
+            self._resident(s)
         need = sum(1 for s in sids if self._needs_block(s, 0))
         if need > len(self.free):
             raise PoolError(NO_FREE_BLOCK, f"need {need}, have {len(self.free)}")
-        return [self._append_one(s) for s in sids]
+        out = []
+        for s in sids:
+            out.append(self._append_one(s))
+            self._touch(s)
+        return out
 
     def seq_append_tokens(self, sid: int, n: int) -> list[int]:
         """Append ``n`` tokens to one sequence (a prompt); all-or-nothing."""
-        if sid not in self.tables:
-            raise PoolError(INVALID_ARG, f"unknown sequence {sid}")
+        self._resident(sid)
         if n < 0:
             raise PoolError(INVALID_ARG, "negative count")
         have = len(self.tables[sid]) * self.block_size
@@ -218,7 +251,9 @@ class Pool:
             need += 1
         if need > len(self.free):
             raise PoolError(NO_FREE_BLOCK, f"need {need}, have {len(self.free)}")
-        return [self._append_one(sid) for _ in range(n)]
+        out = [self._append_one(sid) for _ in range(n)]
+        self._touch(sid)
+        return out
 
     def take_copies(self) -> list[tuple[int, int]]:
         """The pending (source block, new block) copies, oldest first; clears them."""
@@ -230,7 +265,8 @@ class Pool:
         """``cache_prefix``: the blocks holding ``sid``'s first ``len(tokens)``
         tokens are remembered under ``tokens`` with count 1."""
         key = tuple(int(t) for t in tokens)
-        if sid not in self.tables or not key or len(key) > self.lens[sid] or key in self.prefix:
+        if (sid not in self.tables or sid in self.on_host or not key or len(key) > self.lens[sid]
+                or key in self.prefix):
             raise PoolError(INVALID_ARG, "bad prefix insert")
         blocks = self.tables[sid][: -(-len(key) // self.block_size)]
         for b in blocks:
@@ -264,6 +300,7 @@ class Pool:
             self.block_ref(b)
         self.tables[sid] = blocks
         self.lens[sid] = length
+        self._touch(sid)
         return length
 
     def prefix_release(self, tokens):
@@ -286,10 +323,64 @@ class Pool:
     def seq_free(self, sid: int):
         if sid not in self.tables:
             raise PoolError(INVALID_ARG, f"unknown sequence {sid}")
-        for b in self.tables[sid]:
-            self.block_free(b)
+        host = self.on_host.pop(sid, set())
+        for j, b in enumerate(self.tables[sid]):
+            if j in host:
+                self.host_free.append(b)
+            else:
+                self.block_free(b)
         del self.tables[sid]
         del self.lens[sid]
+        del self.last_use[sid]
+
+    # -- swap to host memory (ToPG section 2.3, LRU) ---------------------------
+    def host_init(self, num_host_blocks: int):
+        """Host swap area of ``num_host_blocks`` block slots, FIFO free list."""
+        if self.host_blocks or num_host_blocks <= 0:
+            raise PoolError(INVALID_ARG, "host area already set or empty")
+        self.host_blocks = num_host_blocks
+        self.host_free = deque(range(num_host_blocks))
+
+    def lru_order(self) -> list[int]:
+        """Resident sequences, least recently appended first (ties by id)."""
+        return sorted((s for s in self.tables if s not in self.on_host),
+                      key=lambda s: (self.last_use[s], s))
+
+    def seq_swap_out(self, sid: int) -> list[tuple[int, int]]:
+        """Move the sequence's private blocks (count 1) to host slots; returns
+        the (device block, host slot) pairs, in table order, for the copy."""
+        self._resident(sid)
+        priv = [j for j, b in enumerate(self.tables[sid]) if self.ref[b] == 1]
+        if len(priv) > len(self.host_free):
+            raise PoolError(NO_FREE_BLOCK, f"need {len(priv)} host blocks")
+        pairs = []
+        t = self.tables[sid]
+        for j in priv:
+            h = self.host_free.popleft()
+            pairs.append((t[j], h))
+            self.block_free(t[j])
+            t[j] = h
+        self.on_host[sid] = set(priv)
+        return pairs
+
+    def seq_swap_in(self, sid: int) -> list[tuple[int, int]]:
+        """Give every host block of a swapped-out sequence a device block from
+        the free-list front; returns the (host slot, device block) pairs."""
+        if sid not in self.on_host:
+            raise PoolError(INVALID_ARG, f"sequence {sid} is not swapped out")
+        host = sorted(self.on_host[sid])
+        if len(host) > len(self.free):
+            raise PoolError(NO_FREE_BLOCK, f"need {len(host)} device blocks")
+        pairs = []
+        t = self.tables[sid]
+        for j in host:
+            b = self.block_alloc()
+            pairs.append((t[j], b))
+            self.host_free.append(t[j])
+            t[j] = b
+        del self.on_host[sid]
+        self._touch(sid)
+        return pairs
 
     # -- views ----------------------------------------------------------------
     def block_table(self, sid: int) -> list[int]:
@@ -299,6 +390,7 @@ class Pool:
         """``[len(sids), max_blocks]`` table rows padded with ``pad``, and lens."""
         rows, lens = [], []
         for s in sids:
+            self._resident(s)
             t = self.tables[s]
             if len(t) > max_blocks:
                 raise PoolError(INVALID_ARG, "table longer than max_blocks")

@@ -191,19 +191,34 @@ def test_copy_on_write_counts_in_all_or_nothing():
     assert pool.seq_append_tokens(1, 3) and pool.lens[1] == 5 and len(pool.copies) == 1
 
 
-def _check_beams(seed, bs, nb, steps, drain=True):
-    """Random forks, appends and frees with a cache of token values; after every
-    append the copy queue is executed before the writes.  Returns the largest
-    mismatch between each live sequence's gathered cache and its own history."""
+def _check_beams(seed, bs, nb, steps, drain=True, swaps=False, swap_in_copy=True):
+    """Random forks, appends, frees (and swaps) with a cache of token values;
+    after every append the copy queue is executed before the writes, and every
+    swap's pairs are copied at once.  Returns the largest mismatch between each
+    live sequence's gathered cache and its own history."""
     from oracle import attention as A
     r = np.random.default_rng(seed)
     pool = P.Pool(1, 1, 1, bs, 4, nb, initial_free_order=r.permutation(nb).tolist())
     cache = np.full((1, 2, nb, bs, 1, 1), np.nan)
+    host = np.full((nb, 1, 2, bs, 1, 1), np.nan)
+    if swaps:
+        pool.host_init(nb)
     hist, nid, val = {}, 0, 0.0
     for _ in range(steps):
-        op = r.integers(0, 6)
-        live = sorted(hist)
+        op = r.integers(0, 8 if swaps else 6)
+        live = sorted(s for s in hist if s not in pool.on_host)
         try:
+            if op == 6:
+                if live:
+                    A.swap_blocks(cache, host, pool.seq_swap_out(int(r.choice(live))), True)
+                continue
+            if op == 7:
+                out = sorted(pool.on_host)
+                if out:
+                    pairs = pool.seq_swap_in(int(r.choice(out)))
+                    if swap_in_copy:
+                        A.swap_blocks(cache, host, pairs, False)
+                continue
             if op == 0 or not live:
                 pool.seq_create(nid)
                 hist[nid] = []
@@ -231,10 +246,18 @@ def _check_beams(seed, bs, nb, steps, drain=True):
                 del hist[sid]
         except P.PoolError as e:
             assert e.status == P.NO_FREE_BLOCK
+    for sid in sorted(pool.on_host):
+        try:
+            A.swap_blocks(cache, host, pool.seq_swap_in(sid), False)
+        except P.PoolError:
+            pass                        # read from the host slots below
     worst = 0.0
     for sid, h in hist.items():
+        on_host = pool.on_host.get(sid, set())
         for kv in (0, 1):
-            got = A.gather_sequence(cache[0, kv], pool.tables[sid], len(h))[:, 0, 0]
+            rows = [host[b, 0, kv] if j in on_host else cache[0, kv, b]
+                    for j, b in enumerate(pool.tables[sid])]
+            got = (np.concatenate(rows)[: len(h), 0, 0] if rows else np.zeros(0))
             d = np.abs(got - np.asarray(h)) if h else np.zeros(1)
             worst = max(worst, float(np.nan_to_num(d, nan=1e9).max()))
     return worst
@@ -300,3 +323,51 @@ def test_prefix_lookup_equals_brute_force_scan():
         best = max((len(e) for e in entries if tuple(q[:len(e)]) == e), default=0)
         hit = pool.prefix_lookup(q)
         assert (hit[1] if hit else 0) == best
+
+
+@pytest.mark.parametrize("seed,bs", [(0, 4), (1, 1), (2, 16)])
+def test_swapped_sequences_read_back_their_history(seed, bs):
+    """Swapping out (device -> host copies) and back in (host -> device) in the
+    middle of forks and appends never changes what a sequence reads."""
+    assert _check_beams(seed, bs, 96, 900, swaps=True) == 0.0
+
+
+def test_skipping_the_swap_in_copy_is_caught():
+    assert _check_beams(0, 4, 96, 900, swaps=True, swap_in_copy=False) > 0.0
+
+
+def test_swap_trace_and_lru_order():
+    """Hand-derived: private blocks go to host slots (FIFO), shared ones stay;
+    swap-in takes device blocks from the free-list front; LRU = last append."""
+    pool = P.Pool(1, 1, 8, 4, 2, 8)
+    pool.host_init(3)
+    pool.seq_create(0)
+    pool.seq_append_tokens(0, 6)            # blocks 0, 1
+    pool.seq_fork_prefix(1, 0, 4)           # shares block 0
+    pool.seq_create(2)                      # block 2
+    assert pool.lru_order() == [0, 1, 2]
+    pool.seq_append_slots([0])
+    assert pool.lru_order() == [1, 2, 0]
+    assert pool.seq_swap_out(0) == [(1, 0)]          # block 1 private, block 0 shared
+    assert pool.tables[0] == [0, 0] and pool.on_host[0] == {1}
+    assert list(pool.free)[-1] == 1 and pool.lru_order() == [1, 2]
+    with pytest.raises(P.PoolError):
+        pool.seq_append_slots([0])                  # swapped out: no appends
+    with pytest.raises(P.PoolError):
+        pool.padded_tables([0], 4)
+    assert pool.seq_swap_in(0) == [(0, 3)]           # free list front is block 3
+    assert pool.tables[0] == [0, 3] and list(pool.host_free) == [1, 2, 0]
+    assert pool.lru_order() == [1, 2, 0]
+    pool.seq_swap_out(2)
+    pool.seq_free(2)                                 # its host slot goes back
+    assert list(pool.host_free) == [2, 0, 1]
+
+
+def test_swap_out_is_all_or_nothing():
+    pool = P.Pool(1, 1, 8, 4, 2, 8)
+    pool.host_init(1)
+    pool.seq_create(0)
+    pool.seq_append_tokens(0, 8)
+    with pytest.raises(P.PoolError) as e:
+        pool.seq_swap_out(0)
+    assert e.value.status == P.NO_FREE_BLOCK and pool.tables[0] == [0, 1]
