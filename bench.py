@@ -46,7 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged decode attention: effective KV GB/s (% HBM peak), decode tokens/s"
 PREFILL_METRIC = "paged prefill attention: TFLOP/s (% bf16 tensor peak), prefill tokens/s"
 FORK_METRIC = "copy-on-write block copies of a beam fork: GB/s (distinct sources read + copies written; % HBM peak)"
-WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL + W.FORK}
+SWAP_METRIC = "swap of whole sequences to host memory and back: GB/s over the host link"
+WORKLOADS = {w.name: w for w in W.ALL + W.EXTRA + W.PREFILL + W.FORK + W.SWAP}
 DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
@@ -993,6 +994,193 @@ def run_fork_reference(args):
     }), flush=True)
 
 
+# ------------------------------------------------------------- swap arm ---
+class SwapStep:
+    """Every sequence swapped out (device -> host) and back in, through the
+    pool and swap_blocks; the host area is page-locked memory."""
+
+    def __init__(self, w, device):
+        import torch
+        import paged_kv_cache_295_gb300 as pkv
+        from paged_kv_cache_295_gb300.engine import PagedKVCache
+        self.w = w
+        self.lens = W.swap_lens(w)
+        bs = w.block_size
+        blocks = int((-(-self.lens // bs)).sum())
+        nb = blocks + 16
+        self.eng = eng = PagedKVCache(w.num_layers, w.num_kv_heads, w.head_dim, bs, nb, pkv.BF16,
+                                      device=device, initial_free_order=W.free_order(w, nb),
+                                      poison=False)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 1000)
+        for layer in range(w.num_layers):
+            eng.storage[layer].copy_(torch.randn(eng.storage[layer].shape, generator=gen,
+                                                 device=device).to(torch.bfloat16))
+        eng.host_area(blocks)
+        for s, n in enumerate(self.lens):
+            eng.pool.seq_create(s)
+            eng.pool.append_tokens(s, int(n), want_slots=False)
+        plane = eng.storage[0, 0]
+        self.block_bytes = plane[0].numel() * plane.element_size()
+        self.moved = blocks * 2 * w.num_layers * self.block_bytes   # each way
+        self.nb = nb
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def run(self, ev=None):
+        seqs = range(len(self.lens))
+        if ev is not None:
+            ev[0].record()
+        for s in seqs:
+            self.eng.swap_out(s, device_status=self.status)
+        if ev is not None:
+            ev[1].record()
+        for s in seqs:
+            self.eng.swap_in(s, device_status=self.status)
+        if ev is not None:
+            ev[2].record()
+
+
+def link_reference(device, nbytes=1 << 30, reps=5):
+    """GB/s of cudaMemcpyAsync between page-locked host memory and the device."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    res = {}
+    for name, fn in (("d2h_gbs", lambda: h.copy_(d, non_blocking=True)),
+                     ("h2d_gbs", lambda: d.copy_(h, non_blocking=True))):
+        fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        res[name] = nbytes / min(ts) / 1e9
+    del h, d
+    return res
+
+
+def run_swap(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be >= 3")
+    link = link_reference(dev)
+    st = SwapStep(w, dev)
+    for _ in range(Wm):
+        st.run()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for i in range(K):
+        st.run(ev[i])
+    torch.cuda.synchronize(dev)
+    dt = max_over_ranks(time.perf_counter() - t, world, dev)
+    barrier(world)
+    clk = clocks.stop()
+    out_s = statistics.fmean(e[0].elapsed_time(e[1]) * 1e-3 for e in ev)
+    in_s = statistics.fmean(e[1].elapsed_time(e[2]) * 1e-3 for e in ev)
+    value = sum_over_ranks(2 * st.moved * K, world, dev) / dt / 1e9
+    out_gbs, in_gbs = st.moved / out_s / 1e9, st.moved / in_s / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args)
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": SWAP_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_layers": w.num_layers,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+                   "context_lens": f"uniform[{w.ctx_lo},{w.ctx_hi}] seed {w.seed}",
+                   "bytes_each_way": st.moved, "num_blocks": st.nb,
+                   "l2": f"inputs larger than L2: {st.moved / 1e9:.2f} GB each way vs 129 MB L2"},
+        "swap_out_gbs": round(out_gbs, 2), "swap_in_gbs": round(in_gbs, 2),
+        "roofline": {"bound": "host_link", "achieved": round(min(out_gbs, in_gbs), 2),
+                     "peak": round(min(link["d2h_gbs"], link["h2d_gbs"]), 2), "unit": "GB/s",
+                     "frac": round(min(out_gbs / link["d2h_gbs"], in_gbs / link["h2d_gbs"]), 4),
+                     "traffic": None,
+                     "peak_source": "in-run cudaMemcpyAsync of 1 GiB between page-locked host "
+                                    "memory and the device (the slower direction)",
+                     "kernel": "swap_blocks_kernel (timed by direction, host pool calls and "
+                               "pair uploads inside)",
+                     "alg_bytes_per_direction": st.moved},
+        "in_run_link_gbs": {k: round(v, 1) for k, v in link.items()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 2), "unit": "GB/s", "steps": K,
+                "ms_per_step": round(dt / K * 1e3, 5),
+                "h2d_bytes_per_step": int(st.moved), "d2h_bytes_per_step": int(st.moved),
+                "timer": "host wall clock over the whole step (pool calls, pair uploads, "
+                         "both directions)"},
+        "gpu_launches": 2 * w.num_seqs * K, "clocks": clk,
+        "device_status": int(st.status.item()), "kernel_sources_sha": kernel_sources_sha(),
+    }), flush=True)
+
+
+def run_swap_reference(args):
+    """The oracle pool's swap out and in plus its host copies for one sequence
+    per step, on a host pool of the workload's plane shape."""
+    from oracle import attention as OA
+    from oracle import pool as OP
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    lens = W.swap_lens(w)
+    n = int(lens[0])
+    nb = -(-n // w.block_size) + 2
+    pool = W.store(W.rng(w.seed, 900).standard_normal(
+        (w.num_layers, 2, nb, w.block_size, w.num_kv_heads, w.head_dim), dtype=np.float32), "bf16")
+    host = np.zeros((nb,) + pool.shape[:2] + pool.shape[3:], dtype=pool.dtype)
+    op = OP.Pool(w.num_layers, w.num_kv_heads, w.head_dim, w.block_size, 2, nb)
+    op.host_init(nb)
+    op.seq_create(0)
+    op.seq_append_tokens(0, n)
+    moved = 0
+
+    def step():
+        OA.swap_blocks(pool, host, op.seq_swap_out(0), True)
+        pairs = op.seq_swap_in(0)
+        OA.swap_blocks(pool, host, pairs, False)
+        return 2 * len(pairs) * pool[:, :, 0].nbytes
+
+    for _ in range(Wm):
+        step()
+    t = time.perf_counter()
+    for _ in range(K):
+        moved += step()
+    dt = time.perf_counter() - t
+    value = moved / dt / 1e9
+    sample = f"sequence 0 ({n} tokens) out and back in per step, {K} steps, numpy, 1 thread"
+    print(json.dumps({
+        "impl": "reference", "metric": SWAP_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 # ------------------------------------------------- reference arm (oracle) ---
 def workload_config(w, lens, nb):
     """The workload description both arms report (no launch details)."""
@@ -1115,8 +1303,8 @@ def cpu_baseline(args):
     """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
     w = WORKLOADS[args.workload]
     prefill = isinstance(w, W.PrefillWorkload)
-    if isinstance(w, W.ForkWorkload):
-        steps = 200
+    if isinstance(w, (W.ForkWorkload, W.SwapWorkload)):
+        steps = 100
     else:
         lens = W.prefill_lens(w)[1] if prefill else W.context_lens(w)
         per_step = float(np.mean(lens)) * w.num_q_heads * 1.2e-6     # ~1.2 us per token-head
@@ -1155,6 +1343,8 @@ def main(argv=None):
         arms = (run_prefill_reference, run_prefill)
     elif isinstance(w, W.ForkWorkload):
         arms = (run_fork_reference, run_fork)
+    elif isinstance(w, W.SwapWorkload):
+        arms = (run_swap_reference, run_swap)
     else:
         arms = (run_reference, run_ours)
     arms[0 if args.impl == "reference" else 1](args)

@@ -15,8 +15,9 @@
  *   [TGI]  "TGI architecture" (intelliparadigm 2004249), section 3.2 paged
  *          blocks of 128-256 tokens shared between requests; 5.1 CUDA graphs
  *          recorded for common batch sizes at warm-up.
- *   [TOPG] "ToPG framework" (intelliparadigm 2232463), section 3.3: the KV
- *          cache stored compressed as FP8.
+ *   [TOPG] "ToPG framework" (intelliparadigm 2232463), section 2.3: KV pages
+ *          managed LRU so contexts can exceed device memory; section 3.3: the
+ *          KV cache stored compressed as FP8.
  *
  * Conventions for every call:
  *   - Host functions never abort; they return a pkv_status.
@@ -178,6 +179,33 @@ pkv_status seq_free(pkv_pool* pool, int64_t seq_id);
  * is a fresh block that is nobody's source. */
 pkv_status pool_take_copies(pkv_pool* pool, int32_t* pairs, int32_t cap, int32_t* n);
 
+/* Swap to host memory [TOPG 2.3: pages managed LRU, contexts beyond device
+ * memory].  The pool's clock ticks on every seq_create, fork, append and
+ * swap-in; a sequence's last tick orders it for eviction.
+ *   kv_pool_host_init: a host swap area of num_host_blocks block slots (FIFO
+ *     free list 0 .. n-1); once per pool.
+ *   pool_lru_order: resident sequence ids, least recently used first, into
+ *     seq_ids[0 .. cap); *n = their number (INVALID_ARG if cap < *n).
+ *   seq_swap_out: every block of the sequence with reference count 1 moves to
+ *     a host slot (front of the host free list; the device block goes to the
+ *     free-list tail), in table order; shared blocks stay.  pairs[0 .. 2 *n)
+ *     = (device block, host slot).  Copy them device -> host (swap_blocks)
+ *     before the freed device blocks are written again.  All-or-nothing:
+ *     NO_FREE_BLOCK if the host area is short; INVALID_ARG (nothing changed,
+ *     *n = pairs needed) if cap < *n.
+ *   seq_swap_in: every host block of a swapped-out sequence gets a device
+ *     block from the free-list front; pairs = (host slot, device block); copy
+ *     them host -> device before the sequence is read.  Same error rules.
+ *   seq_is_swapped: 1 while the sequence is swapped out.
+ * A swapped-out sequence refuses appends, forks, prefix inserts and batch
+ * tables (INVALID_ARG); seq_free returns its host slots to the host free-list
+ * tail. */
+pkv_status kv_pool_host_init(pkv_pool* pool, int64_t num_host_blocks);
+pkv_status pool_lru_order(const pkv_pool* pool, int64_t* seq_ids, int64_t cap, int64_t* n);
+pkv_status seq_swap_out(pkv_pool* pool, int64_t seq_id, int32_t* pairs, int32_t cap, int32_t* n);
+pkv_status seq_swap_in(pkv_pool* pool, int64_t seq_id, int32_t* pairs, int32_t cap, int32_t* n);
+pkv_status seq_is_swapped(const pkv_pool* pool, int64_t seq_id, int32_t* swapped);
+
 /* Prefix cache [TUT 4.3 PrefixCacheManager].  Entries are keyed by the token
  * ids themselves (host int32 arrays; a hash only speeds the search and a hit
  * is confirmed token by token).
@@ -312,6 +340,21 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
  * plane_stride_bytes multiples of 16. */
 pkv_status copy_blocks(void* base, int32_t num_planes, int64_t plane_stride_bytes,
                        int64_t block_bytes, int64_t num_blocks, const int32_t* pairs, int32_t n,
+                       int32_t* device_status, pkv_stream_t stream);
+
+/* Swap copies [TOPG 2.3]: for each pair of pairs[0 .. 2n) (device int32),
+ * with to_host = 1 (device block, host slot): host slot <- every plane's
+ * block; with to_host = 0 (host slot, device block): every plane's block <-
+ * host slot.  Planes as in copy_blocks.  host is page-locked host memory
+ * (cudaHostAlloc / pinned) of num_host_blocks slots, slot h holding
+ * [num_planes][block_bytes] at host + h * num_planes * block_bytes; the
+ * kernel reads and writes it directly over the host link.  Ids outside
+ * [0, num_blocks) or [0, num_host_blocks) are skipped and flagged
+ * PKV_DEV_BAD_BLOCK.  INVALID_ARG if host is not page-locked memory the
+ * device can address. */
+pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_bytes,
+                       int64_t block_bytes, int64_t num_blocks, void* host,
+                       int64_t num_host_blocks, const int32_t* pairs, int32_t n, int32_t to_host,
                        int32_t* device_status, pkv_stream_t stream);
 
 /* Paged prefill attention: a chunk of query tokens per sequence attends,

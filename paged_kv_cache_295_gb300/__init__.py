@@ -90,6 +90,12 @@ _SIGS = {
     "prefix_cache_release": (I32, [P, P, I32]),
     "prefix_cache_count": (I32, [P, P, I32, C.POINTER(I32)]),
     "copy_blocks": (I32, [P, I32, I64, I64, I64, P, I32, P, P]),
+    "kv_pool_host_init": (I32, [P, I64]),
+    "pool_lru_order": (I32, [P, P, I64, C.POINTER(I64)]),
+    "seq_swap_out": (I32, [P, I64, P, I32, C.POINTER(I32)]),
+    "seq_swap_in": (I32, [P, I64, P, I32, C.POINTER(I32)]),
+    "seq_is_swapped": (I32, [P, I64, C.POINTER(I32)]),
+    "swap_blocks": (I32, [P, I32, I64, I64, I64, P, I64, P, I32, I32, P, P]),
     "decode_graph_create": (I32, [C.POINTER(_GraphConfig), C.POINTER(P)]),
     "decode_graph_launch": (I32, [P, I32, C.POINTER(I32), P]),
     "decode_graph_destroy": (None, [P]),
@@ -262,6 +268,39 @@ class Pool:
         _check(library().pool_take_copies(self._h, _np_ptr(buf), buf.shape[0], C.byref(n)),
                "pool_take_copies")
         return buf[: n.value]
+
+    def host_init(self, num_host_blocks: int):
+        _check(library().kv_pool_host_init(self._h, int(num_host_blocks)), "kv_pool_host_init")
+
+    def lru_order(self) -> list:
+        n = C.c_int64()
+        st = library().pool_lru_order(self._h, None, 0, C.byref(n))
+        if st != 0 and n.value == 0:
+            _check(st, "pool_lru_order")
+        buf = np.empty(max(n.value, 1), dtype=np.int64)
+        _check(library().pool_lru_order(self._h, _np_ptr(buf), buf.size, C.byref(n)),
+               "pool_lru_order")
+        return buf[: n.value].tolist()
+
+    def _swap(self, fn, sid, where):
+        n = C.c_int32()
+        cap = max(len(self.block_table(sid)), 1)   # at most one pair per table entry
+        buf = np.empty((cap, 2), dtype=np.int32)
+        _check(fn(self._h, sid, _np_ptr(buf), cap, C.byref(n)), where)
+        return buf[: n.value]
+
+    def swap_out(self, sid: int) -> np.ndarray:
+        """(device block, host slot) pairs ``[k, 2]`` of the sequence's private blocks."""
+        return self._swap(library().seq_swap_out, sid, "seq_swap_out")
+
+    def swap_in(self, sid: int) -> np.ndarray:
+        """(host slot, device block) pairs ``[k, 2]``."""
+        return self._swap(library().seq_swap_in, sid, "seq_swap_in")
+
+    def is_swapped(self, sid: int) -> bool:
+        v = C.c_int32()
+        _check(library().seq_is_swapped(self._h, sid, C.byref(v)), "seq_is_swapped")
+        return bool(v.value)
 
     @staticmethod
     def _tokens(tokens):
@@ -517,6 +556,23 @@ class DecodeGraph:
             self.close()
         except Exception:
             pass
+
+
+def swap_blocks(pool_tensor, host_tensor, pairs, to_host, device_status=None, stream=None):
+    """Block copies between the pool tensor ``[L, 2, NB, bs, Hkv, D]`` and a
+    pinned host tensor ``[H, L, 2, bs, Hkv, D]``; ``pairs`` device int32
+    ``[k, 2]`` ((device, host) to host, (host, device) back)."""
+    L, two, nb = pool_tensor.shape[:3]
+    plane = pool_tensor[0, 0]
+    bb = plane[0].numel() * plane.element_size()
+    if not host_tensor.is_pinned():
+        raise ValueError("host_tensor must be page-locked (pin_memory)")
+    k = pairs.shape[0] if pairs.dim() else 0
+    st = library().swap_blocks(_dev(pool_tensor, "pool"), L * two, nb * bb, bb, nb,
+                               C.c_void_p(host_tensor.data_ptr()), host_tensor.shape[0],
+                               _dev(pairs, "pairs") if k else None, k, 1 if to_host else 0,
+                               _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "swap_blocks")
 
 
 def copy_kernel(src, dst, stream=None):

@@ -18,6 +18,15 @@
 // that the caller drains (pool_take_copies) and executes on the device
 // (copy_blocks) before writing the token.
 //
+// Swap ("ToPG framework" section 2.3: LRU-managed pages, contexts beyond
+// device memory): sequences are ordered by their last create / fork / append
+// (least recently used first); a swap-out moves a sequence's private blocks
+// (count 1) to slots of a host area (FIFO free list) and leaves its shared
+// blocks on the device; a swapped-out sequence takes no append, fork, prefix
+// insert or batch view until its swap-in gives each host block a device block
+// from the free-list front.  Both return the pairs the caller copies
+// (swap_blocks) on its stream.
+//
 // Prefix cache (section 4.3, PrefixCacheManager): entries map a token prefix
 // to the blocks holding it, with a count that starts at 1 (cache_prefix),
 // rises on every hit of the longest-prefix lookup (get_cached_prefix) and
@@ -48,8 +57,10 @@ int dtype_size(int32_t dt) {
 }
 
 struct Seq {
-  std::vector<int32_t> table;
+  std::vector<int32_t> table;     // device block ids; host slot ids where on_host[j]
+  std::vector<uint8_t> on_host;   // empty while resident
   int32_t len = 0;
+  uint64_t last_use = 0;          // pool clock at the last create / fork / append
 };
 
 struct PrefixEntry {
@@ -86,6 +97,21 @@ struct pkv_pool {
   std::vector<int32_t> ref;    // reference count per block (0 = free)
   std::unordered_map<int64_t, Seq> seqs;
   std::vector<std::pair<int32_t, int32_t>> copies;   // pending copy-on-write (src, dst)
+  std::vector<int32_t> host_ring;   // host swap slots, FIFO free list
+  int64_t host_head = 0, host_count = 0, host_blocks = 0;
+  uint64_t clock = 0;
+
+  void touch(Seq& s) { s.last_use = ++clock; }
+  int32_t host_pop() {
+    const int32_t h = host_ring[host_head];
+    host_head = (host_head + 1) % host_blocks;
+    --host_count;
+    return h;
+  }
+  void host_push(int32_t h) {
+    host_ring[(host_head + host_count) % host_blocks] = h;
+    ++host_count;
+  }
   std::unordered_map<uint64_t, std::vector<PrefixEntry>> prefix;   // prefix hash -> entries
 
   // The entry cached for exactly tokens[0..n) (hash h), or nullptr.
@@ -285,6 +311,7 @@ pkv_status seq_create(pkv_pool* p, int64_t sid) {
     const int32_t b = p->pop_front();
     p->ref[b] = 1;
     s.table.push_back(b);
+    p->touch(s);
     p->seqs.emplace(sid, std::move(s));
   } catch (const std::bad_alloc&) {
     return PKV_ERR_HOST_MEMORY;
@@ -295,13 +322,15 @@ pkv_status seq_create(pkv_pool* p, int64_t sid) {
 pkv_status seq_fork_prefix(pkv_pool* p, int64_t dst, int64_t src, int32_t ntok) {
   if (!p) return PKV_ERR_INVALID_ARG;
   auto it = p->seqs.find(src);
-  if (it == p->seqs.end() || p->seqs.count(dst)) return PKV_ERR_INVALID_ARG;
+  if (it == p->seqs.end() || p->seqs.count(dst) || !it->second.on_host.empty())
+    return PKV_ERR_INVALID_ARG;
   const int32_t bs = p->cfg.block_size;
   if (ntok <= 0 || ntok > it->second.len) return PKV_ERR_INVALID_ARG;
   try {
     Seq s;
     s.table.assign(it->second.table.begin(), it->second.table.begin() + (ntok + bs - 1) / bs);
     s.len = ntok;
+    p->touch(s);
     for (int32_t b : s.table) ++p->ref[b];
     p->seqs.emplace(dst, std::move(s));
   } catch (const std::bad_alloc&) {
@@ -320,7 +349,8 @@ pkv_status seq_append_slots(pkv_pool* p, const int64_t* ids, int32_t n, int64_t*
     int64_t need = 0;
     for (int32_t i = 0; i < n; ++i) {
       auto it = p->seqs.find(ids[i]);
-      if (it == p->seqs.end() || !seen.insert(ids[i]).second) return PKV_ERR_INVALID_ARG;
+      if (it == p->seqs.end() || !seen.insert(ids[i]).second || !it->second.on_host.empty())
+        return PKV_ERR_INVALID_ARG;
       if (seq_needs_block(p, it->second)) ++need;
       v.push_back(&it->second);
     }
@@ -338,6 +368,7 @@ pkv_status seq_append_slots(pkv_pool* p, const int64_t* ids, int32_t n, int64_t*
     const int32_t pos = s.len;
     append_one(p, s);
     slots[i] = slot_of(p, s, pos);
+    p->touch(s);
   }
   return PKV_OK;
 }
@@ -345,7 +376,7 @@ pkv_status seq_append_slots(pkv_pool* p, const int64_t* ids, int32_t n, int64_t*
 pkv_status seq_append_tokens(pkv_pool* p, int64_t sid, int32_t n, int64_t* slots) {
   if (!p || n < 0) return PKV_ERR_INVALID_ARG;
   auto it = p->seqs.find(sid);
-  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  if (it == p->seqs.end() || !it->second.on_host.empty()) return PKV_ERR_INVALID_ARG;
   Seq& s = it->second;
   const int64_t bs = p->cfg.block_size;
   const int64_t have = static_cast<int64_t>(s.table.size()) * bs;
@@ -365,6 +396,7 @@ pkv_status seq_append_tokens(pkv_pool* p, int64_t sid, int32_t n, int64_t* slots
     append_one(p, s);
     if (slots) slots[i] = slot_of(p, s, pos);
   }
+  p->touch(s);
   return PKV_OK;
 }
 
@@ -394,7 +426,7 @@ pkv_status seq_batch_tables(const pkv_pool* p, const int64_t* ids, int32_t n, in
     return PKV_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n; ++i) {
     auto it = p->seqs.find(ids[i]);
-    if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+    if (it == p->seqs.end() || !it->second.on_host.empty()) return PKV_ERR_INVALID_ARG;
     if (static_cast<int64_t>(it->second.table.size()) > mb) return PKV_ERR_INVALID_ARG;
   }
   for (int32_t i = 0; i < n; ++i) {
@@ -412,8 +444,13 @@ pkv_status seq_free(pkv_pool* p, int64_t sid) {
   if (!p) return PKV_ERR_INVALID_ARG;
   auto it = p->seqs.find(sid);
   if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
-  for (int32_t b : it->second.table) {
-    if (--p->ref[b] == 0) p->push_back(b);
+  const Seq& s = it->second;
+  for (size_t j = 0; j < s.table.size(); ++j) {
+    const int32_t b = s.table[j];
+    if (!s.on_host.empty() && s.on_host[j])
+      p->host_push(b);
+    else if (--p->ref[b] == 0)
+      p->push_back(b);
   }
   p->seqs.erase(it);
   return PKV_OK;
@@ -436,7 +473,8 @@ pkv_status pool_take_copies(pkv_pool* p, int32_t* pairs, int32_t cap, int32_t* n
 pkv_status prefix_cache_insert(pkv_pool* p, const int32_t* tokens, int32_t n, int64_t sid) {
   if (!p || n <= 0 || !tokens) return PKV_ERR_INVALID_ARG;
   auto it = p->seqs.find(sid);
-  if (it == p->seqs.end() || n > it->second.len) return PKV_ERR_INVALID_ARG;
+  if (it == p->seqs.end() || n > it->second.len || !it->second.on_host.empty())
+    return PKV_ERR_INVALID_ARG;
   try {
     std::vector<uint64_t> h;
     prefix_hashes(tokens, n, h);
@@ -505,6 +543,7 @@ pkv_status seq_create_from_prefix(pkv_pool* p, int64_t sid, const int32_t* token
     Seq s;
     s.table = e->blocks;
     s.len = len;
+    p->touch(s);
     p->seqs.emplace(sid, std::move(s));
     for (int32_t b : e->blocks) ++p->ref[b];
     ++e->count;
@@ -553,6 +592,104 @@ pkv_status prefix_cache_count(const pkv_pool* p, const int32_t* tokens, int32_t 
   } catch (const std::bad_alloc&) {
     return PKV_ERR_HOST_MEMORY;
   }
+  return PKV_OK;
+}
+
+pkv_status kv_pool_host_init(pkv_pool* p, int64_t num_host_blocks) {
+  if (!p || num_host_blocks <= 0 || num_host_blocks > INT32_MAX || p->host_blocks)
+    return PKV_ERR_INVALID_ARG;
+  try {
+    p->host_ring.resize(num_host_blocks);
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  for (int64_t i = 0; i < num_host_blocks; ++i) p->host_ring[i] = static_cast<int32_t>(i);
+  p->host_blocks = num_host_blocks;
+  p->host_head = 0;
+  p->host_count = num_host_blocks;
+  return PKV_OK;
+}
+
+pkv_status pool_lru_order(const pkv_pool* p, int64_t* ids, int64_t cap, int64_t* n) {
+  if (!p || !n || cap < 0) return PKV_ERR_INVALID_ARG;
+  try {
+    std::vector<std::pair<uint64_t, int64_t>> v;
+    v.reserve(p->seqs.size());
+    for (const auto& kv : p->seqs)
+      if (kv.second.on_host.empty()) v.emplace_back(kv.second.last_use, kv.first);
+    std::sort(v.begin(), v.end());
+    *n = static_cast<int64_t>(v.size());
+    if (cap < *n || (!ids && *n > 0)) return PKV_ERR_INVALID_ARG;
+    for (size_t i = 0; i < v.size(); ++i) ids[i] = v[i].second;
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_is_swapped(const pkv_pool* p, int64_t sid, int32_t* swapped) {
+  if (!p || !swapped) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
+  *swapped = it->second.on_host.empty() ? 0 : 1;
+  return PKV_OK;
+}
+
+pkv_status seq_swap_out(pkv_pool* p, int64_t sid, int32_t* pairs, int32_t cap, int32_t* n) {
+  if (!p || !n || cap < 0) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end() || !it->second.on_host.empty()) return PKV_ERR_INVALID_ARG;
+  Seq& s = it->second;
+  int32_t k = 0;
+  for (int32_t b : s.table)
+    if (p->ref[b] == 1) ++k;
+  *n = k;
+  if (cap < k || (!pairs && k > 0)) return PKV_ERR_INVALID_ARG;
+  if (k > p->host_count) return PKV_ERR_NO_FREE_BLOCK;
+  try {
+    s.on_host.assign(s.table.size(), 0);
+  } catch (const std::bad_alloc&) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+  int32_t i = 0;
+  for (size_t j = 0; j < s.table.size(); ++j) {
+    const int32_t b = s.table[j];
+    if (p->ref[b] != 1) continue;
+    const int32_t h = p->host_pop();
+    pairs[2 * i] = b;
+    pairs[2 * i + 1] = h;
+    ++i;
+    p->ref[b] = 0;
+    p->push_back(b);
+    s.table[j] = h;
+    s.on_host[j] = 1;
+  }
+  return PKV_OK;
+}
+
+pkv_status seq_swap_in(pkv_pool* p, int64_t sid, int32_t* pairs, int32_t cap, int32_t* n) {
+  if (!p || !n || cap < 0) return PKV_ERR_INVALID_ARG;
+  auto it = p->seqs.find(sid);
+  if (it == p->seqs.end() || it->second.on_host.empty()) return PKV_ERR_INVALID_ARG;
+  Seq& s = it->second;
+  int32_t k = 0;
+  for (uint8_t f : s.on_host) k += f;
+  *n = k;
+  if (cap < k || (!pairs && k > 0)) return PKV_ERR_INVALID_ARG;
+  if (k > p->count) return PKV_ERR_NO_FREE_BLOCK;
+  int32_t i = 0;
+  for (size_t j = 0; j < s.table.size(); ++j) {
+    if (!s.on_host[j]) continue;
+    const int32_t b = p->pop_front();
+    p->ref[b] = 1;
+    pairs[2 * i] = s.table[j];
+    pairs[2 * i + 1] = b;
+    ++i;
+    p->host_push(s.table[j]);
+    s.table[j] = b;
+  }
+  s.on_host.clear();
+  p->touch(s);
   return PKV_OK;
 }
 

@@ -15,7 +15,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import (BF16, F32, FP8_E4M3, INT8, Pool, copy_blocks, paged_attention_decode,
-               paged_attention_prefill, reshape_and_cache, workspace_bytes)
+               paged_attention_prefill, reshape_and_cache, swap_blocks, workspace_bytes)
 
 
 def _torch():
@@ -78,6 +78,34 @@ class PagedKVCache:
         if pairs.shape[0]:
             d = torch.from_numpy(pairs).to(self.storage.device, non_blocking=False)
             copy_blocks(self.storage, d, device_status=device_status, stream=stream)
+        return pairs
+
+    def host_area(self, num_host_blocks):
+        """Page-locked host swap area ``[H, L, 2, bs, Hkv, D]`` and the pool's
+        host slot list (once)."""
+        torch = _torch()
+        self.pool.host_init(num_host_blocks)
+        self.host = torch.empty((num_host_blocks,) + tuple(self.storage.shape[:2]) +
+                                tuple(self.storage.shape[3:]), dtype=self.storage.dtype,
+                                pin_memory=True)
+        return self.host
+
+    def swap_out(self, sid, device_status=None, stream=None):
+        """Move the sequence's private blocks to host slots (device -> host copies)."""
+        torch = _torch()
+        pairs = self.pool.swap_out(sid)
+        if pairs.shape[0]:
+            swap_blocks(self.storage, self.host, torch.from_numpy(pairs).to(self.storage.device),
+                        True, device_status=device_status, stream=stream)
+        return pairs
+
+    def swap_in(self, sid, device_status=None, stream=None):
+        """Bring a swapped-out sequence back (host -> device copies)."""
+        torch = _torch()
+        pairs = self.pool.swap_in(sid)
+        if pairs.shape[0]:
+            swap_blocks(self.storage, self.host, torch.from_numpy(pairs).to(self.storage.device),
+                        False, device_status=device_status, stream=stream)
         return pairs
 
     def attend(self, layer, q, block_tables, context_lens, max_context_len, out=None,

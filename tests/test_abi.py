@@ -79,10 +79,29 @@ def test_c_pool_replays_oracle_bit_exact(lib, seed):
     order = r.permutation(nb).tolist()
     o = OP.Pool(1, 2, 16, bs, 2, nb, initial_free_order=order)
     c = lib.Pool(1, 2, 16, bs, lib.BF16, num_blocks=nb, initial_free_order=order)
+    o.host_init(24)
+    c.host_init(24)
     live, nid = [], 0
     prompts = {}                       # token ids of a few cached prefixes
     for _ in range(600):
-        op = int(r.integers(0, 10))
+        op = int(r.integers(0, 12))
+        if op == 10 and live:            # swap a sequence out or back in
+            s = int(r.choice(live))
+            if s in o.on_host:
+                fo, fc = o.seq_swap_in, c.swap_in
+            else:
+                fo, fc = o.seq_swap_out, c.swap_out
+            res_o, res_c = {}, {}
+            a = _status_of(lambda: res_o.setdefault("v", fo(s)))
+            b = _c_status_of(lib, lambda: res_c.setdefault("v", fc(s)))
+            assert a == b
+            if a == OP.OK:
+                assert [tuple(x) for x in res_o["v"]] == [tuple(x) for x in res_c["v"].tolist()]
+            assert (s in o.on_host) == c.is_swapped(s)
+            continue
+        if op == 11:
+            assert o.lru_order() == c.lru_order()
+            continue
         if op == 0 or not live:
             a = _status_of(lambda: o.seq_create(nid))
             b = _c_status_of(lib, lambda: c.seq_create(nid))
@@ -171,10 +190,12 @@ def test_c_pool_replays_oracle_bit_exact(lib, seed):
         for s in live:
             assert o.tables[s] == c.block_table(s)
             assert o.lens[s] == c.seq_length(s)
+        assert o.lru_order() == c.lru_order()
         so, sc = o.stats(), c.stats()
         assert (so["used_blocks"], so["free_blocks"]) == (sc["used_blocks"], sc["free_blocks"])
     for b_id in range(nb):
         assert o.ref[b_id] == c.refcount(b_id)
+    live = [s for s in live if s not in o.on_host]
     if live:
         mb = max(len(o.tables[s]) for s in live)
         t_c, l_c = c.batch_tables(live, mb)

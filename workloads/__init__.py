@@ -275,3 +275,31 @@ def fork_prompt_lens(w: ForkWorkload) -> np.ndarray:
     lens = np.where(lens % w.block_size == 0, lens + 1, lens)
     return lens.astype(np.int64)
 
+
+@dataclass(frozen=True)
+class SwapWorkload:
+    """Swapping whole sequences to host memory and back ("ToPG framework"
+    section 2.3: pages beyond device memory): ``num_seqs`` sequences of
+    U[ctx_lo, ctx_hi] tokens over ``num_layers`` layers; one step swaps every
+    sequence out, then back in."""
+    name: str
+    num_seqs: int
+    num_layers: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    seed: int
+    ctx_lo: int
+    ctx_hi: int
+    kv_dtype: str = BF16
+
+
+# 8 layers of the 7B shape, 16 sequences of 256-1024 tokens (~1.2 GB each way).
+SWAP_7B = SwapWorkload("swap_7b_8layer_bf16", 16, 8, 32, 128, 16, seed=10, ctx_lo=256,
+                       ctx_hi=1024)
+SWAP = (SWAP_7B,)
+
+
+def swap_lens(w: SwapWorkload) -> np.ndarray:
+    return rng(w.seed, 1).integers(w.ctx_lo, w.ctx_hi + 1, size=w.num_seqs).astype(np.int64)
+
