@@ -88,8 +88,8 @@ extern "C" pkv_status paged_attention_prefill(
       return PKV_ERR_CUDA;
     configured = static_cast<int>(smem);
   }
-  const int tiles = (max_query_len + p.tile_tokens - 1) / p.tile_tokens;
-  dim3 grid(tiles, num_kv_heads, num_seqs);
+  const int pairs = (max_query_len + 2 * p.tile_tokens - 1) / (2 * p.tile_tokens);
+  dim3 grid(pairs, num_kv_heads, num_seqs);
   kern<<<grid, kPfThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

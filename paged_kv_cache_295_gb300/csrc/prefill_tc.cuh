@@ -6,37 +6,42 @@
 // prefill) attends, causally, over every cached key of its sequence, which the
 // kernel reads through the block table ("nano-vLLM architecture" section 4.2).
 //
-// Work split: one CTA per (query tile, KV head, sequence).  A query tile is
-// 128 accumulator rows: TQ = 128 / G consecutive query tokens times the G
-// query heads that share the KV head ("LLM inference tutorial" section 4.4
+// Work split: one CTA per (pair of query tiles, KV head, sequence).  A query
+// tile is 128 accumulator rows: TQ = 128 / G consecutive query tokens times the
+// G query heads that share the KV head ("LLM inference tutorial" section 4.4
 // GQA), row r = token (r / G), head (r % G), so every K/V byte a CTA loads
-// serves all G heads.  The CTA walks its keys in 64-token tiles:
+// serves all G heads of both tiles.  The CTA walks its keys in 64-token tiles:
 //
-//   S  = Q K^T      tcgen05.mma M=128 N=64  K=128   A = Q   (smem, K-major)
-//                                                   B = K tile (smem, K-major)
-//   P  = 2^(S*scale*log2e - m)  in the softmax warps, one TMEM lane = one row
-//   O += P V        tcgen05.mma M=128 N=128 K=64    A = P   (smem, K-major,
-//                                                        bf16 hi + lo parts)
-//                                                   B = V tile (smem, MN-major)
+//   S_t  = Q_t K^T    tcgen05.mma M=128 N=64  K=128   A = Q_t (smem, K-major)
+//                                                     B = K tile (smem, K-major)
+//   P_t  = 2^(S_t*scale*log2e - m)  in tile t's softmax warpgroup, one TMEM
+//                                   lane = one row
+//   O_t += P_t V      tcgen05.mma M=128 N=128 K=64    A = P_t (smem, K-major,
+//                                                          bf16 hi + lo parts)
+//                                                     B = V tile (smem, MN-major)
 //
-// S (two 64-column buffers) and O (128 columns) live in TMEM.  Warp roles:
-// warps 0-3 softmax (warp w owns TMEM lanes 32w..32w+31, i.e. rows), warp 4
-// TMA producer (lanes issue one tile's boxes in parallel, each box one block's
-// rows), warp 5 MMA issuer.  They talk only through mbarriers.  The running
-// max moves only when a tile's row max exceeds it by more than 2^8, so O is
-// rarely rescaled; a warp that must rescale loads its O lanes, scales and
-// stores them after PV(j-1) completed.  Every wait is bounded (2 s) and gives
-// up when another role has given up; TMEM is released before the CTA exits.
+// for t = A (the earlier tokens) and B.  TMEM: per tile, S in two 64-column
+// buffers and O in 128 columns (512 columns in all).  Warp roles: warps 0-3
+// softmax of tile A, warps 4-7 softmax of tile B (warp w owns TMEM lanes
+// 32(w%4)..+31, i.e. rows), warp 8 TMA producer (lanes look up one key tile's
+// blocks in one round trip and issue its boxes), warp 9 MMA issuer (event-
+// driven: whichever QK or PV is ready next, so QK runs ahead).  The two
+// softmax warpgroups work on the same key tile at once, so each SM sub-
+// partition has two softmax warps to interleave.  Tile A needs no key past
+// its last token: its MMAs and softmax stop there.  The running max moves only
+// when a tile's row max exceeds it by more than 2^8, so O is rarely rescaled.
+// Every wait is bounded (2 s) and gives up when another role has given up;
+// TMEM is released before the CTA exits.
 #pragma once
 
 #include "decode_tc.cuh"
 
 namespace pkv {
 
-constexpr int kPfRows = 128;   // accumulator rows per CTA (M)
+constexpr int kPfRows = 128;   // accumulator rows per query tile (M)
 constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
 constexpr int kPfD = 128;
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;   // 2 softmax warpgroups, producer warp, MMA warp
 constexpr int kPfStages = 3;
 
 struct PrefillParams {
@@ -52,26 +57,11 @@ struct PrefillParams {
   int32_t max_blocks_per_seq;
   int32_t bs_log2;
   int32_t box_rows;              // min(block_size, 64)
-  int32_t tile_tokens;           // TQ = 128 / G
+  int32_t tile_tokens;           // TQ = 128 / G tokens per query tile (two per CTA)
   int32_t causal;
   int32_t max_context_len;       // host bound: larger context_lens are flagged
   int32_t num_tokens;            // T: rows of q and out
   float qk_scale_log2;
-};
-
-struct PfLayout {
-  // [Q: 2 x 16 KB][P buffer 0: hi 16 KB, lo 16 KB][P buffer 1][stages: K 16 KB, V 16 KB]
-  static constexpr int kQHalf = kPfRows * 128;         // [128 rows][128 B]
-  static constexpr int kQ = 0;
-  static constexpr int kP = 2 * kQHalf;
-  static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
-  static constexpr int kPBuf = 2 * kPPart;             // hi + lo
-  static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
-  static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
-  static constexpr int kStages = kP + 2 * kPBuf;
-  static constexpr size_t bytes(int stages) {
-    return 1024 + static_cast<size_t>(kStages) + static_cast<size_t>(stages) * kStage;
-  }
 };
 
 // 2^x with the MUFU instruction (relative error about 2^-22; 2^-inf = +0,
@@ -104,8 +94,35 @@ __device__ __forceinline__ void pf_ld64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+struct PfLayout {
+  // [Q_A 2 x 16 KB][Q_B][P_A: hi 16 KB, lo 16 KB][P_B][stages: K 16 KB, V 16 KB]
+  static constexpr int kQHalf = kPfRows * 128;         // [128 rows][128 B]
+  static constexpr int kQ = 2 * kQHalf;                // one query tile
+  static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
+  static constexpr int kPBuf = 2 * kPPart;             // hi + lo
+  static constexpr int kP = 2 * kQ;                    // P_A, then P_B
+  static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
+  static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
+  static constexpr int kStages = kP + 2 * kPBuf;
+  static constexpr size_t bytes(int stages) {
+    return 1024 + static_cast<size_t>(kStages) + static_cast<size_t>(stages) * kStage;
+  }
+};
+
+// Non-blocking check of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 template <int STAGES>
-__global__ void __launch_bounds__(kPfThreads)
+__global__ void __launch_bounds__(kPfThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   using LY = PfLayout;
@@ -114,7 +131,7 @@ __global__ void __launch_bounds__(kPfThreads)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
-  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+  __shared__ __align__(8) uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], drain;
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -123,7 +140,7 @@ __global__ void __launch_bounds__(kPfThreads)
   volatile int* abort_flag = &abort_sh;
 
   const int s = blockIdx.z, g = blockIdx.y;
-  const int tile = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
+  const int pair = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int q0 = __ldg(p.query_start + s);
@@ -133,53 +150,61 @@ __global__ void __launch_bounds__(kPfThreads)
     return;
   }
   const int n = q1 - q0;
-  if (tile == 0 && tid == 0 && n > static_cast<int>(gridDim.x) * TQ)
+  if (pair == 0 && tid == 0 && n > 2 * static_cast<int>(gridDim.x) * TQ)
     flag_status(p.status, PKV_DEV_BAD_CONTEXT);   // more queries than max_query_len
-  const int tok0 = tile * TQ;
+  const int tok0 = pair * 2 * TQ;                 // tile A: tok0 .., tile B: tok0 + TQ ..
   if (n <= 0 || tok0 >= n) return;
+  const bool has_b = tok0 + TQ < n;
   int ctx = __ldg(p.context_lens + s);
   const int cap = min(p.max_context_len, p.max_blocks_per_seq << p.bs_log2);
   if (ctx < n || ctx > cap) {   // queries must be the last n of a context the table covers
-    if (tile == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
-    const int ntok = min(TQ, n - tok0);
+    if (pair == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    const int ntok = min(2 * TQ, n - tok0);
     for (int i = tid; i < ntok * G * kPfD; i += kPfThreads) {
       const int t = i / (G * kPfD), r = i % (G * kPfD);
       p.out[(static_cast<int64_t>(q0 + tok0 + t) * p.num_q_heads + g * G) * kPfD + r] = 0.f;
     }
     return;
   }
-  const int tok_end = min(tok0 + TQ, n);
-  const int nkeys = p.causal ? ctx - n + tok_end : ctx;
-  const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
+  // key tiles each query tile needs (causal: up to its last token's position)
+  const int end_a = min(tok0 + TQ, n), end_b = min(tok0 + 2 * TQ, n);
+  const int nt_a = ((p.causal ? ctx - n + end_a : ctx) + kPfKeys - 1) / kPfKeys;
+  const int nt_b = has_b ? ((p.causal ? ctx - n + end_b : ctx) + kPfKeys - 1) / kPfKeys : 0;
+  const int ntiles = max(nt_a, nt_b);
   const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
 
-  // Q (A operand of QK): row r = token tok0 + r / G, head g*G + r % G; 16-byte
-  // chunks into two 128-byte-swizzled halves.  Rows past the chunk are zero.
-  for (int i = tid; i < kPfRows * 16; i += kPfThreads) {
-    const int r = i >> 4, u = i & 15, hh = u >> 3, uu = u & 7;
-    const int t = tok0 + r / G;
+  // Q tiles (A operands of QK): tile t row r = token tok0 + t*TQ + r / G, head
+  // g*G + r % G; 16-byte chunks into two 128-byte-swizzled halves.  Rows past
+  // the chunk are zero.
+  for (int i = tid; i < 2 * kPfRows * 16; i += kPfThreads) {
+    const int t = i / (kPfRows * 16), j = i % (kPfRows * 16);
+    const int r = j >> 4, u = j & 15, hh = u >> 3, uu = u & 7;
+    const int tk = tok0 + t * TQ + r / G;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TQ * G && t < n)
+    if (r < TQ * G && tk < n)
       v = *reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(q0 + t) * p.num_q_heads + g * G + r % G) * kPfD + 8 * u);
-    *reinterpret_cast<uint4*>(sm + LY::kQ + hh * LY::kQHalf + swz(r, uu)) = v;
+          p.q + (static_cast<int64_t>(q0 + tk) * p.num_q_heads + g * G + r % G) * kPfD + 8 * u);
+    *reinterpret_cast<uint4*>(sm + t * LY::kQ + hh * LY::kQHalf + swz(r, uu)) = v;
   }
   if (tid == 0) {
     for (int st = 0; st < STAGES; ++st) {
       mbar_init(smem_u32(&full[st]), 1);
       mbar_init(smem_u32(&empty[st]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&s_full[b]), 1);
-      mbar_init(smem_u32(&s_free[b]), 4);
-      mbar_init(smem_u32(&p_full[b]), 4);
-      mbar_init(smem_u32(&o_done[b]), 1);
+    for (int t = 0; t < 2; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_u32(&s_full[t][b]), 1);
+        mbar_init(smem_u32(&s_free[t][b]), 4);
+      }
+      mbar_init(smem_u32(&p_full[t]), 4);
+      mbar_init(smem_u32(&o_done[t]), 1);
     }
+    mbar_init(smem_u32(&drain), 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
                      smem_u32(&tmem_base_sh))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
@@ -188,10 +213,10 @@ __global__ void __launch_bounds__(kPfThreads)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tm = tmem_base_sh;   // S buffers at columns 0 / 64, O at 128
-  const uint32_t tmO = tm + 2 * kPfKeys;
+  // TMEM: tile t's S buffers at columns 256t + {0, 64}, its O at 256t + 128
+  const uint32_t tm = tmem_base_sh;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     // Lane i looks up box i's block (one round trip per tile, issued before the
     // wait for the stage), lane 0 publishes the tile's key mask next to the
@@ -243,70 +268,106 @@ __global__ void __launch_bounds__(kPfThreads)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------ MMA issuer --------------------------------
+    // Event-driven: each pass issues the next QK (key tiles in order, tile A
+    // then B) as soon as its stage has landed and its S buffer is free, and the
+    // next PV as soon as its P is written, so the S of the next key tiles is
+    // computed while the softmax warpgroups work.  A stage is released after
+    // the last PV that reads it.
     if (lane == 0) {
       const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, true);
       const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
-      int issued_qk = 0, issued_pv = 0;
-      for (int j = 0; j <= ntiles; ++j) {
-        if (j < ntiles) {
-          if (!tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
-          if (j >= 2 && !tc_wait(smem_u32(&s_free[j & 1]), ((j - 2) >> 1) & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
-          const uint32_t dst = tm + (j & 1) * kPfKeys;
-#pragma unroll
-          for (int ks = 0; ks < kPfD / 16; ++ks) {
-            const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
-            const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
-            tc_mma(dst, tc_desc(sma + LY::kQ + off_q, 0, 1024), tc_desc(kb + off_k, 0, 1024),
-                   idesc_qk, ks > 0);
+      int qj = 0, qt = 0;   // next QK: key tile qj, query tile qt
+      int pj = 0, pt = 0;   // next PV
+      auto active = [&](int j, int t) { return j < (t == 0 ? nt_a : nt_b); };
+      uint64_t idle_since = global_ns();
+      while (pj < ntiles) {
+        bool progressed = false;
+        if (qj < ntiles) {
+          if (!active(qj, qt)) {   // only tile B needs the late key tiles
+            if (++qt == 2) { qt = 0; ++qj; }
+            continue;
           }
-          tc_commit(smem_u32(&s_full[j & 1]));
-          ++issued_qk;
+          if (mbar_test(smem_u32(&full[qj % STAGES]), (qj / STAGES) & 1) &&
+              (qj < 2 || mbar_test(smem_u32(&s_free[qt][qj & 1]), ((qj - 2) >> 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kb = sma + LY::kStages + (qj % STAGES) * LY::kStage;
+            const uint32_t dst = tm + 256 * qt + (qj & 1) * kPfKeys;
+#pragma unroll
+            for (int ks = 0; ks < kPfD / 16; ++ks) {
+              const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
+              const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
+              tc_mma(dst, tc_desc(sma + qt * LY::kQ + off_q, 0, 1024),
+                     tc_desc(kb + off_k, 0, 1024), idesc_qk, ks > 0);
+            }
+            tc_commit(smem_u32(&s_full[qt][qj & 1]));
+            if (++qt == 2) { qt = 0; ++qj; }
+            progressed = true;
+          }
         }
-        if (j >= 1) {
-          const int jp = j - 1;
-          if (!tc_wait(smem_u32(&p_full[jp & 1]), (jp >> 1) & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t vb = sma + LY::kStages + (jp % STAGES) * LY::kStage + 2 * LY::kKVHalf;
-          const uint32_t pb = sma + LY::kP + (jp & 1) * LY::kPBuf;
-#pragma unroll
-          for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-            const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
-            tc_mma(tmO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (jp > 0 || kk > 0));
-            tc_mma(tmO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+        if (pj < qj || (pj == qj && pt < qt)) {   // its QK has been issued
+          if (!active(pj, pt)) {
+            if (++pt == 2) { pt = 0; ++pj; }
+            continue;
           }
-          tc_commit(smem_u32(&o_done[jp & 1]));
-          tc_commit(smem_u32(&empty[jp % STAGES]));
-          ++issued_pv;
+          if (mbar_test(smem_u32(&p_full[pt]), pj & 1)) {
+            tc_fence_after();
+            const uint32_t vb = sma + LY::kStages + (pj % STAGES) * LY::kStage + 2 * LY::kKVHalf;
+            const uint32_t pb = sma + LY::kP + pt * LY::kPBuf;
+            const uint32_t dO = tm + 256 * pt + 2 * kPfKeys;
+#pragma unroll
+            for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+              const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
+              tc_mma(dO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (pj > 0 || kk > 0));
+              tc_mma(dO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+            }
+            tc_commit(smem_u32(&o_done[pt]));
+            if (pt == 1 || !active(pj, 1)) {   // last reader of this stage
+              tc_commit(smem_u32(&empty[pj % STAGES]));
+              pt = 0;
+              ++pj;
+            } else {
+              pt = 1;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = global_ns();
+        } else if (*abort_flag) {
+          break;
+        } else if (global_ns() - idle_since > kWaitLimitNs) {
+          *abort_flag = 1;
+          break;
         }
       }
-      if (*abort_flag) {   // let issued tensor-core work finish before TMEM is released
-        volatile int no_abort = 0;
-        if (issued_pv > 0)
-          tc_wait(smem_u32(&o_done[(issued_pv - 1) & 1]), ((issued_pv - 1) >> 1) & 1, &no_abort);
-        if (issued_qk > 0)
-          tc_wait(smem_u32(&s_full[(issued_qk - 1) & 1]), ((issued_qk - 1) >> 1) & 1, &no_abort);
-      }
+      // every issued MMA completes before TMEM can be released
+      tc_commit(smem_u32(&drain));
+      volatile int no_abort = 0;
+      tc_wait(smem_u32(&drain), 0, &no_abort);
     }
   } else {
-    // ------------------------- softmax warps 0-3 ------------------------------
-    const int r = tid;                                  // accumulator row = TMEM lane
-    const uint32_t lane_q = static_cast<uint32_t>(warp * 32) << 16;
+    // -------------------- softmax warpgroups (A: 0-3, B: 4-7) -----------------
+    const int t = warp >> 2;                            // query tile of this warpgroup
+    const int r = tid & 127;                            // accumulator row = TMEM lane
+    const int my_nt = t == 0 ? nt_a : nt_b;
+    const uint32_t lane_q = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tm + 256 * t, tO = tm + 256 * t + 2 * kPfKeys;
     const int tl = r / G;
-    const bool row_ok = r < TQ * G && tok0 + tl < n;
-    const int qpos = ctx - n + tok0 + tl;               // this row's position
+    const bool row_ok = r < TQ * G && tok0 + t * TQ + tl < n;
+    const int qpos = ctx - n + tok0 + t * TQ + tl;      // this row's position
     const int last = p.causal ? qpos : ctx - 1;         // last key it sees
     const float sl2 = p.qk_scale_log2;
-    float m = -CUDART_INF_F, l = 0.f;
+    const bool pos_scale = sl2 > 0.f;
+    uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
+    float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units
     bool alive = true;
-    for (int j = 0; j < ntiles && alive; ++j) {
+    for (int j = 0; j < my_nt && alive; ++j) {
       const int k0 = j * kPfKeys;
       // S(j) ready implies the stage's copies landed; waiting on the stage's
       // barrier as well makes the producer's key mask for it visible here.
-      if (!tc_wait(smem_u32(&s_full[j & 1]), (j >> 1) & 1, abort_flag) ||
+      if (!tc_wait(smem_u32(&s_full[t][j & 1]), (j >> 1) & 1, abort_flag) ||
           !tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag))
         alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
@@ -315,30 +376,30 @@ __global__ void __launch_bounds__(kPfThreads)
       const int lim = last - k0 + 1;
       uint64_t rmask = lim >= kPfKeys ? ~0ull : (lim <= 0 ? 0ull : ((1ull << lim) - 1ull));
       rmask = row_ok ? (rmask & vmask) : 0ull;
-      const bool dense = __all_sync(0xffffffffu, rmask == ~0ull);
+      const bool dense = pos_scale && __all_sync(0xffffffffu, rmask == ~0ull);
       tc_fence_after();
       float sv[kPfKeys];
-      pf_ld64(tm + lane_q + (j & 1) * kPfKeys, sv);
+      pf_ld64(tS + lane_q + (j & 1) * kPfKeys, sv);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
-      float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-      if (dense) {   // warp-uniform: no key of the tile is masked for any row
+      if ((lane & 31) == 0) mbar_arrive(smem_u32(&s_free[t][j & 1]));
+      float mt;
+      if (dense) {   // warp-uniform: nothing masked; max of the raw logits, then scale
+        float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-          sv[c] *= sl2;
-          mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
-        }
+        for (int c = 4; c < kPfKeys; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+        mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       } else {
         const uint32_t mlo = static_cast<uint32_t>(rmask), mhi = static_cast<uint32_t>(rmask >> 32);
+        float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
         for (int c = 0; c < kPfKeys; ++c) {
           const bool ok = ((c < 32 ? mlo : mhi) >> (c & 31)) & 1u;
           sv[c] = ok ? sv[c] * sl2 : -CUDART_INF_F;
           mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
         }
+        mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       }
-      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       float alpha = 1.f;
       bool resc = false;
       if (mt > m + 8.f) {
@@ -350,31 +411,23 @@ __global__ void __launch_bounds__(kPfThreads)
       }
       const float mu = m == -CUDART_INF_F ? 0.f : m;   // rows with nothing seen yet: p = 0
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      if (dense) {
 #pragma unroll
-      for (int c = 0; c < kPfKeys; ++c) {
-        sv[c] = pf_ex2(sv[c] - mu);   // 2^-inf = 0 for masked keys
-        ls4[c & 3] += sv[c];
-      }
-      l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-      if (__any_sync(0xffffffffu, resc)) {   // PV(j-1) must be in O before scaling it
-        if (!tc_wait(smem_u32(&o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag))
-          alive = false;
-        if (!__all_sync(0xffffffffu, alive)) break;
-        tc_fence_after();
+        for (int c = 0; c < kPfKeys; ++c) {
+          sv[c] = pf_ex2(fmaf(sv[c], sl2, -mu));
+          ls4[c & 3] += sv[c];
+        }
+      } else {
 #pragma unroll
-        for (int c = 0; c < kPfD; c += 32) {
-          float o[32];
-          tc_ld32(tmO + lane_q + c, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc_st32(tmO + lane_q + c, o);
+        for (int c = 0; c < kPfKeys; ++c) {
+          sv[c] = pf_ex2(sv[c] - mu);   // 2^-inf = 0 for masked keys
+          ls4[c & 3] += sv[c];
         }
       }
-      // P buffer j%2 is free once PV(j-2) is done
-      if (j >= 2 && !tc_wait(smem_u32(&o_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag))
-        alive = false;
+      l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+      // PV(j-1) must be finished before P is overwritten and before O is scaled
+      if (j >= 1 && !tc_wait(smem_u32(&o_done[t]), (j - 1) & 1, abort_flag)) alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
-      uint8_t* pb = sm + LY::kP + (j & 1) * LY::kPBuf;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
@@ -389,7 +442,21 @@ __global__ void __launch_bounds__(kPfThreads)
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
             make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
-      if (r < kPfKeys && !((vmask >> r) & 1ull)) {   // V rows without cache data -> 0
+      if (__any_sync(0xffffffffu, resc)) {   // after P is out of the registers
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kPfD; c += 32) {
+          float o[32];
+          tc_ld32(tO + lane_q + c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc_st32(tO + lane_q + c, o);
+        }
+      }
+      // V rows without cache data -> 0, once per key tile: by tile A's group
+      // while it still needs this tile, else by tile B's
+      const bool zeroer = (t == 0) == (j < nt_a);
+      if (zeroer && r < kPfKeys && !((vmask >> r) & 1ull)) {
         uint8_t* vrow = sm + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -400,20 +467,20 @@ __global__ void __launch_bounds__(kPfThreads)
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
     // epilogue: this warp's O rows / l
-    bool ok = alive && tc_wait(smem_u32(&o_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1,
-                               abort_flag);
+    const bool ok = alive && my_nt > 0 &&
+                    tc_wait(smem_u32(&o_done[t]), (my_nt - 1) & 1, abort_flag);
     if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + tl) * p.num_q_heads + g * G + r % G) *
-                                kPfD;
+      float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads +
+                             g * G + r % G) * kPfD;
 #pragma unroll
       for (int c = 0; c < kPfD; c += 32) {
         float o[32];
-        tc_ld32(tmO + lane_q + c, o);
+        tc_ld32(tO + lane_q + c, o);
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
@@ -426,7 +493,7 @@ __global__ void __launch_bounds__(kPfThreads)
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tm) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tm) : "memory");
   if (tid == 0 && *abort_flag) flag_status(p.status, PKV_DEV_TIMEOUT);
 }
 
