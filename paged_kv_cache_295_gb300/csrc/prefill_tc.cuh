@@ -24,9 +24,10 @@
 // buffers and O in 128 columns (512 columns in all).  Warp roles: warps 0-3
 // softmax of tile A, warps 4-7 softmax of tile B (warp w owns TMEM lanes
 // 32(w%4)..+31, i.e. rows), warp 8 TMA producer (lanes look up one key tile's
-// blocks in one round trip and issue its boxes), warp 9 MMA issuer (event-
-// driven: whichever QK or PV is ready next, so QK runs ahead).  The two
-// softmax warpgroups work on the same key tile at once, so each SM sub-
+// blocks in one round trip and issue its boxes), warp 9 issues the QK MMAs
+// and warp 10 the PV MMAs: a single thread issues one tcgen05.mma about every
+// 125 cycles, so two issuing threads double the MMA rate and let QK run ahead
+// of PV.  The two softmax warpgroups work on the same key tile at once, so each SM sub-
 // partition has two softmax warps to interleave.  Tile A needs no key past
 // its last token: its MMAs and softmax stop there.  The running max moves only
 // when a tile's row max exceeds it by more than 2^8, so O is rarely rescaled.
@@ -41,7 +42,7 @@ namespace pkv {
 constexpr int kPfRows = 128;   // accumulator rows per query tile (M)
 constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
 constexpr int kPfD = 128;
-constexpr int kPfThreads = 320;   // 2 softmax warpgroups, producer warp, MMA warp
+constexpr int kPfThreads = 352;   // 2 softmax warpgroups, producer, QK issuer, PV issuer
 constexpr int kPfStages = 3;
 
 struct PrefillParams {
@@ -109,18 +110,6 @@ struct PfLayout {
   }
 };
 
-// Non-blocking check of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 template <int STAGES>
 __global__ void __launch_bounds__(kPfThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -131,7 +120,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
-  __shared__ __align__(8) uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], drain;
+  __shared__ __align__(8) uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], drain[2];
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -199,7 +188,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(smem_u32(&p_full[t]), 4);
       mbar_init(smem_u32(&o_done[t]), 1);
     }
-    mbar_init(smem_u32(&drain), 1);
+    mbar_init(smem_u32(&drain[0]), 1);
+    mbar_init(smem_u32(&drain[1]), 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -269,83 +259,72 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ------------------------------ MMA issuer --------------------------------
-    // Event-driven: each pass issues the next QK (key tiles in order, tile A
-    // then B) as soon as its stage has landed and its S buffer is free, and the
-    // next PV as soon as its P is written, so the S of the next key tiles is
-    // computed while the softmax warpgroups work.  A stage is released after
-    // the last PV that reads it.
+    // ---------------------------- QK issuer ------------------------------------
+    // Key tiles in order, tile A then B: once the stage has landed and the S
+    // buffer is free.  Its commits cover only its own MMAs (s_full).
     if (lane == 0) {
       const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, true);
-      const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
-      int qj = 0, qt = 0;   // next QK: key tile qj, query tile qt
-      int pj = 0, pt = 0;   // next PV
-      auto active = [&](int j, int t) { return j < (t == 0 ? nt_a : nt_b); };
-      uint64_t idle_since = global_ns();
-      while (pj < ntiles) {
-        bool progressed = false;
-        if (qj < ntiles) {
-          if (!active(qj, qt)) {   // only tile B needs the late key tiles
-            if (++qt == 2) { qt = 0; ++qj; }
-            continue;
+      for (int j = 0; j < ntiles; ++j) {
+        if (!tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
+        const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
+        bool ok = true;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= (t == 0 ? nt_a : nt_b)) continue;
+          if (j >= 2 && !tc_wait(smem_u32(&s_free[t][j & 1]), ((j - 2) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (mbar_test(smem_u32(&full[qj % STAGES]), (qj / STAGES) & 1) &&
-              (qj < 2 || mbar_test(smem_u32(&s_free[qt][qj & 1]), ((qj - 2) >> 1) & 1))) {
-            tc_fence_after();
-            const uint32_t kb = sma + LY::kStages + (qj % STAGES) * LY::kStage;
-            const uint32_t dst = tm + 256 * qt + (qj & 1) * kPfKeys;
+          tc_fence_after();
+          const uint32_t dst = tm + 256 * t + (j & 1) * kPfKeys;
+          const uint32_t qa = sma + t * LY::kQ;
 #pragma unroll
-            for (int ks = 0; ks < kPfD / 16; ++ks) {
-              const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
-              const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
-              tc_mma(dst, tc_desc(sma + qt * LY::kQ + off_q, 0, 1024),
-                     tc_desc(kb + off_k, 0, 1024), idesc_qk, ks > 0);
-            }
-            tc_commit(smem_u32(&s_full[qt][qj & 1]));
-            if (++qt == 2) { qt = 0; ++qj; }
-            progressed = true;
+          for (int ks = 0; ks < kPfD / 16; ++ks) {
+            const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
+            const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
+            tc_mma(dst, tc_desc(qa + off_q, 0, 1024), tc_desc(kb + off_k, 0, 1024), idesc_qk,
+                   ks > 0);
           }
+          tc_commit(smem_u32(&s_full[t][j & 1]));
         }
-        if (pj < qj || (pj == qj && pt < qt)) {   // its QK has been issued
-          if (!active(pj, pt)) {
-            if (++pt == 2) { pt = 0; ++pj; }
-            continue;
-          }
-          if (mbar_test(smem_u32(&p_full[pt]), pj & 1)) {
-            tc_fence_after();
-            const uint32_t vb = sma + LY::kStages + (pj % STAGES) * LY::kStage + 2 * LY::kKVHalf;
-            const uint32_t pb = sma + LY::kP + pt * LY::kPBuf;
-            const uint32_t dO = tm + 256 * pt + 2 * kPfKeys;
-#pragma unroll
-            for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-              const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
-              tc_mma(dO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (pj > 0 || kk > 0));
-              tc_mma(dO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
-            }
-            tc_commit(smem_u32(&o_done[pt]));
-            if (pt == 1 || !active(pj, 1)) {   // last reader of this stage
-              tc_commit(smem_u32(&empty[pj % STAGES]));
-              pt = 0;
-              ++pj;
-            } else {
-              pt = 1;
-            }
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          idle_since = global_ns();
-        } else if (*abort_flag) {
-          break;
-        } else if (global_ns() - idle_since > kWaitLimitNs) {
-          *abort_flag = 1;
-          break;
-        }
+        if (!ok) break;
       }
-      // every issued MMA completes before TMEM can be released
-      tc_commit(smem_u32(&drain));
+      tc_commit(smem_u32(&drain[0]));   // its MMAs finish before TMEM is released
       volatile int no_abort = 0;
-      tc_wait(smem_u32(&drain), 0, &no_abort);
+      tc_wait(smem_u32(&drain[0]), 0, &no_abort);
+    }
+  } else if (warp == 10) {
+    // ---------------------------- PV issuer ------------------------------------
+    // Tile A then B of each key tile, once its P is written; after the last PV
+    // that reads a stage, the stage is released (its QK finished before its P
+    // could be written).
+    if (lane == 0) {
+      const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
+      for (int j = 0; j < ntiles; ++j) {
+        const uint32_t vb = sma + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf;
+        bool ok = true;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= (t == 0 ? nt_a : nt_b)) continue;
+          if (!tc_wait(smem_u32(&p_full[t]), j & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pb = sma + LY::kP + t * LY::kPBuf;
+          const uint32_t dO = tm + 256 * t + 2 * kPfKeys;
+#pragma unroll
+          for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+            const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
+            tc_mma(dO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (j > 0 || kk > 0));
+            tc_mma(dO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+          }
+          tc_commit(smem_u32(&o_done[t]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&empty[j % STAGES]));
+      }
+      tc_commit(smem_u32(&drain[1]));
+      volatile int no_abort = 0;
+      tc_wait(smem_u32(&drain[1]), 0, &no_abort);
     }
   } else {
     // -------------------- softmax warpgroups (A: 0-3, B: 4-7) -----------------
