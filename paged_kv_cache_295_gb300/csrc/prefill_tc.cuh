@@ -23,8 +23,9 @@
 // for t = A (the earlier tokens) and B.  TMEM: per tile, S in two 64-column
 // buffers and O in 128 columns (512 columns in all).  Warp roles: warps 0-3
 // softmax of tile A, warps 4-7 softmax of tile B (warp w owns TMEM lanes
-// 32(w%4)..+31, i.e. rows), warp 8 TMA producer (lanes look up one key tile's
-// blocks in one round trip and issue its boxes), warp 9 issues the QK MMAs
+// 32(w%4)..+31, i.e. rows), warps 8 and 11 TMA producers of K and V (lanes
+// look up one key tile's blocks in one round trip and issue its boxes, one
+// 64-column half each), warp 9 issues the QK MMAs
 // and warp 10 the PV MMAs: a single thread issues one tcgen05.mma about every
 // 125 cycles, so two issuing threads double the MMA rate and let QK run ahead
 // of PV.  The two softmax warpgroups work on the same key tile at once, so each SM sub-
@@ -42,7 +43,8 @@ namespace pkv {
 constexpr int kPfRows = 128;   // accumulator rows per query tile (M)
 constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
 constexpr int kPfD = 128;
-constexpr int kPfThreads = 352;   // 2 softmax warpgroups, producer, QK issuer, PV issuer
+constexpr int kPfThreads = 384;   // 2 softmax warpgroups, K producer, QK issuer, PV issuer,
+                                  // V producer
 constexpr int kPfStages = 3;
 
 struct PrefillParams {
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int TQ = p.tile_tokens;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES];
+  __shared__ __align__(8) uint64_t full[STAGES], full_v[STAGES], empty[STAGES];
   __shared__ __align__(8) uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], drain[2];
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   if (tid == 0) {
     for (int st = 0; st < STAGES; ++st) {
-      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&full[st]), 1);     // K copies and the key mask
+      mbar_init(smem_u32(&full_v[st]), 1);   // V copies
       mbar_init(smem_u32(&empty[st]), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -206,26 +209,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // TMEM: tile t's S buffers at columns 256t + {0, 64}, its O at 256t + 128
   const uint32_t tm = tmem_base_sh;
 
-  if (warp == 8) {
-    // ------------------------------ TMA producer ------------------------------
-    // Lane i looks up box i's block (one round trip per tile, issued before the
-    // wait for the stage), lane 0 publishes the tile's key mask next to the
-    // stage and arms its barrier, and each lane with a real block issues its
-    // box's four copies (K and V, two 64-column halves).
+  if (warp == 8 || warp == 11) {
+    // --------------------- TMA producers: warp 8 K, warp 11 V -------------------
+    // Per key tile, lane 2i + h looks up box i's block (one round trip, issued
+    // before the wait for the stage) and copies its 64-column half h, so one
+    // instruction issues the tile's boxes of this producer's tensor.  Warp 8's
+    // lane 0 publishes the tile's key mask next to the stage; each producer
+    // arms its own barrier (full_k / full_v) with its bytes.
+    const bool is_v = warp == 11;
     const int box_rows = p.box_rows;
     const int nbox = kPfKeys / box_rows;
+    const int bx = lane >> 1, hh = lane & 1;
     bool flagged = false;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % STAGES;
       const int k0 = j * kPfKeys;
-      const int kb = k0 + lane * box_rows;
+      const int kb = k0 + bx * box_rows;
       int32_t blk = -1;
-      if (lane < nbox && kb < ctx) {
+      if (bx < nbox && kb < ctx) {
         const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
         blk = (b >= 0 && b < p.num_blocks) ? b : -2;
       }
-      const uint32_t valid = __ballot_sync(0xffffffffu, blk >= 0);
-      if (__ballot_sync(0xffffffffu, blk == -2) && !flagged) {
+      const uint32_t valid = __ballot_sync(0xffffffffu, blk >= 0 && hh == 0);   // bit 2i: box i
+      if (!is_v && __ballot_sync(0xffffffffu, blk == -2) && !flagged) {
         if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
         flagged = true;
       }
@@ -234,28 +240,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      const uint32_t bar = smem_u32(&full[st]);
+      const uint32_t bar = smem_u32(is_v ? &full_v[st] : &full[st]);
       if (lane == 0) {
-        uint64_t m = 0;
-        for (int bx = 0; bx < nbox; ++bx) {
-          if (!((valid >> bx) & 1u)) continue;
-          const int rows = min(box_rows, ctx - (k0 + bx * box_rows));
-          const uint64_t run = rows >= 64 ? ~0ull : ((1ull << rows) - 1ull);
-          m |= run << (bx * box_rows);
+        if (!is_v) {
+          uint64_t m = 0;
+          for (int i = 0; i < nbox; ++i) {
+            if (!((valid >> (2 * i)) & 1u)) continue;
+            const int rows = min(box_rows, ctx - (k0 + i * box_rows));
+            const uint64_t run = rows >= 64 ? ~0ull : ((1ull << rows) - 1ull);
+            m |= run << (i * box_rows);
+          }
+          key_mask[st] = m;
         }
-        key_mask[st] = m;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(valid)) * 4u * box_rows * 128u);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(valid)) * 2u * box_rows * 128u);
       }
       __syncwarp();
       if (blk >= 0) {
-        const uint32_t sbase = sma + LY::kStages + st * LY::kStage + lane * box_rows * 128;
+        const uint32_t dst = sma + LY::kStages + st * LY::kStage + (is_v ? 2 * LY::kKVHalf : 0) +
+                             hh * LY::kKVHalf + bx * box_rows * 128;
         const int z = (blk << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {   // (K/V, half)
-          const int kv = k >> 1, hh = k & 1;
-          tma_load_3d(sbase + kv * 2 * LY::kKVHalf + hh * LY::kKVHalf, kv ? &tmap_v : &tmap_k,
-                      hh * 64, g, z, bar);
-        }
+        tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, hh * 64, g, z, bar);
       }
     }
   } else if (warp == 9) {
@@ -276,13 +280,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_fence_after();
           const uint32_t dst = tm + 256 * t + (j & 1) * kPfKeys;
-          const uint32_t qa = sma + t * LY::kQ;
+          // descriptors built once; a k-step only moves the start address
+          // (bits 0-13, in 16-byte units)
+          const uint64_t qd = tc_desc(sma + t * LY::kQ, 0, 1024);
+          const uint64_t kd = tc_desc(kb, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < kPfD / 16; ++ks) {
             const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
             const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
-            tc_mma(dst, tc_desc(qa + off_q, 0, 1024), tc_desc(kb + off_k, 0, 1024), idesc_qk,
-                   ks > 0);
+            tc_mma(dst, qd + (off_q >> 4), kd + (off_k >> 4), idesc_qk, ks > 0);
           }
           tc_commit(smem_u32(&s_full[t][j & 1]));
         }
@@ -301,6 +307,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
       for (int j = 0; j < ntiles; ++j) {
         const uint32_t vb = sma + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf;
+        if (!tc_wait(smem_u32(&full_v[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
         bool ok = true;
         for (int t = 0; t < 2; ++t) {
           if (j >= (t == 0 ? nt_a : nt_b)) continue;
@@ -309,13 +316,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t pb = sma + LY::kP + t * LY::kPBuf;
           const uint32_t dO = tm + 256 * t + 2 * kPfKeys;
+          const uint64_t pd = tc_desc(sma + LY::kP + t * LY::kPBuf, 0, 1024);
+          const uint64_t vd = tc_desc(vb, LY::kKVHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-            const uint64_t bdesc = tc_desc(vb + kk * 2048, LY::kKVHalf, 1024);
-            tc_mma(dO, tc_desc(pb + kk * 32, 0, 1024), bdesc, idesc_pv, (j > 0 || kk > 0));
-            tc_mma(dO, tc_desc(pb + LY::kPPart + kk * 32, 0, 1024), bdesc, idesc_pv, 1);
+            const uint64_t bdesc = vd + ((kk * 2048) >> 4);
+            tc_mma(dO, pd + ((kk * 32) >> 4), bdesc, idesc_pv, (j > 0 || kk > 0));
+            tc_mma(dO, pd + ((LY::kPPart + kk * 32) >> 4), bdesc, idesc_pv, 1);
           }
           tc_commit(smem_u32(&o_done[t]));
         }
@@ -433,9 +441,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       // V rows without cache data -> 0, once per key tile: by tile A's group
-      // while it still needs this tile, else by tile B's
+      // while it still needs this tile, else by tile B's; after the V copies
+      // landed (a partly valid box also brings rows past the context)
       const bool zeroer = (t == 0) == (j < nt_a);
-      if (zeroer && r < kPfKeys && !((vmask >> r) & 1ull)) {
+      if (zeroer && vmask != ~0ull &&
+          !tc_wait(smem_u32(&full_v[j % STAGES]), (j / STAGES) & 1, abort_flag))
+        alive = false;
+      if (zeroer && alive && r < kPfKeys && !((vmask >> r) & 1ull)) {
         uint8_t* vrow = sm + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
