@@ -65,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--num-layers", type=int, default=0,
+                    help="override the workload's layer count (small profiling captures)")
     ap.add_argument("--partition", type=int, default=0, help="split-KV tokens (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=0, help="e2e steps (0 = min(steps, 200))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -73,6 +75,15 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
+
+
+def workload_of(args):
+    """The selected workload, with --num-layers applied when given."""
+    import dataclasses
+    w = WORKLOADS[args.workload]
+    if getattr(args, "num_layers", 0) and hasattr(w, "num_layers"):
+        w = dataclasses.replace(w, num_layers=args.num_layers)
+    return w
 
 
 def kernel_sources_sha() -> str:
@@ -368,7 +379,7 @@ def run_ours(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -689,7 +700,7 @@ def run_prefill(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -780,7 +791,7 @@ def run_prefill_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     st = OraclePrefillStep(w)
     for i in range(Wm):
@@ -882,7 +893,7 @@ def run_fork(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -964,7 +975,7 @@ def run_fork_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     nb = 2 * w.beams
     pool = W.store(W.rng(w.seed, 900).standard_normal(
@@ -1071,7 +1082,7 @@ def run_swap(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -1141,7 +1152,7 @@ def run_swap_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     lens = W.swap_lens(w)
     n = int(lens[0])
@@ -1273,7 +1284,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     K, Wm = args.steps, args.warmup
     order = [i % w.num_seqs for i in range(Wm + K)]
     st = OracleStep(w, sorted(set(order)))
@@ -1301,7 +1312,7 @@ def run_reference(args):
 
 def cpu_baseline(args):
     """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     prefill = isinstance(w, W.PrefillWorkload)
     if isinstance(w, (W.ForkWorkload, W.SwapWorkload)):
         steps = 100
@@ -1338,7 +1349,7 @@ def _cpu_model():
 
 def main(argv=None):
     args = parse_args(argv)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     if isinstance(w, W.PrefillWorkload):
         arms = (run_prefill_reference, run_prefill)
     elif isinstance(w, W.ForkWorkload):
