@@ -560,11 +560,34 @@ def run_e2e(st, args, dev, world):
         one(i)
     dt = max_over_ranks(time.perf_counter() - t, world, dev)
     kv = sum_over_ranks(kv_bytes_logical(w, st.lens) * L * n, world, dev)
-    return {"value": round(kv / dt / 1e9, 2), "unit": "GB/s", "steps": n,
-            "ms_per_step": round(dt / n * 1e3, 5),
-            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-            "decode_tokens_per_s": round(world * S * n / dt, 1),
-            "timer": "host wall clock, one stream sync per step"}
+    eager = {"value": round(kv / dt / 1e9, 2), "ms_per_step": round(dt / n * 1e3, 5),
+             "calls": "per step: pool tables, torch copies, reshape_and_cache and "
+                      "paged_attention_decode per layer, D2H, sync"}
+
+    # the same step as one public call: decode_graph_step_host on a captured graph
+    import paged_kv_cache_295_gb300 as pkv
+    g = pkv.DecodeGraph(st.eng, w.num_q_heads, mb, [S], device_status=st.status)
+    qg = torch.stack([q_h[l][0] for l in range(L)]).pin_memory()
+    kg = torch.stack([kn_h[l][0] for l in range(L)]).pin_memory()
+    vg = torch.stack([vn_h[l][0] for l in range(L)]).pin_memory()
+    outg = torch.empty((L, S, w.num_q_heads, w.head_dim), dtype=torch.float32, pin_memory=True)
+    for _ in range(3):
+        g.step_host(st.eng.pool, seqs, qg, kg, vg, slots_h, outg, stream=stream)
+    barrier(world)
+    t = time.perf_counter()
+    for _ in range(n):
+        g.step_host(st.eng.pool, seqs, qg, kg, vg, slots_h, outg, stream=stream)
+    dtg = max_over_ranks(time.perf_counter() - t, world, dev)
+    g.close()
+    bo_g = outg.numel() * 4
+    return {"value": round(kv / dtg / 1e9, 2), "unit": "GB/s", "steps": n,
+            "ms_per_step": round(dtg / n * 1e3, 5),
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo_g),
+            "decode_tokens_per_s": round(world * S * n / dtg, 1),
+            "call": "decode_graph_step_host: pool tables -> pinned staging, one copy per "
+                    "input buffer, graph replay of every layer's append + decode, output "
+                    "copy, one stream sync",
+            "timer": "host wall clock around each call", "eager": eager}
 
 
 # ---------------------------------------------------------- prefill arm ---

@@ -32,7 +32,9 @@
  *     pointers.
  *   - A pool handle is not thread-safe: the caller serialises calls on it.
  *   - decode_graph_create is the one device-side call that allocates (graph
- *     objects and a private stream) and synchronises; it is a set-up call.
+ *     objects, a private stream, a page-locked staging area) and synchronises;
+ *     it is a set-up call.  decode_graph_step_host synchronises by design: it
+ *     returns with the step's output in host memory.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -461,6 +463,29 @@ pkv_status decode_graph_create(const pkv_decode_graph_config* cfg, pkv_decode_gr
 pkv_status decode_graph_launch(pkv_decode_graph* g, int32_t batch, int32_t* bucket_out,
                                pkv_stream_t stream);
 void decode_graph_destroy(pkv_decode_graph* g);
+/* One decode step from host memory: the whole step a caller makes per token.
+ * Builds the batch's block tables and lengths from the pool into a
+ * page-locked staging area the graph owns, copies them and the step's inputs
+ * to the graph's buffers (one cudaMemcpyAsync or cudaMemcpy2DAsync per
+ * buffer), replays the bucket's graph, copies the output back and waits for
+ * the stream.
+ *   seq_ids   : host [batch] int64, resident sequences whose tables fit
+ *               max_blocks_per_seq.
+ *   q_host    : host [num_layers][batch][num_q_heads][head_dim], q_dtype.
+ *   k_new_host, v_new_host : host [num_layers][batch][num_kv_heads][head_dim],
+ *               src_dtype.
+ *   slots_host: host [batch] int64, the slots of the step's tokens
+ *               (seq_append_slots; the pool's lengths already include them).
+ *   out_host  : host [num_layers][batch][num_q_heads][head_dim] float32.
+ * Page-locked host buffers make the copies asynchronous; pageable ones work
+ * but are staged by the driver.  Returns INVALID_ARG for a bad batch, an
+ * unknown or swapped-out sequence or a table longer than max_blocks_per_seq,
+ * CUDA if a copy or the launch fails. */
+pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool* pool,
+                                  const int64_t* seq_ids, int32_t batch, const void* q_host,
+                                  const void* k_new_host, const void* v_new_host,
+                                  const int64_t* slots_host, float* out_host,
+                                  pkv_stream_t stream);
 
 /* Size of the device scratch compiled into the library for
  * paged_attention_decode_noalloc (held on every GPU that loads the library,

@@ -99,6 +99,7 @@ _SIGS = {
     "decode_graph_create": (I32, [C.POINTER(_GraphConfig), C.POINTER(P)]),
     "decode_graph_launch": (I32, [P, I32, C.POINTER(I32), P]),
     "decode_graph_destroy": (None, [P]),
+    "decode_graph_step_host": (I32, [P, P, P, I32, P, P, P, P, P, P]),
     "reshape_and_cache": (I32, [P, P, P, P, P, I32, I32, I32, I32, I64, I32, I32, P, P, P, P]),
     "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32]),
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
@@ -545,6 +546,23 @@ class DecodeGraph:
         _check(library().decode_graph_launch(self._h, int(batch), C.byref(b), _stream(stream)),
                "decode_graph_launch")
         return b.value
+
+    def step_host(self, pool, seq_ids, q_host, k_new_host, v_new_host, slots_host, out_host,
+                  stream=None):
+        """The whole step from host memory (``decode_graph_step_host``): tables
+        from ``pool``, host inputs ``q [L, B, Hq, D]``, ``k/v [L, B, Hkv, D]``,
+        ``slots [B]`` copied in, the replay, ``out [L, B, Hq, D]`` copied back.
+        Host tensors should be pinned; returns when the output is in host memory."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        for t, name in ((q_host, "q"), (k_new_host, "k_new"), (v_new_host, "v_new"),
+                        (slots_host, "slots"), (out_host, "out")):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        st = library().decode_graph_step_host(
+            self._h, pool._h, _np_ptr(ids), ids.size, C.c_void_p(q_host.data_ptr()),
+            C.c_void_p(k_new_host.data_ptr()), C.c_void_p(v_new_host.data_ptr()),
+            C.c_void_p(slots_host.data_ptr()), C.c_void_p(out_host.data_ptr()), _stream(stream))
+        _check(st, "decode_graph_step_host")
 
     def close(self):
         if getattr(self, "_h", None):

@@ -6,7 +6,10 @@
 // K/V rows and the decode attention (with its split-KV reduce), captured from
 // the library's own entry points on a private stream.  A launch pads the rows
 // between the batch and the bucket (context 0, slot -1) with one small kernel
-// and replays the bucket's graph on the caller's stream.
+// and replays the bucket's graph on the caller's stream.  decode_graph_step_host
+// wraps a launch into the per-token call a serving loop makes from host
+// memory: block tables straight from the pool into page-locked staging, one
+// copy per input buffer, the replay, the output copied back, one stream sync.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -22,6 +25,7 @@ struct pkv_decode_graph {
   std::vector<int32_t> buckets;
   std::vector<cudaGraphExec_t> execs;
   int device = 0;
+  int32_t* host_meta = nullptr;   // page-locked [Bmax][max_blocks] tables, then [Bmax] lengths
 };
 
 namespace pkv {
@@ -75,6 +79,7 @@ void release(pkv_decode_graph* g) {
   if (!g) return;
   for (cudaGraphExec_t e : g->execs)
     if (e) cudaGraphExecDestroy(e);
+  if (g->host_meta) cudaFreeHost(g->host_meta);
   delete g;
 }
 
@@ -101,13 +106,10 @@ extern "C" pkv_status decode_graph_create(const pkv_decode_graph_config* cfg,
   const int64_t max_ctx = static_cast<int64_t>(c.max_blocks_per_seq) * c.block_size;
   if (max_ctx > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
   const int32_t Bmax = c.buckets[c.num_buckets - 1];
-  const size_t need = paged_attention_workspace_bytes(Bmax, c.num_q_heads, c.num_kv_heads,
-                                                      c.head_dim, static_cast<int32_t>(max_ctx), 0);
   for (int32_t i = 0; i < c.num_buckets; ++i)   // every bucket's partials fit the workspace
     if (paged_attention_workspace_bytes(c.buckets[i], c.num_q_heads, c.num_kv_heads, c.head_dim,
                                         static_cast<int32_t>(max_ctx), 0) > c.workspace_bytes)
       return PKV_ERR_INVALID_ARG;
-  (void)need;
 
   pkv_decode_graph* g = new (std::nothrow) pkv_decode_graph();
   if (!g) return PKV_ERR_HOST_MEMORY;
@@ -131,6 +133,14 @@ extern "C" pkv_status decode_graph_create(const pkv_decode_graph_config* cfg,
   g->cfg.v_scales = nullptr;
   g->cfg.buckets = nullptr;
   cudaGetDevice(&g->device);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&g->host_meta),
+                    static_cast<size_t>(Bmax) * (c.max_blocks_per_seq + 1) * sizeof(int32_t),
+                    cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    g->host_meta = nullptr;
+    release(g);
+    return PKV_ERR_CUDA;
+  }
 
   cudaStream_t st = nullptr;
   if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
@@ -192,3 +202,52 @@ extern "C" pkv_status decode_graph_launch(pkv_decode_graph* g, int32_t batch, in
 }
 
 extern "C" void decode_graph_destroy(pkv_decode_graph* g) { pkv::release(g); }
+
+extern "C" pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool* pool,
+                                             const int64_t* seq_ids, int32_t batch,
+                                             const void* q_host, const void* k_new_host,
+                                             const void* v_new_host, const int64_t* slots_host,
+                                             float* out_host, pkv_stream_t stream) {
+  using namespace pkv;
+  if (!g || !pool || !seq_ids || !q_host || !k_new_host || !v_new_host || !slots_host ||
+      !out_host || batch <= 0 || batch > g->buckets.back())
+    return PKV_ERR_INVALID_ARG;
+  const pkv_decode_graph_config& c = g->cfg;
+  const int32_t Bmax = g->buckets.back(), mb = c.max_blocks_per_seq;
+  int32_t* tables = g->host_meta;
+  int32_t* lens = g->host_meta + static_cast<size_t>(Bmax) * mb;
+  pkv_status s = seq_batch_tables(pool, seq_ids, batch, mb, tables, lens);
+  if (s != PKV_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t qrow = static_cast<size_t>(c.num_q_heads) * c.head_dim * elem_bytes(c.q_dtype);
+  const size_t kvrow = static_cast<size_t>(c.num_kv_heads) * c.head_dim * elem_bytes(c.src_dtype);
+  const size_t orow = static_cast<size_t>(c.num_q_heads) * c.head_dim * sizeof(float);
+  const size_t L = static_cast<size_t>(c.num_layers);
+  bool ok =
+      cudaMemcpyAsync(c.block_tables, tables, static_cast<size_t>(batch) * mb * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, st) == cudaSuccess &&
+      cudaMemcpyAsync(c.context_lens, lens, static_cast<size_t>(batch) * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, st) == cudaSuccess &&
+      cudaMemcpyAsync(c.slot_mapping, slots_host, static_cast<size_t>(batch) * sizeof(int64_t),
+                      cudaMemcpyHostToDevice, st) == cudaSuccess &&
+      cudaMemcpy2DAsync(c.q, Bmax * qrow, q_host, batch * qrow, batch * qrow, L,
+                        cudaMemcpyHostToDevice, st) == cudaSuccess &&
+      cudaMemcpy2DAsync(c.k_new, Bmax * kvrow, k_new_host, batch * kvrow, batch * kvrow, L,
+                        cudaMemcpyHostToDevice, st) == cudaSuccess &&
+      cudaMemcpy2DAsync(c.v_new, Bmax * kvrow, v_new_host, batch * kvrow, batch * kvrow, L,
+                        cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  s = decode_graph_launch(g, batch, nullptr, stream);
+  if (s != PKV_OK) return s;
+  if (cudaMemcpy2DAsync(out_host, batch * orow, c.out, Bmax * orow, batch * orow, L,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+

@@ -102,3 +102,41 @@ def test_graph_batch_out_of_range_is_refused(lib):
         with pytest.raises(pkv.PagedKVError):
             g.launch(bad)
     g.close()
+
+
+def test_step_from_host_memory_equals_graph_launch(lib):
+    """decode_graph_step_host (tables from the pool, host inputs in, output out)
+    gives the same bytes as filling the buffers and launching."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    eng, op, host, r = _setup(seed=3)
+    L, hq, hkv, d = eng.num_layers, 8, eng.num_kv_heads, eng.head_dim
+    g = pkv.DecodeGraph(eng, hq, 16, [1, 2, 4, 8])
+    sids = [0, 2, 5]
+    slots = eng.pool.append_slots(sids)
+    q = torch.from_numpy(W_store(r, (L, 3, hq, d)).view(np.int16)).view(torch.bfloat16)
+    kn = torch.from_numpy(W_store(r, (L, 3, hkv, d)).view(np.int16)).view(torch.bfloat16)
+    vn = torch.from_numpy(W_store(r, (L, 3, hkv, d)).view(np.int16)).view(torch.bfloat16)
+    q_h, kn_h, vn_h = q.pin_memory(), kn.pin_memory(), vn.pin_memory()
+    slots_h = torch.from_numpy(slots).pin_memory()
+    out_h = torch.empty((L, 3, hq, d), dtype=torch.float32).pin_memory()
+    before = eng.storage.clone()
+    g.step_host(eng.pool, sids, q_h, kn_h, vn_h, slots_h, out_h)
+    via_host = out_h.numpy().copy()
+    after = eng.storage.clone()
+    eng.storage.copy_(before)
+    tables, lens = eng.pool.batch_tables(sids, 16)
+    g.q[:, :3] = q.cuda()
+    g.k_new[:, :3] = kn.cuda()
+    g.v_new[:, :3] = vn.cuda()
+    g.slots[:3] = torch.from_numpy(slots).cuda()
+    g.tables[:3] = torch.from_numpy(tables).cuda()
+    g.lens[:3] = torch.from_numpy(lens).cuda()
+    g.launch(3)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.out[:, :3].cpu().numpy(), via_host)
+    assert torch.equal(eng.storage.view(torch.int16), after.view(torch.int16))
+    with pytest.raises(pkv.PagedKVError):
+        g.step_host(eng.pool, [0, 99], q_h[:, :2].contiguous(), kn_h[:, :2].contiguous(),
+                    vn_h[:, :2].contiguous(), slots_h[:2].contiguous(), out_h[:, :2].contiguous())
+    g.close()
