@@ -86,14 +86,20 @@ def workload_of(args):
     return w
 
 
+# The sources the decode kernels (and their launch) are built from.
+DECODE_SOURCES = ("common.cuh", "decode_api.cu", "decode_kernel.cuh", "decode_launch.cuh",
+                  "decode_mma.cuh", "decode_mma2.cuh", "decode_mma_fp8.cuh",
+                  "decode_mma_launch.cu", "decode_tc.cuh", "tmap.cuh")
+
+
 def kernel_sources_sha() -> str:
-    """Hash of the CUDA sources, to tie an ncu traffic figure to one kernel version."""
+    """Hash of the decode kernels' sources, to tie an ncu traffic figure to one
+    kernel version (changes elsewhere in the library do not invalidate it)."""
     csrc = os.path.join(ROOT, "paged_kv_cache_295_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in DECODE_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
