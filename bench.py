@@ -880,7 +880,9 @@ class ForkStep:
                 beams.append(nid)
                 nid += 1
         eng.pool.append_slots(beams)
-        self.pairs_h = eng.pool.take_copies()
+        pairs = eng.pool.take_copies()
+        # the engine's order: pairs of one source side by side (re-reads hit L2)
+        self.pairs_h = np.ascontiguousarray(pairs[np.argsort(pairs[:, 0], kind="stable")])
         self.pairs = torch.from_numpy(self.pairs_h).to(device)
         self.lens = lens
         plane = eng.storage[0, 0]

@@ -336,7 +336,8 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
  * so the whole pool has num_planes = 2 * num_layers, plane_stride_bytes =
  * num_blocks * block_bytes and block_bytes = block_size * num_kv_heads *
  * head_dim * element size.  Destinations must be distinct and no destination
- * may be another pair's source (true of one pool_take_copies batch).  Pairs
+ * may be another pair's source (true of one pool_take_copies batch); pairs
+ * that share a source are best placed side by side, so its re-reads hit L2.  Pairs
  * with an id outside [0, num_blocks) are skipped and flagged
  * PKV_DEV_BAD_BLOCK.  base 16-byte aligned; block_bytes and
  * plane_stride_bytes multiples of 16. */

@@ -76,7 +76,9 @@ class PagedKVCache:
         torch = _torch()
         pairs = self.pool.take_copies()
         if pairs.shape[0]:
-            d = torch.from_numpy(pairs).to(self.storage.device, non_blocking=False)
+            # pairs of one source side by side: its re-reads then hit L2
+            grouped = pairs[np.argsort(pairs[:, 0], kind="stable")]
+            d = torch.from_numpy(np.ascontiguousarray(grouped)).to(self.storage.device)
             copy_blocks(self.storage, d, device_status=device_status, stream=stream)
         return pairs
 
