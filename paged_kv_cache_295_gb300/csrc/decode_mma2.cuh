@@ -34,10 +34,15 @@
 namespace pkv {
 
 // Four 8-bit cache codes -> two f16x2 (bytes 0, 1 -> lo; 2, 3 -> hi), exactly.
+// INT8 codes come out as code + 1152 (kBias): in S^T = K q^T the offset adds
+// the same 1152 * sum(q) to every logit of a head, which its softmax (and the
+// split-KV merge) cancels; in O^T = V^T P^T it adds 1152 * sum(P), which the
+// epilogue subtracts, summing P as the fp16 values the MMA used.
+constexpr float kI8Bias = 1152.f;
 template <typename KV>
 __device__ __forceinline__ void byte4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   if constexpr (std::is_same<KV, INT8>::value)
-    s8x4_to_f16x2x2(w, lo, hi);
+    s8x4_to_f16x2x2_biased(w, lo, hi);
   else
     e4m3x4_to_f16x2x2(w, lo, hi);
 }
@@ -49,7 +54,7 @@ struct Mma2Smem {
   static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;      // K + V
   static constexpr int kScratch = 512;                            // P^T hi + lo (8 x 16 x 2 B each)
   static constexpr int kWarpBytes = STAGES * kStageBytes + 1024;  // + scratch, 1 KiB aligned
-  static_assert(STAGES * kStageBytes >= 8 * (D + 2) * 4, "combine area fits a warp ring");
+  static_assert(STAGES * kStageBytes >= 8 * (D + 3) * 4, "combine area fits a warp ring");
   static size_t bytes(int table_entries) {
     return 1024 + static_cast<size_t>(NW) * kWarpBytes + static_cast<size_t>(table_entries) * 4;
   }
@@ -60,7 +65,8 @@ __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma2_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const MmaParams mp) {
   using SM = Mma2Smem<KV, D, NW, STAGES>;
-  constexpr bool F8 = KV::kBytes == 1;
+  constexpr bool F8 = KV::kBytes == 1;                      // 8-bit codes (FP8 or INT8)
+  constexpr bool I8 = std::is_same<KV, INT8>::value;
   static_assert(!F8 || D == 128, "the 8-bit path is built for head_dim 128");
   constexpr int H = SM::kBoxes;
   constexpr int KSTEPS = D / 16;   // QK k-steps
@@ -158,6 +164,7 @@ __global__ void __launch_bounds__(NW * 32)
   for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   // softmax state of heads 2*tig and 2*tig+1
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  float ps0 = 0.f, ps1 = 0.f;   // INT8: sum of P as rounded to fp16 (the V offset's weight)
   const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
   const float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
 
@@ -292,6 +299,10 @@ __global__ void __launch_bounds__(NW * 32)
       const float a1 = h1ok ? exp2f(m1 - mn1) : 1.f;
       l0 *= a0;
       l1 *= a1;
+      if (I8) {
+        ps0 *= a0;
+        ps1 *= a1;
+      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         o[mt][0] *= a0;
@@ -310,9 +321,11 @@ __global__ void __launch_bounds__(NW * 32)
     l1 += p01 + p11;
     // P^T to B fragments via scratch: [head][token] (hi; lo for 16-bit caches)
     {
-      auto put = [&](int off, float v) {
+      auto put = [&](int off, float v, float& psum) {
         if (F8) {
-          *reinterpret_cast<__half*>(scratch + off) = __float2half_rn(v);
+          const __half hv = __float2half_rn(v);
+          *reinterpret_cast<__half*>(scratch + off) = hv;
+          if (I8) psum += __half2float(hv);
         } else {
           const __nv_bfloat16 hv = __float2bfloat16_rn(v);
           *reinterpret_cast<__nv_bfloat16*>(scratch + off) = hv;
@@ -320,10 +333,10 @@ __global__ void __launch_bounds__(NW * 32)
               __float2bfloat16_rn(v - __bfloat162float(hv));
         }
       };
-      put(((2 * tig) * 16 + gid) * 2, p00);
-      put(((2 * tig + 1) * 16 + gid) * 2, p01);
-      put(((2 * tig) * 16 + gid + 8) * 2, p10);
-      put(((2 * tig + 1) * 16 + gid + 8) * 2, p11);
+      put(((2 * tig) * 16 + gid) * 2, p00, ps0);
+      put(((2 * tig + 1) * 16 + gid) * 2, p01, ps1);
+      put(((2 * tig) * 16 + gid + 8) * 2, p10, ps0);
+      put(((2 * tig + 1) * 16 + gid + 8) * 2, p11, ps1);
     }
     __syncwarp();
     const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(scratch + (gid * 16 + 2 * tig) * 2);
@@ -377,13 +390,17 @@ __global__ void __launch_bounds__(NW * 32)
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (I8) {
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+    }
   }
   if (!alive) {
     m0 = m1 = -CUDART_INF_F;
     l0 = l1 = 0.f;
   }
   __syncwarp();
-  float* wres = reinterpret_cast<float*>(ring);   // [8][D] acc, then m[8], l[8]
+  float* wres = reinterpret_cast<float*>(ring);   // [8][D] acc, then m[8], l[8], psum[8]
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int h = 2 * tig + e;
@@ -398,6 +415,7 @@ __global__ void __launch_bounds__(NW * 32)
       if (gid == 0) {
         wres[8 * D + h] = e ? m1 : m0;
         wres[8 * D + 8 + h] = e ? l1 : l0;
+        wres[8 * D + 16 + h] = alive ? (e ? ps1 : ps0) : 0.f;
       }
     }
   }
@@ -411,14 +429,16 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int w = 0; w < NW; ++w)
       M = fmaxf(M, reinterpret_cast<const float*>(smem + w * SM::kWarpBytes)[8 * D + h]);
-    float L = 0.f, O = 0.f;
+    float L = 0.f, O = 0.f, PS = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float* r = reinterpret_cast<const float*>(smem + w * SM::kWarpBytes);
       const float c = exp2f(r[8 * D + h] - M);
       L = fmaf(r[8 * D + 8 + h], c, L);
       O = fmaf(r[h * D + d], c, O);
+      if (I8) PS = fmaf(r[8 * D + 16 + h], c, PS);
     }
+    if (I8) O = fmaf(-kI8Bias, PS, O);   // the V codes' offset
     const int64_t sh = static_cast<int64_t>(s) * p.num_q_heads + hq0 + h;
     if (single) {
       p.out[sh * D + d] = O / L * vsc;

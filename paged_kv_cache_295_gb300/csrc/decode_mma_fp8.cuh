@@ -64,6 +64,16 @@ __device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
+// The same widening without the final subtraction: each value is code + 1152,
+// exactly.  A caller that keeps the offset corrects for it (a constant added
+// to every logit of a head cancels in its softmax; for P V it subtracts
+// 1152 * sum(P) once at the end).
+__device__ __forceinline__ void s8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
+
 // Two E4M3 codes (low byte first) -> f16x2 with the low byte in the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu),
