@@ -16,7 +16,7 @@ from oracle import attention as OA
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2}
+TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2, "int8": 1e-2}
 
 
 def _bits(t, dtype):
@@ -26,6 +26,8 @@ def _bits(t, dtype):
         return t.view(torch.int16).numpy().view(np.uint16)
     if dtype == "f32":
         return t.numpy()
+    if dtype == "int8":
+        return t.numpy().astype(np.int8)
     return t.numpy().astype(np.uint8)
 
 
@@ -38,7 +40,7 @@ def _sample_seqs(w, lens):
     return sorted(pick)
 
 
-@pytest.mark.parametrize("name", [w.name for w in W.ALL])
+@pytest.mark.parametrize("name", [w.name for w in W.ALL] + ["llama7b_layer_int8"])
 def test_fullsize_sampled_parity(lib, name):
     import torch
     import bench
@@ -62,7 +64,7 @@ def test_fullsize_sampled_parity(lib, name):
         assert np.isfinite(got).all()
         ks_dev, vs_dev = st.src[layer]
         kscale = vscale = None
-        if w.kv_dtype == "fp8_e4m3":
+        if w.kv_dtype in ("fp8_e4m3", "int8"):
             kscale = eng.k_scale[layer].cpu().numpy()
             vscale = eng.v_scale[layer].cpu().numpy()
         qh = _bits(st.q[layer][0], w.q_dtype)
@@ -78,7 +80,8 @@ def test_fullsize_sampled_parity(lib, name):
             vsrc = np.concatenate([_bits(vs_dev[idx], sd), vn[s:s + 1]])
             assert ksrc.shape[0] == L
             nb = -(-L // bs)
-            dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}[w.kv_dtype]
+            dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8,
+                  "int8": np.int8}[w.kv_dtype]
             kc = np.zeros((nb, bs, w.num_kv_heads, w.head_dim), dtype=dt)
             vc = np.zeros_like(kc)
             OA.reshape_and_cache(ksrc, vsrc, np.arange(L), kc, vc, sd, w.kv_dtype, kscale, vscale)
