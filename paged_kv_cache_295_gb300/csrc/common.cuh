@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <array>
+#include <mutex>
+#include <unordered_map>
+
 #include "pagedkv.h"
 
 namespace pkv {
@@ -20,6 +24,29 @@ inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK 
 
 // Number of SMs of the current device, cached per device.
 int device_sm_count();
+
+// Opts kernel `kern` into `bytes` of dynamic shared memory on the current
+// device.  The attribute belongs to the function in each device's context, so
+// the largest value set so far is remembered per (kernel, device).
+inline bool opt_in_smem(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, std::array<int, 64>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    dev = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find(kern);
+  if (it == done.end()) it = done.emplace(kern, std::array<int, 64>{}).first;
+  int& have = it->second[dev];
+  if (bytes <= have) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  have = bytes;
+  return true;
+}
 
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);

@@ -19,13 +19,8 @@ pkv_status launch_decode(const DecodeLaunch& a) {
   const int table_entries = (p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = SM::bytes(table_entries);
   auto kern = paged_decode_kernel<KV, D, G, kDecodeWarps, kDecodeStages>;
-  static int configured_bytes = 0;   // largest dynamic smem opted in so far
-  if (static_cast<int>(smem) > configured_bytes) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
-    configured_bytes = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   dim3 grid(p.max_parts, p.num_kv_heads, a.num_seqs);
   kern<<<grid, kDecodeWarps * 32, smem, a.stream>>>(p);
   cudaError_t e = cudaGetLastError();

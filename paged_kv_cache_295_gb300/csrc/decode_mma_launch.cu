@@ -34,13 +34,8 @@ pkv_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams&
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = SM::bytes(table_entries);
   auto kern = paged_decode_mma_kernel<D, QF32, ROWS16, NW, STAGES>;
-  static int configured = 0;
-  if (static_cast<int>(smem) > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -57,13 +52,8 @@ pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPar
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = SM::bytes(table_entries);
   auto kern = paged_decode_mma_fp8_kernel<QF32, ROWS16, NW, STAGES>;
-  static int configured = 0;
-  if (static_cast<int>(smem) > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -79,13 +69,8 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = TcLayout::bytes(STAGES, table_entries);
   auto kern = paged_decode_tc_kernel<QF32, STAGES>;
-  static int configured = 0;
-  if (static_cast<int>(smem) > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
   kern<<<grid, kTcThreads, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -106,13 +91,8 @@ pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = SM::bytes(table_entries);
   auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES>;
-  static int configured = 0;
-  if (static_cast<int>(smem) > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;

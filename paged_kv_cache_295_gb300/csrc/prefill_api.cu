@@ -81,13 +81,8 @@ extern "C" pkv_status paged_attention_prefill(
   constexpr int STAGES = kPfStages;
   const size_t smem = PfLayout::bytes(STAGES);
   auto kern = paged_prefill_tc_kernel<STAGES>;
-  static int configured = 0;
-  if (static_cast<int>(smem) > configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured = static_cast<int>(smem);
-  }
+  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+    return PKV_ERR_CUDA;
   const int pairs = (max_query_len + 2 * p.tile_tokens - 1) / (2 * p.tile_tokens);
   dim3 grid(pairs, num_kv_heads, num_seqs);
   kern<<<grid, kPfThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tk, tv, p);
