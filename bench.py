@@ -124,8 +124,8 @@ class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
 
     def __init__(self, gpu_index: int, period_ms: int = 50):
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"pagedkv_clocks_gpu{gpu_index}.csv")
         self.proc = None
         try:
             self.fh = open(self.path, "w")
