@@ -4,7 +4,11 @@
 //
 // Work decomposition.  One CTA per (sequence s, KV head g, partition of P
 // tokens).  The CTA owns all G = Hq/Hkv query heads of KV head g, so every
-// K/V byte is read from HBM once per KV head (query-group packing).  Inside
+// K/V byte is read from HBM once per KV head (query-group packing).  The grid
+// is (Hkv, partitions, sequences) with the KV head fastest: CTAs that start
+// together read the same tokens of every head, i.e. whole [Hkv, D] token rows
+// of a block, so DRAM pages are read end to end instead of one head's slice
+// at a time (worth about 3 % of HBM bandwidth on 128K-token contexts).  Inside
 // the CTA each warp is an independent streaming consumer: it takes every
 // NW-th chunk of CH tokens of the partition, stages the chunk's K and V rows
 // into its own shared-memory ring with 16-byte cp.async copies (STAGES deep,
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int LPR = S::LPR, TPI = S::TPI, EPL = S::EPL, CH = S::CH, RB = S::RB;
 
   extern __shared__ __align__(16) uint4 smem[];
-  const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
+  const int s = blockIdx.z, g = blockIdx.x, part = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, seg = lane % LPR;
   const int P = p.partition_tokens;

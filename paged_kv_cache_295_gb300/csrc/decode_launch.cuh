@@ -21,7 +21,7 @@ pkv_status launch_decode(const DecodeLaunch& a) {
   auto kern = paged_decode_kernel<KV, D, G, kDecodeWarps, kDecodeStages>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(p.max_parts, p.num_kv_heads, a.num_seqs);
+  dim3 grid(p.num_kv_heads, p.max_parts, a.num_seqs);
   kern<<<grid, kDecodeWarps * 32, smem, a.stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return PKV_ERR_CUDA;

@@ -78,10 +78,10 @@ __global__ void __launch_bounds__(NW * 32)
   __shared__ __align__(8) uint64_t bars[NW][STAGES];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
-  const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int P = p.partition_tokens;
+  const int s = blockIdx.z, g = blockIdx.x, part = blockIdx.y;
 
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);

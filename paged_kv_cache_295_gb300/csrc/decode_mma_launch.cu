@@ -36,7 +36,7 @@ pkv_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams&
   auto kern = paged_decode_mma_kernel<D, QF32, ROWS16, NW, STAGES>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
@@ -54,7 +54,7 @@ pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPar
   auto kern = paged_decode_mma_fp8_kernel<QF32, ROWS16, NW, STAGES>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
@@ -71,7 +71,7 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
   auto kern = paged_decode_tc_kernel<QF32, STAGES>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
   kern<<<grid, kTcThreads, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
@@ -93,7 +93,7 @@ pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
   auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(mp.p.max_parts, mp.p.num_kv_heads, num_seqs);
+  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;

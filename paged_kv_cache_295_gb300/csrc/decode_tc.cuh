@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads)
   const uint32_t sma = smem_u32(sm);
   volatile int* abort_flag = &abort_sh;
 
-  const int s = blockIdx.z, g = blockIdx.y, part = blockIdx.x;
+  const int s = blockIdx.z, g = blockIdx.x, part = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_tokens;
 
