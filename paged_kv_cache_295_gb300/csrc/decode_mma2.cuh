@@ -60,6 +60,10 @@ struct Mma2Smem {
   }
 };
 
+// Largest log2 gap between a head's reference max and a chunk's max before
+// the running state is rescaled (p = 2^(s - m) < 2^8 in the P operands).
+constexpr float kLazyLog2 = 8.f;
+
 template <typename KV, int D, bool QF32, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma2_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -293,10 +297,16 @@ __global__ void __launch_bounds__(NW * 32)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
-      const float a0 = h0ok ? exp2f(m0 - mn0) : 1.f;   // m = -inf first: exp2(-inf) = 0
-      const float a1 = h1ok ? exp2f(m1 - mn1) : 1.f;
+    // Lazy rescale: a head's reference max moves only when the chunk's max is
+    // more than 2^kLazyLog2 above it, so p = 2^(s - m) stays below 256 and the
+    // O rescale runs about once per partition instead of on most chunks (with
+    // 8 heads one of them sets a new max in most chunks).  l and O share m, so
+    // the normalised result is unchanged.  m = -inf first: every real head moves.
+    const bool up0 = mx0 > m0 + kLazyLog2, up1 = mx1 > m1 + kLazyLog2;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+      const float a0 = up0 ? exp2f(m0 - mn0) : 1.f;   // exp2(-inf) = 0
+      const float a1 = up1 ? exp2f(m1 - mn1) : 1.f;
       l0 *= a0;
       l1 *= a1;
       if (I8) {
