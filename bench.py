@@ -313,7 +313,7 @@ class DeviceStep:
             self.vn.append(vn)
         self.out = torch.empty((S, hq, d), dtype=torch.float32, device=device)
         self.ws = eng.workspace_for(S, hq, self.max_ctx, partition, device=device)
-        self.P = pkv.partition_tokens(S, hkv, self.max_ctx, partition)
+        self.P = pkv.partition_tokens(S, hq, hkv, self.max_ctx, partition)
         self.max_parts = max(1, -(-self.max_ctx // self.P))
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         torch.cuda.synchronize(device)
@@ -506,7 +506,7 @@ def run_graph(st, K, Wm, world, dev, dt_eager, kv_log):
     rep = {"buckets": buckets, "bucket_used": S, "ms_per_step": round(dt / K * 1e3, 5),
            "eager_ms_per_step": round(dt_eager / K * 1e3, 5),
            "speedup_vs_eager": round(dt_eager / dt, 3),
-           "partition_tokens": pkv.partition_tokens(S, w.num_kv_heads,
+           "partition_tokens": pkv.partition_tokens(S, w.num_q_heads, w.num_kv_heads,
                                                     st.tables.shape[1] * w.block_size),
            "note": "value, ms_per_step and decode_tokens_per_s are the graph replay's"}
     g.close()

@@ -275,9 +275,13 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, const int64_t
 
 /* Tokens per split-KV partition that paged_attention_decode uses for this
  * problem when its partition_tokens argument is 0 (depends on the current
- * device's SM count).  Returns 0 on bad arguments. */
-int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_kv_heads,
-                                         int32_t max_context_len, int32_t partition_tokens);
+ * device's SM count and on the group size num_q_heads / num_kv_heads); a
+ * non-zero partition_tokens (a multiple of 64) is returned as is.  Returns 0
+ * on bad arguments (negative sizes, num_q_heads not a multiple of
+ * num_kv_heads, partition_tokens not a multiple of 64). */
+int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t max_context_len,
+                                         int32_t partition_tokens);
 
 /* Device scratch that paged_attention_decode needs for its split-KV partials
  * (0 when every sequence fits one partition): num_seqs * num_q_heads *

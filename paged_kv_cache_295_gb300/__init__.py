@@ -101,7 +101,7 @@ _SIGS = {
     "decode_graph_destroy": (None, [P]),
     "decode_graph_step_host": (I32, [P, P, P, I32, P, P, P, P, P, P]),
     "reshape_and_cache": (I32, [P, P, P, P, P, I32, I32, I32, I32, I64, I32, I32, P, P, P, P]),
-    "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32]),
+    "paged_attention_partition_tokens": (I32, [I32, I32, I32, I32, I32]),
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "paged_attention_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32, I32, FL,
                                      I32, I32, P, P, P, P, SZ, I32, P, P]),
@@ -390,8 +390,8 @@ def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=None
     _check(st, "reshape_and_cache")
 
 
-def partition_tokens(num_seqs, num_kv_heads, max_context_len, requested=0) -> int:
-    return int(library().paged_attention_partition_tokens(num_seqs, num_kv_heads,
+def partition_tokens(num_seqs, num_q_heads, num_kv_heads, max_context_len, requested=0) -> int:
+    return int(library().paged_attention_partition_tokens(num_seqs, num_q_heads, num_kv_heads,
                                                            max_context_len, requested))
 
 

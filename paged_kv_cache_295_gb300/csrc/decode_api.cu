@@ -53,18 +53,26 @@ int log2i(int64_t x) {
 // tokens) per SM over the longest sequence, so the grid runs many waves and
 // a ragged tail costs little; keep partitions between 256 and 4096 tokens so
 // per-CTA set-up and the partial round trip stay a small share of the bytes.
-int32_t auto_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_ctx) {
+// A partition writes G * (D + 2) floats of partials (and the reduce reads them
+// back) per 2 * P * D cache elements it reads, so the partials' share of the
+// traffic grows with the group size G: P is at least 256 * G, which keeps it
+// near 0.4 % (GQA-8 on the 70B-shaped layer: 2048 instead of 1024, 2 % faster).
+int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t max_ctx) {
   const double work = static_cast<double>(num_seqs) * num_kv_heads * (max_ctx > 0 ? max_ctx : 1);
   const double items = 16.0 * device_sm_count();
   int64_t want = static_cast<int64_t>(work / items);
+  const int64_t floor_g = 256LL * (num_q_heads / num_kv_heads);
+  if (want < floor_g) want = floor_g;
   int64_t P = 256;
   while (P * 2 <= want && P < 4096) P *= 2;
   return static_cast<int32_t>(P);
 }
 
-int32_t resolve_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_ctx, int32_t req) {
+int32_t resolve_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t max_ctx, int32_t req) {
   if (req < 0 || (req > 0 && req % 64 != 0)) return 0;
-  return req > 0 ? req : auto_partition(num_seqs, num_kv_heads, max_ctx);
+  return req > 0 ? req : auto_partition(num_seqs, num_q_heads, num_kv_heads, max_ctx);
 }
 
 int32_t parts_for(int32_t max_ctx, int32_t P) {
@@ -114,11 +122,15 @@ LaunchFn pick(int32_t kv_dtype, int D, int G) {
 }  // namespace
 }  // namespace pkv
 
-extern "C" int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_kv_heads,
+extern "C" int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_q_heads,
+                                                    int32_t num_kv_heads,
                                                     int32_t max_context_len,
                                                     int32_t partition_tokens) {
-  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
-  return pkv::resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+      max_context_len < 0)
+    return 0;
+  return pkv::resolve_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+                                partition_tokens);
 }
 
 extern "C" size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
@@ -128,7 +140,8 @@ extern "C" size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_context_len < 0)
     return 0;
-  const int32_t P = pkv::resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+  const int32_t P = pkv::resolve_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+                                           partition_tokens);
   if (P <= 0) return 0;
   const int32_t parts = pkv::parts_for(max_context_len, P);
   if (parts <= 1) return 0;
@@ -172,7 +185,8 @@ extern "C" pkv_status paged_attention_decode(
   if ((kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) && (!k_scale || !v_scale))
     return PKV_ERR_INVALID_ARG;
 
-  const int32_t P = resolve_partition(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+  const int32_t P =
+      resolve_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len, partition_tokens);
   const int32_t parts = parts_for(max_context_len, P);
   const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
                                                       head_dim, max_context_len, P);

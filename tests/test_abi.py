@@ -271,5 +271,18 @@ def test_workspace_formula(lib):
     # explicit partition: S * Hq * ceil(ctx/P) * (D+2) * 4
     assert lib.workspace_bytes(8, 32, 8, 128, 131072, 2048) == 8 * 32 * 64 * 130 * 4
     assert lib.workspace_bytes(8, 32, 8, 128, 2048, 2048) == 0
-    assert lib.partition_tokens(8, 8, 1000, 192) == 192
-    assert lib.partition_tokens(8, 8, 1000, 100) == 0
+    assert lib.partition_tokens(8, 32, 8, 1000, 192) == 192
+    assert lib.partition_tokens(8, 32, 8, 1000, 100) == 0
+    assert lib.partition_tokens(8, 30, 8, 1000, 0) == 0          # Hq not a multiple of Hkv
+
+
+def test_auto_partition_floor_grows_with_group(lib):
+    """The automatic partition is a power of two in [256, 4096] and at least
+    256 * G tokens (the partials' share of the traffic grows with G)."""
+    for S, hq, hkv, ctx in [(32, 32, 32, 4085), (64, 64, 8, 8117), (8, 32, 8, 128932),
+                            (1, 8, 8, 10), (256, 32, 32, 16384), (4, 128, 8, 300)]:
+        P = lib.partition_tokens(S, hq, hkv, ctx, 0)
+        G = hq // hkv
+        assert 256 <= P <= 4096 and P & (P - 1) == 0
+        assert P >= min(256 * G, 4096)
+    assert lib.partition_tokens(64, 64, 8, 8117, 0) >= 2048        # 70B-shaped GQA-8 layer
