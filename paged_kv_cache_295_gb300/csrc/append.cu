@@ -21,6 +21,8 @@ __global__ void append_copy_kernel(const uint4* __restrict__ k_new, const uint4*
                                    uint4* __restrict__ v_cache, int32_t num_tokens,
                                    int32_t num_kv_heads, int32_t segs, int64_t num_slots,
                                    int32_t* status) {
+  grid_dependency_wait();   // launched with launch_pdl: earlier work on the stream is done
+  allow_dependents();
   const int64_t per_kv = static_cast<int64_t>(num_tokens) * num_kv_heads * segs;
   const int64_t total = 2 * per_kv;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -101,6 +103,8 @@ __global__ void append_quant_kernel(const Src* __restrict__ k_new, const Src* __
                                   const float* __restrict__ v_scale, int32_t num_tokens,
                                   int32_t num_kv_heads, int32_t head_dim, int64_t num_slots,
                                   int32_t* status) {
+  grid_dependency_wait();   // launched with launch_pdl: earlier work on the stream is done
+  allow_dependents();
   const int32_t segs = head_dim / 16;
   const int64_t per_kv = static_cast<int64_t>(num_tokens) * num_kv_heads * segs;
   const int64_t total = 2 * per_kv;
@@ -170,10 +174,11 @@ extern "C" pkv_status reshape_and_cache(const void* k_new, const void* v_new,
   if (src_dtype == cache_dtype && !quant) {
     const int32_t segs = head_dim * es_dst / 16;
     const int64_t work = 2LL * num_tokens * num_kv_heads * segs;
-    append_copy_kernel<<<grid_for(work, kThreads), kThreads, 0, st>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, num_kv_heads, segs,
-        num_slots, device_status);
+    if (launch_pdl(append_copy_kernel, dim3(grid_for(work, kThreads)), dim3(kThreads), 0, st,
+                   static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                   slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                   num_tokens, num_kv_heads, segs, num_slots, device_status) != cudaSuccess)
+      return PKV_ERR_CUDA;
   } else if (quant && (src_dtype == PKV_F32 || src_dtype == PKV_BF16)) {
     if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
     const int64_t work = 2LL * num_tokens * num_kv_heads * (head_dim / 16);
@@ -181,15 +186,18 @@ extern "C" pkv_status reshape_and_cache(const void* k_new, const void* v_new,
     auto launch = [&](auto src_tag, auto q_tag) {
       using Src = decltype(src_tag);
       using Q = decltype(q_tag);
-      append_quant_kernel<Src, Q><<<grid, kThreads, 0, st>>>(
-          static_cast<const Src*>(k_new), static_cast<const Src*>(v_new), slot_mapping,
-          static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), k_scale, v_scale,
-          num_tokens, num_kv_heads, head_dim, num_slots, device_status);
+      return launch_pdl(append_quant_kernel<Src, Q>, dim3(grid), dim3(kThreads), 0, st,
+                        static_cast<const Src*>(k_new), static_cast<const Src*>(v_new),
+                        slot_mapping, static_cast<uint4*>(k_cache),
+                        static_cast<uint4*>(v_cache), k_scale, v_scale, num_tokens,
+                        num_kv_heads, head_dim, num_slots, device_status);
     };
+    cudaError_t e;
     if (cache_dtype == PKV_FP8_E4M3)
-      src_dtype == PKV_F32 ? launch(float{}, FP8{}) : launch(__nv_bfloat16{}, FP8{});
+      e = src_dtype == PKV_F32 ? launch(float{}, FP8{}) : launch(__nv_bfloat16{}, FP8{});
     else
-      src_dtype == PKV_F32 ? launch(float{}, INT8{}) : launch(__nv_bfloat16{}, INT8{});
+      e = src_dtype == PKV_F32 ? launch(float{}, INT8{}) : launch(__nv_bfloat16{}, INT8{});
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
   } else {
     return PKV_ERR_UNSUPPORTED;
   }

@@ -9,6 +9,7 @@
 #include <array>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "pagedkv.h"
 
@@ -21,6 +22,37 @@ inline int elem_bytes(int32_t dt) { return (dt >= 0 && dt <= 3) ? kElemBytes[dt]
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Programmatic dependent launch.  A kernel started by launch_pdl may begin
+// while the kernel before it on the stream is still running (its CTAs are
+// placed as soon as the earlier kernel's CTAs have all called
+// allow_dependents() or exited), so it must call grid_dependency_wait() before
+// it reads anything written by earlier work on the stream; the wait returns
+// once that work has completed and its writes are visible (at once when the
+// kernel was launched without the attribute).  This hides the launch and CTA
+// placement of back-to-back kernels (append, decode, split-KV reduce).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Number of SMs of the current device, cached per device.
 int device_sm_count();

@@ -360,6 +360,8 @@ __global__ void __launch_bounds__(NW * 32)
 // Combine split-KV partials: one CTA per (sequence, query head).
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeParams p) {
+  grid_dependency_wait();   // launched with launch_pdl: the partials are written
+  allow_dependents();
   const int sh = blockIdx.x;
   const int s = sh / p.num_q_heads;
   int ctx = __ldg(p.context_lens + s);

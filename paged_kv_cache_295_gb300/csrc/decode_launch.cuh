@@ -26,8 +26,8 @@ pkv_status launch_decode(const DecodeLaunch& a) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {
-    paged_decode_reduce_kernel<D><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(paged_decode_reduce_kernel<D>, dim3(a.num_seqs * p.num_q_heads), dim3(128), 0,
+                   a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;

@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(NW * 32)
   const int gid = lane >> 2, tig = lane & 3;
   const int P = p.partition_tokens;
   const int s = blockIdx.z, g = blockIdx.x, part = blockIdx.y;
+  grid_dependency_wait();   // launched with launch_pdl: earlier work on the stream is done
+  allow_dependents();
 
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);

@@ -89,8 +89,8 @@ pkv_status launch_mma2_shape(const CUtensorMap& tk, const CUtensorMap& tv, const
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
   dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
-  kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (launch_pdl(kern, grid, dim3(NW * 32), smem, stream, tk, tv, mp) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return PKV_OK;
 }
 
@@ -156,11 +156,11 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
                : launch_mma2<BF16, 64, false>(tk, tv, mp, a.num_seqs, a.stream);
   if (st != PKV_OK) return st;
   if (p.max_parts > 1) {
-    if (head_dim == 128)
-      paged_decode_reduce_kernel<128><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    else
-      paged_decode_reduce_kernel<64><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    const dim3 rgrid(a.num_seqs * p.num_q_heads);
+    const cudaError_t e =
+        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(128), 0, a.stream, p)
+                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(128), 0, a.stream, p);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
@@ -188,8 +188,9 @@ pkv_status launch_decode_tc(const DecodeLaunch& a, const void* k_cache, const vo
                               : launch_tc<false>(tk, tv, mp, a.num_seqs, a.stream);
   if (st != PKV_OK) return st;
   if (p.max_parts > 1) {
-    paged_decode_reduce_kernel<kTcD><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_pdl(paged_decode_reduce_kernel<kTcD>, dim3(a.num_seqs * p.num_q_heads), dim3(128),
+                   0, a.stream, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
@@ -245,11 +246,11 @@ pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const v
   }
   if (st != PKV_OK) return st;
   if (p.max_parts > 1) {
-    if (head_dim == 128)
-      paged_decode_reduce_kernel<128><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    else
-      paged_decode_reduce_kernel<64><<<a.num_seqs * p.num_q_heads, 128, 0, a.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    const dim3 rgrid(a.num_seqs * p.num_q_heads);
+    const cudaError_t e =
+        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(128), 0, a.stream, p)
+                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(128), 0, a.stream, p);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
