@@ -12,7 +12,7 @@
 // GQA), row r = token (r / G), head (r % G), so every K/V byte a CTA loads
 // serves all G heads of both tiles.  The CTA walks its keys in 64-token tiles:
 //
-//   S_t  = Q_t K^T    tcgen05.mma M=128 N=64  K=128   A = Q_t (smem, K-major)
+//   S_t  = Q_t K^T    tcgen05.mma M=128 N=64  K=128   A = Q_t (TMEM, written once)
 //                                                     B = K tile (smem, K-major)
 //   P_t  = 2^(S_t*scale*log2e - m)  in tile t's softmax warpgroup, one TMEM
 //                                   lane = one row
@@ -20,8 +20,12 @@
 //                                                          bf16 hi + lo parts)
 //                                                     B = V tile (smem, MN-major)
 //
-// for t = A (the earlier tokens) and B.  TMEM: per tile, S in two 64-column
-// buffers and O in 128 columns (512 columns in all).  Warp roles: warps 0-3
+// for t = A (the earlier tokens) and B.  TMEM: per tile, Q in 64 columns (row =
+// lane, column c = dims 2c and 2c+1), S in 64 and O in 128 (512 columns in
+// all).  Q read from TMEM takes its 32 KB per key tile and tile off the
+// tensor cores' shared-memory reads, which are close to the port's limit, and
+// frees the shared memory for 5 K/V stages; S is single-buffered, so QK of key
+// tile j+1 waits until the softmax has loaded S(j).  Warp roles: warps 0-3
 // softmax of tile A, warps 4-7 softmax of tile B (warp w owns TMEM lanes
 // 32(w%4)..+31, i.e. rows), warps 8 and 11 TMA producers of K and V (lanes
 // look up one key tile's blocks in one round trip and issue its boxes, one
@@ -45,7 +49,7 @@ constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
 constexpr int kPfD = 128;
 constexpr int kPfThreads = 384;   // 2 softmax warpgroups, K producer, QK issuer, PV issuer,
                                   // V producer
-constexpr int kPfStages = 3;
+constexpr int kPfStages = 5;
 
 struct PrefillParams {
   const __nv_bfloat16* q;        // [T, Hq, D]
@@ -98,15 +102,13 @@ __device__ __forceinline__ void pf_ld64(uint32_t taddr, float* v) {
 }
 
 struct PfLayout {
-  // [Q_A 2 x 16 KB][Q_B][P_A: hi 16 KB, lo 16 KB][P_B][stages: K 16 KB, V 16 KB]
-  static constexpr int kQHalf = kPfRows * 128;         // [128 rows][128 B]
-  static constexpr int kQ = 2 * kQHalf;                // one query tile
+  // [P_A: hi 16 KB, lo 16 KB][P_B][stages: K 16 KB, V 16 KB]
   static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
   static constexpr int kPBuf = 2 * kPPart;             // hi + lo
-  static constexpr int kP = 2 * kQ;                    // P_A, then P_B
+  static constexpr int kP = 0;                         // P_A, then P_B
   static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
   static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
-  static constexpr int kStages = kP + 2 * kPBuf;
+  static constexpr int kStages = kP + 2 * kPBuf;       // offset of the stage ring
   static constexpr size_t bytes(int stages) {
     return 1024 + static_cast<size_t>(kStages) + static_cast<size_t>(stages) * kStage;
   }
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[STAGES], full_v[STAGES], empty[STAGES];
-  __shared__ __align__(8) uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], drain[2];
+  __shared__ __align__(8) uint64_t s_full[2], s_free[2], q_ready[2], p_full[2], o_done[2], drain[2];
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -164,19 +166,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int ntiles = max(nt_a, nt_b);
   const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
 
-  // Q tiles (A operands of QK): tile t row r = token tok0 + t*TQ + r / G, head
-  // g*G + r % G; 16-byte chunks into two 128-byte-swizzled halves.  Rows past
-  // the chunk are zero.
-  for (int i = tid; i < 2 * kPfRows * 16; i += kPfThreads) {
-    const int t = i / (kPfRows * 16), j = i % (kPfRows * 16);
-    const int r = j >> 4, u = j & 15, hh = u >> 3, uu = u & 7;
-    const int tk = tok0 + t * TQ + r / G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TQ * G && tk < n)
-      v = *reinterpret_cast<const uint4*>(
-          p.q + (static_cast<int64_t>(q0 + tk) * p.num_q_heads + g * G + r % G) * kPfD + 8 * u);
-    *reinterpret_cast<uint4*>(sm + t * LY::kQ + hh * LY::kQHalf + swz(r, uu)) = v;
-  }
   if (tid == 0) {
     for (int st = 0; st < STAGES; ++st) {
       mbar_init(smem_u32(&full[st]), 1);     // K copies and the key mask
@@ -184,10 +173,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(smem_u32(&empty[st]), 1);
     }
     for (int t = 0; t < 2; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&s_full[t][b]), 1);
-        mbar_init(smem_u32(&s_free[t][b]), 4);
-      }
+      mbar_init(smem_u32(&s_full[t]), 1);
+      mbar_init(smem_u32(&s_free[t]), 4);
+      mbar_init(smem_u32(&q_ready[t]), 4);
       mbar_init(smem_u32(&p_full[t]), 4);
       mbar_init(smem_u32(&o_done[t]), 1);
     }
@@ -206,7 +194,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM: tile t's S buffers at columns 256t + {0, 64}, its O at 256t + 128
+  // TMEM: tile t's Q at columns 256t + [0, 64), S at 256t + 64, O at 256t + 128
   const uint32_t tm = tmem_base_sh;
 
   if (warp == 8 || warp == 11) {
@@ -265,7 +253,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 9) {
     // ---------------------------- QK issuer ------------------------------------
     // Key tiles in order, tile A then B: once the stage has landed and the S
-    // buffer is free.  Its commits cover only its own MMAs (s_full).
+    // buffer is free (the softmax has loaded the previous S; Q is in TMEM
+    // before the first).  Its commits cover only its own MMAs (s_full).
     if (lane == 0) {
       const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, true);
       for (int j = 0; j < ntiles; ++j) {
@@ -274,23 +263,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         bool ok = true;
         for (int t = 0; t < 2; ++t) {
           if (j >= (t == 0 ? nt_a : nt_b)) continue;
-          if (j >= 2 && !tc_wait(smem_u32(&s_free[t][j & 1]), ((j - 2) >> 1) & 1, abort_flag)) {
+          const bool ready = j == 0 ? tc_wait(smem_u32(&q_ready[t]), 0, abort_flag)
+                                    : tc_wait(smem_u32(&s_free[t]), (j - 1) & 1, abort_flag);
+          if (!ready) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dst = tm + 256 * t + (j & 1) * kPfKeys;
-          // descriptors built once; a k-step only moves the start address
-          // (bits 0-13, in 16-byte units)
-          const uint64_t qd = tc_desc(sma + t * LY::kQ, 0, 1024);
+          const uint32_t dst = tm + 256 * t + kPfKeys;
+          // the K descriptor is built once; a k-step only moves its start
+          // address (bits 0-13, in 16-byte units) and Q's TMEM column (8 per
+          // 16 dims)
           const uint64_t kd = tc_desc(kb, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < kPfD / 16; ++ks) {
-            const uint32_t off_q = (ks >> 2) * LY::kQHalf + (ks & 3) * 32;
             const uint32_t off_k = (ks >> 2) * LY::kKVHalf + (ks & 3) * 32;
-            tc_mma(dst, qd + (off_q >> 4), kd + (off_k >> 4), idesc_qk, ks > 0);
+            tc_mma_ts(dst, tm + 256 * t + 8 * ks, kd + (off_k >> 4), idesc_qk, ks > 0);
           }
-          tc_commit(smem_u32(&s_full[t][j & 1]));
+          tc_commit(smem_u32(&s_full[t]));
         }
         if (!ok) break;
       }
@@ -340,9 +330,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = tid & 127;                            // accumulator row = TMEM lane
     const int my_nt = t == 0 ? nt_a : nt_b;
     const uint32_t lane_q = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tm + 256 * t, tO = tm + 256 * t + 2 * kPfKeys;
+    const uint32_t tQ = tm + 256 * t, tS = tQ + kPfKeys, tO = tQ + 2 * kPfKeys;
     const int tl = r / G;
     const bool row_ok = r < TQ * G && tok0 + t * TQ + tl < n;
+    {   // this row of Q_t (token tok0 + t*TQ + r/G, head g*G + r%G; 0 past the
+        // chunk) into TMEM, bf16 pairs per column: the A operand of every QK
+      float w[64];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads + g * G + r % G) *
+                    kPfD);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 v = row_ok ? src[i] : make_uint4(0, 0, 0, 0);
+        w[4 * i] = __uint_as_float(v.x);
+        w[4 * i + 1] = __uint_as_float(v.y);
+        w[4 * i + 2] = __uint_as_float(v.z);
+        w[4 * i + 3] = __uint_as_float(v.w);
+      }
+      tc_st32(tQ + lane_q, w);
+      tc_st32(tQ + lane_q + 32, w + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&q_ready[t]));
+    }
     const int qpos = ctx - n + tok0 + t * TQ + tl;      // this row's position
     const int last = p.causal ? qpos : ctx - 1;         // last key it sees
     const float sl2 = p.qk_scale_log2;
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int k0 = j * kPfKeys;
       // S(j) ready implies the stage's copies landed; waiting on the stage's
       // barrier as well makes the producer's key mask for it visible here.
-      if (!tc_wait(smem_u32(&s_full[t][j & 1]), (j >> 1) & 1, abort_flag) ||
+      if (!tc_wait(smem_u32(&s_full[t]), j & 1, abort_flag) ||
           !tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag))
         alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
@@ -366,10 +376,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool dense = pos_scale && __all_sync(0xffffffffu, rmask == ~0ull);
       tc_fence_after();
       float sv[kPfKeys];
-      pf_ld64(tS + lane_q + (j & 1) * kPfKeys, sv);
+      pf_ld64(tS + lane_q, sv);
       tc_fence_before();
       __syncwarp();
-      if ((lane & 31) == 0) mbar_arrive(smem_u32(&s_free[t][j & 1]));
+      if ((lane & 31) == 0) mbar_arrive(smem_u32(&s_free[t]));
       float mt;
       if (dense) {   // warp-uniform: nothing masked; max of the raw logits, then scale
         float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
