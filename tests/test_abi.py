@@ -286,3 +286,12 @@ def test_auto_partition_floor_grows_with_group(lib):
         assert 256 <= P <= 4096 and P & (P - 1) == 0
         assert P >= min(256 * G, 4096)
     assert lib.partition_tokens(64, 64, 8, 8117, 0) >= 2048        # 70B-shaped GQA-8 layer
+
+
+def test_auto_partition_small_batches_fill_one_wave(lib):
+    """Below 1024 tokens the partition doubles while the grid still fills one
+    wave of three CTAs per SM (152 SMs here and without a device)."""
+    assert lib.partition_tokens(2, 32, 32, 974, 0) == 256          # 256 items at 256 already
+    assert lib.partition_tokens(8, 32, 32, 974, 0) == 512          # 512 items at 512
+    assert lib.partition_tokens(32, 32, 32, 974, 0) == 1024        # one partition each
+    assert lib.partition_tokens(32, 32, 32, 4085, 0) == 1024       # large work: unchanged
