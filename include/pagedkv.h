@@ -332,6 +332,32 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   int32_t partition_tokens, int32_t* device_status,
                                   pkv_stream_t stream);
 
+/* One decode step with the append fused in: the same as
+ *   reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, num_seqs, ...)
+ *   paged_attention_decode(q, k_cache, v_cache, ...)
+ * on the same stream [TUT 4.2 append_token, then 4.4 forward], for one new
+ * token per sequence: k_new / v_new are device [num_seqs, num_kv_heads,
+ * head_dim] of src_dtype (f32|bf16; equal to kv_dtype for f32 / bf16
+ * caches), slot_mapping device [num_seqs] int64.  slot_mapping[s] must be the
+ * slot of position context_lens[s] - 1 (the appended token is the last one
+ * attended), or negative for no append.
+ * Where the transposed tensor-core kernel runs (bf16, FP8 and INT8 caches,
+ * head_dim 128, and bf16 64; G <= 8; block_size >= 8), that kernel writes
+ * each sequence's new row for its KV head before it reads the block, in the
+ * same launch, with the append kernel's exact rounding.  A slot that is not
+ * the block table's slot for position context_lens[s] - 1 (or a context of
+ * 0 with a slot) is not written and flags PKV_DEV_BAD_SLOT, and the
+ * attention then reads the cache as it was.  Elsewhere the call runs the two
+ * kernels.  Arguments and errors otherwise as the two calls'. */
+pkv_status paged_attention_decode_append(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    int32_t src_dtype, void* k_cache, void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
+    const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
+    int32_t partition_tokens, int32_t* device_status, pkv_stream_t stream);
+
 /* Copy-on-write block copies [TUT 4.2]: for each (src, dst) pair of
  * pairs[0 .. 2n) (device int32), every plane's block dst becomes a copy of its
  * block src.  A plane is one (layer, K or V) slice of the pool tensor

@@ -105,6 +105,9 @@ _SIGS = {
     "paged_attention_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "paged_attention_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32, I32, FL,
                                      I32, I32, P, P, P, P, SZ, I32, P, P]),
+    "paged_attention_decode_append": (I32, [P, P, P, P, I32, P, P, P, P, I32, I32, I32, I32, I32,
+                                            I64, I32, I32, FL, I32, I32, P, P, P, P, SZ, I32, P,
+                                            P]),
     "paged_attention_decode_noalloc": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32,
                                              I32, FL, I32, I32, P, P, P, I32, P, P]),
     "paged_attention_prefill": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, I64,
@@ -427,6 +430,36 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         _dev(workspace, "workspace") if workspace is not None else None, ws_bytes,
         int(partition), _dev(device_status, "device_status"), _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                                  context_lens, scale, max_context_len, out=None, k_scale=None,
+                                  v_scale=None, workspace=None, partition=0, device_status=None,
+                                  stream=None):
+    """``reshape_and_cache`` of one new token per sequence (``k_new`` / ``v_new``
+    ``[S, Hkv, D]``, ``slot_mapping`` int64 ``[S]``, each the slot of position
+    ``context_lens[s] - 1``) and ``paged_attention_decode``, as one call."""
+    torch = _torch()
+    S, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((S, hq, d), dtype=torch.float32, device=q.device)
+    need = workspace_bytes(S, hq, hkv, d, max_context_len, partition)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = library().paged_attention_decode_append(
+        _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(slot_mapping, "slot_mapping"), _dtype_code(k_new), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"),
+        _dev(context_lens, "context_lens"), S, hq, hkv, d, bs, nb, mb, int(max_context_len),
+        float(scale), _dtype_code(q), _dtype_code(k_cache), _dev(k_scale, "k_scale"),
+        _dev(v_scale, "v_scale"), _dev(out, "out"),
+        _dev(workspace, "workspace") if workspace is not None else None, ws_bytes,
+        int(partition), _dev(device_status, "device_status"), _stream(stream))
+    _check(st, "paged_attention_decode_append")
     return out
 
 

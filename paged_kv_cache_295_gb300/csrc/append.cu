@@ -11,6 +11,7 @@
 // covers whole rows with coalesced 16-byte stores.  The work is tiny next to
 // the attention read, so the kernel is a plain grid-stride loop.
 #include "common.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 namespace {
@@ -47,54 +48,6 @@ __global__ void append_copy_kernel(const uint4* __restrict__ k_new, const uint4*
   }
 }
 
-template <typename Src>
-__device__ __forceinline__ void load16(const Src* p, float* x);
-
-template <>
-__device__ __forceinline__ void load16<float>(const float* p, float* x) {
-  const float4* v = reinterpret_cast<const float4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 f = __ldg(v + i);
-    x[4 * i + 0] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
-  }
-}
-
-template <>
-__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, float* x) {
-  const uint4* v = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    float y[8];
-    decode16<BF16>(__ldg(v + i), y);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) x[8 * i + k] = y[k];
-  }
-}
-
-// Four float32 quotients -> four cache bytes (low byte first).
-template <typename Q>
-__device__ __forceinline__ uint32_t quant4(const float* q);
-
-template <>
-__device__ __forceinline__ uint32_t quant4<FP8>(const float* q) {   // E4M3, RNE, saturating
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
-  return (lo & 0xFFFFu) | (hi << 16);
-}
-
-template <>
-__device__ __forceinline__ uint32_t quant4<INT8>(const float* q) {   // RNE, clamp, NaN -> 0
-  uint32_t w = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    int v = __float2int_rn(q[b]);   // round half to even; NaN -> 0, +-inf saturate
-    v = v < -128 ? -128 : (v > 127 ? 127 : v);
-    w |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * b);
-  }
-  return w;
-}
-
 // Quantising kernel: f32 / bf16 source -> 8-bit cache (Q = FP8 or INT8), per-head scale.
 template <typename Src, typename Q>
 __global__ void append_quant_kernel(const Src* __restrict__ k_new, const Src* __restrict__ v_new,
@@ -122,19 +75,9 @@ __global__ void append_quant_kernel(const Src* __restrict__ k_new, const Src* __
       if (!is_v && head == 0 && seg == 0) flag_status(status, PKV_DEV_BAD_SLOT);
       continue;
     }
-    float x[16];
-    load16<Src>((is_v ? v_new : k_new) + j * 16, x);
     const float s = __ldg((is_v ? v_scale : k_scale) + head);
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {   // IEEE float32 division, then the 8-bit code
-      float q[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(x[4 * k + e], s);
-      w[k] = quant4<Q>(q);
-    }
     const int64_t dst = (slot * num_kv_heads + head) * segs + seg;
-    (is_v ? v_cache : k_cache)[dst] = make_uint4(w[0], w[1], w[2], w[3]);
+    (is_v ? v_cache : k_cache)[dst] = quant16<Src, Q>((is_v ? v_new : k_new) + j * 16, s);
   }
 }
 

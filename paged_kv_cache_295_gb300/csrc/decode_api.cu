@@ -160,13 +160,24 @@ extern "C" size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_
   return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
 }
 
-extern "C" pkv_status paged_attention_decode(
-    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
-    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
-    const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
-    int32_t partition_tokens, int32_t* device_status, pkv_stream_t stream) {
+namespace {
+
+// The step's new token per sequence, appended by the decode call itself.
+struct FusedAppend {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+  int32_t src_dtype;
+};
+
+pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                       int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype,
+                       const float* k_scale, const float* v_scale, float* out, void* workspace,
+                       size_t workspace_bytes, int32_t partition_tokens, int32_t* device_status,
+                       pkv_stream_t stream, const FusedAppend* fa) {
   using namespace pkv;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       num_blocks <= 0 || num_blocks > INT32_MAX || max_blocks_per_seq <= 0 || max_context_len < 0)
@@ -232,6 +243,20 @@ extern "C" pkv_status paged_attention_decode(
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (fa) {
+    if (use_mma2) {   // the transposed kernel writes the new rows itself
+      p.k_new = fa->k_new;
+      p.v_new = fa->v_new;
+      p.new_slots = fa->slots;
+      p.new_src_dtype = fa->src_dtype;
+    } else {          // other kernels: the append kernel first, on the same stream
+      const pkv_status st = reshape_and_cache(
+          fa->k_new, fa->v_new, fa->slots, const_cast<void*>(k_cache),
+          const_cast<void*>(v_cache), num_seqs, num_kv_heads, head_dim, block_size, num_blocks,
+          fa->src_dtype, kv_dtype, k_scale, v_scale, device_status, stream);
+      if (st != PKV_OK) return st;
+    }
+  }
   if (use_tc) return launch_decode_tc(a, k_cache, v_cache, num_blocks, q_dtype == PKV_F32);
   if (use_mma2)
     return launch_decode_mma2(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
@@ -240,4 +265,45 @@ extern "C" pkv_status paged_attention_decode(
     return launch_decode_mma(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
                              kv_dtype == PKV_FP8_E4M3);
   return fn(a);
+}
+
+}  // namespace
+
+extern "C" pkv_status paged_attention_decode(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
+    const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
+    int32_t partition_tokens, int32_t* device_status, pkv_stream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                     max_context_len, scale, q_dtype, kv_dtype, k_scale, v_scale, out, workspace,
+                     workspace_bytes, partition_tokens, device_status, stream, nullptr);
+}
+
+extern "C" pkv_status paged_attention_decode_append(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    int32_t src_dtype, void* k_cache, void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+    int32_t max_context_len, float scale, int32_t q_dtype, int32_t kv_dtype, const float* k_scale,
+    const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
+    int32_t partition_tokens, int32_t* device_status, pkv_stream_t stream) {
+  using namespace pkv;
+  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8;
+  const bool combo = quant ? (src_dtype == PKV_F32 || src_dtype == PKV_BF16)
+                           : (src_dtype == kv_dtype && (kv_dtype == PKV_F32 || kv_dtype == PKV_BF16));
+  if (!combo) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+      return PKV_ERR_INVALID_ARG;
+  }
+  const FusedAppend fa{k_new, v_new, slot_mapping, src_dtype};
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                     max_context_len, scale, q_dtype, kv_dtype, k_scale, v_scale, out, workspace,
+                     workspace_bytes, partition_tokens, device_status, stream, &fa);
 }

@@ -47,7 +47,8 @@ pkv_status pad_rows(const pkv_decode_graph_config& c, int32_t from, int32_t to, 
   return cuda_status(cudaGetLastError());
 }
 
-// The step for a batch of B rows: every layer's append, then its decode.
+// The step for a batch of B rows: every layer's append and decode (one fused
+// call per layer; one launch per layer where the transposed kernel runs).
 pkv_status record_step(const pkv_decode_graph& g, int32_t B, cudaStream_t st) {
   const pkv_decode_graph_config& c = g.cfg;
   const int32_t Bmax = g.buckets.back();
@@ -58,18 +59,14 @@ pkv_status record_step(const pkv_decode_graph& g, int32_t B, cudaStream_t st) {
   for (int32_t l = 0; l < c.num_layers; ++l) {
     const float* ks = g.k_scales.empty() ? nullptr : g.k_scales[l];
     const float* vs = g.v_scales.empty() ? nullptr : g.v_scales[l];
-    pkv_status s = reshape_and_cache(
+    const pkv_status s = paged_attention_decode_append(
+        static_cast<const uint8_t*>(c.q) + l * q_layer * qb,
         static_cast<const uint8_t*>(c.k_new) + l * kv_layer * sb,
-        static_cast<const uint8_t*>(c.v_new) + l * kv_layer * sb, c.slot_mapping, g.k_caches[l],
-        g.v_caches[l], B, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.src_dtype,
-        c.kv_dtype, ks, vs, c.device_status, reinterpret_cast<pkv_stream_t>(st));
-    if (s != PKV_OK) return s;
-    s = paged_attention_decode(
-        static_cast<const uint8_t*>(c.q) + l * q_layer * qb, g.k_caches[l], g.v_caches[l],
-        c.block_tables, c.context_lens, B, c.num_q_heads, c.num_kv_heads, c.head_dim,
-        c.block_size, c.num_blocks, c.max_blocks_per_seq, max_ctx, c.scale, c.q_dtype, c.kv_dtype,
-        ks, vs, c.out + l * q_layer, c.workspace, c.workspace_bytes, 0, c.device_status,
-        reinterpret_cast<pkv_stream_t>(st));
+        static_cast<const uint8_t*>(c.v_new) + l * kv_layer * sb, c.slot_mapping, c.src_dtype,
+        g.k_caches[l], g.v_caches[l], c.block_tables, c.context_lens, B, c.num_q_heads,
+        c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.max_blocks_per_seq, max_ctx,
+        c.scale, c.q_dtype, c.kv_dtype, ks, vs, c.out + l * q_layer, c.workspace,
+        c.workspace_bytes, 0, c.device_status, reinterpret_cast<pkv_stream_t>(st));
     if (s != PKV_OK) return s;
   }
   return PKV_OK;

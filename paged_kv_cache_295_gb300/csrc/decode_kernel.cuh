@@ -60,6 +60,15 @@ struct DecodeParams {
   int32_t max_parts;
   int32_t q_is_bf16;
   float qk_scale_log2;   // scale * log2(e)
+  // Fused append (transposed kernel only; k_new == nullptr: none): the new
+  // token of sequence s, rows k_new/v_new[s, Hkv, D] of type new_src_dtype,
+  // goes to slot new_slots[s], which must be the slot of position
+  // context_lens[s] - 1; the CTA of that position's partition writes it for
+  // its KV head before it reads the block.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* new_slots;
+  int32_t new_src_dtype;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr, int src_bytes) {

@@ -30,6 +30,7 @@
 #include <type_traits>
 
 #include "decode_mma_fp8.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 
@@ -99,6 +100,9 @@ __global__ void __launch_bounds__(NW * 32)
   if (part >= (nparts > 0 ? nparts : 1)) return;
   const int hq0 = g * G;
   if (ctx == 0) {
+    // a fused append needs its token inside the context
+    if (p.k_new != nullptr && threadIdx.x == 0 && __ldg(p.new_slots + s) >= 0)
+      flag_status(p.status, PKV_DEV_BAD_SLOT);
     for (int i = threadIdx.x; i < G * D; i += NW * 32)
       p.out[(static_cast<int64_t>(s) * p.num_q_heads + hq0) * D + i] = 0.f;
     return;
@@ -124,6 +128,47 @@ __global__ void __launch_bounds__(NW * 32)
   }
   fence_proxy_async();
   __syncthreads();
+  if (p.k_new != nullptr && part == nparts - 1) {
+    // Fused append: this CTA's partition holds position ctx - 1, the new token;
+    // write its K and V rows for KV head g (16 bytes per thread), then order
+    // the writes before the TMA reads of the block.  Only the slot the block
+    // table gives that position is accepted, so no other CTA reads the row.
+    const int64_t slot = __ldg(p.new_slots + s);
+    if (slot >= 0) {
+      const int32_t blk = sbt[((ctx - 1) >> p.bs_log2) - lb0];
+      const int64_t want =
+          blk < 0 ? -1
+                  : (static_cast<int64_t>(blk) << p.bs_log2) + ((ctx - 1) & ((1 << p.bs_log2) - 1));
+      if (slot != want) {
+        if (threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
+      } else {
+        constexpr int SEGS = D * KV::kBytes / 16;   // 16-byte segments per row
+        const int i = threadIdx.x;
+        if (i < 2 * SEGS) {
+          const bool is_v = i >= SEGS;
+          const int seg = i % SEGS;
+          const int64_t row = static_cast<int64_t>(s) * p.num_kv_heads + g;   // source row
+          uint4 val;
+          if (!F8) {
+            val = __ldg(reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row * SEGS + seg);
+          } else {
+            const float sc = __ldg((is_v ? p.v_scale : p.k_scale) + g);
+            const void* src = is_v ? p.v_new : p.k_new;
+            if (p.new_src_dtype == PKV_F32)
+              val = quant16<float, KV>(static_cast<const float*>(src) + (row * SEGS + seg) * 16, sc);
+            else
+              val = quant16<__nv_bfloat16, KV>(
+                  static_cast<const __nv_bfloat16*>(src) + (row * SEGS + seg) * 16, sc);
+          }
+          uint8_t* cache = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
+          *reinterpret_cast<uint4*>(cache + (slot * p.num_kv_heads + g) * (SEGS * 16) + seg * 16) =
+              val;
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncthreads();
+  }
 
   // q^T as B fragments: b0 = q[gid][k 2tig..], b1 = q[gid][k 2tig+8..] of each k-step
   // (FP8: logical k 2tig+e (+8) of k-step ks <-> dim 32*tig + 4*ks + e (+2)).

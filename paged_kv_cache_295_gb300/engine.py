@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, FP8_E4M3, INT8, Pool, copy_blocks, paged_attention_decode,
+from . import (BF16, F32, FP8_E4M3, INT8, Pool, copy_blocks, paged_attention_decode, paged_attention_decode_append,
                paged_attention_prefill, reshape_and_cache, swap_blocks, workspace_bytes)
 
 
@@ -119,6 +119,20 @@ class PagedKVCache:
                                       k_scale=ks, v_scale=vs, workspace=workspace,
                                       partition=partition, device_status=device_status,
                                       stream=stream)
+
+    def append_attend(self, layer, q, k_new, v_new, slot_mapping, block_tables, context_lens,
+                      max_context_len, out=None, workspace=None, partition=0, device_status=None,
+                      stream=None):
+        """One decode step of one layer: append each sequence's new token and
+        attend, fused into the decode kernel where it runs the transposed
+        tensor-core path."""
+        ks = None if self.k_scale is None else self.k_scale[layer]
+        vs = None if self.v_scale is None else self.v_scale[layer]
+        return paged_attention_decode_append(q, k_new, v_new, slot_mapping, self.k_cache(layer),
+                                             self.v_cache(layer), block_tables, context_lens,
+                                             self.scale, max_context_len, out=out, k_scale=ks,
+                                             v_scale=vs, workspace=workspace, partition=partition,
+                                             device_status=device_status, stream=stream)
 
     def prefill(self, layer, q, query_start, block_tables, context_lens, max_query_len,
                 max_context_len, causal=True, out=None, device_status=None, stream=None):
