@@ -328,20 +328,26 @@ class DeviceStep:
             out[a:b] = (x * kh if kh is not None else x).to(self.src_dt)
         return out
 
+    def fused(self) -> bool:
+        """The append runs inside the decode kernel (the transposed kernel)."""
+        return decode_kernel_name(self.w) == "paged_decode_mma2_kernel"
+
     def launches_per_step(self) -> int:
-        """Our kernels per step: per layer one append, one decode, one reduce if split."""
-        return self.w.num_layers * (2 + (1 if self.max_parts > 1 else 0))
+        """Our kernels per step: per layer one decode (with the append fused in,
+        else an append kernel too) and one reduce if split."""
+        return self.w.num_layers * ((1 if self.fused() else 2) + (1 if self.max_parts > 1 else 0))
 
     def run(self, i, ev=None):
-        """One decode step (every layer); ``ev`` = (start, end) event lists per layer."""
+        """One decode step (every layer) through paged_attention_decode_append;
+        ``ev`` = (start, end) event lists per layer around that call."""
         eng, k = self.eng, i % len(self.q[0])
         for layer in range(self.w.num_layers):
-            eng.append(layer, self.kn[layer][k], self.vn[layer][k], self.slots,
-                       device_status=self.status)
             if ev is not None:
                 ev[0][layer].record()
-            eng.attend(layer, self.q[layer][k], self.tables, self.ctx, self.max_ctx, out=self.out,
-                       workspace=self.ws, partition=self.partition, device_status=self.status)
+            eng.append_attend(layer, self.q[layer][k], self.kn[layer][k], self.vn[layer][k],
+                              self.slots, self.tables, self.ctx, self.max_ctx, out=self.out,
+                              workspace=self.ws, partition=self.partition,
+                              device_status=self.status)
             if ev is not None:
                 ev[1][layer].record()
 
@@ -418,7 +424,8 @@ def run_ours(args):
     kv_uni = kv_bytes_unique(w, st.lens) * L
     total_kv = sum_over_ranks(kv_log * K, world, dev)
     value = total_kv / dt / 1e9
-    attn_bytes = attention_alg_bytes(w, st.lens)
+    # the timed call appends too: its rows count (0.04 % of the 7B layer's bytes)
+    attn_bytes = attention_alg_bytes(w, st.lens) + append_alg_bytes(w)
     attn_avg = statistics.fmean(attn_s)
     peak, peak_src = measured_peaks()
     achieved = attn_bytes / attn_avg / 1e9
@@ -449,6 +456,7 @@ def run_ours(args):
         "decode_tokens_per_s": round(world * w.num_seqs * K / dt, 1),
         "attention_us_per_layer": round(attn_avg * 1e6, 3),
         "append_plus_attention_us_per_layer": round(dt_local / K / L * 1e6, 3),
+        "append": "fused into the decode kernel" if st.fused() else "append kernel, then decode",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
@@ -551,9 +559,9 @@ def run_e2e(st, args, dev, world):
             q_d[l].copy_(q_h[l][k], non_blocking=True)
             kn_d[l].copy_(kn_h[l][k], non_blocking=True)
             vn_d[l].copy_(vn_h[l][k], non_blocking=True)
-            st.eng.append(l, kn_d[l], vn_d[l], slots_d)
-            st.eng.attend(l, q_d[l], tables_d, lens_d, st.max_ctx, out=st.out, workspace=st.ws,
-                          partition=st.partition)
+            st.eng.append_attend(l, q_d[l], kn_d[l], vn_d[l], slots_d, tables_d, lens_d,
+                                 st.max_ctx, out=st.out, workspace=st.ws,
+                                 partition=st.partition)
         out_h.copy_(st.out, non_blocking=True)
         stream.synchronize()
 
@@ -567,8 +575,8 @@ def run_e2e(st, args, dev, world):
     dt = max_over_ranks(time.perf_counter() - t, world, dev)
     kv = sum_over_ranks(kv_bytes_logical(w, st.lens) * L * n, world, dev)
     eager = {"value": round(kv / dt / 1e9, 2), "ms_per_step": round(dt / n * 1e3, 5),
-             "calls": "per step: pool tables, torch copies, reshape_and_cache and "
-                      "paged_attention_decode per layer, D2H, sync"}
+             "calls": "per step: pool tables, torch copies, paged_attention_decode_append "
+                      "per layer, D2H, sync"}
 
     # the same step as one public call: decode_graph_step_host on a captured graph
     import paged_kv_cache_295_gb300 as pkv
