@@ -329,8 +329,9 @@ class DeviceStep:
         return out
 
     def fused(self) -> bool:
-        """The append runs inside the decode kernel (the transposed kernel)."""
-        return decode_kernel_name(self.w) == "paged_decode_mma2_kernel"
+        """The append runs inside the decode kernel (the transposed kernel, 16-bit
+        caches); 8-bit caches run the append kernel first."""
+        return decode_kernel_name(self.w) == "paged_decode_mma2_kernel" and self.w.kv_dtype == "bf16"
 
     def launches_per_step(self) -> int:
         """Our kernels per step: per layer one decode (with the append fused in,

@@ -341,14 +341,15 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
  * caches), slot_mapping device [num_seqs] int64.  slot_mapping[s] must be the
  * slot of position context_lens[s] - 1 (the appended token is the last one
  * attended), or negative for no append.
- * Where the transposed tensor-core kernel runs (bf16, FP8 and INT8 caches,
- * head_dim 128, and bf16 64; G <= 8; block_size >= 8), that kernel writes
- * each sequence's new row for its KV head before it reads the block, in the
- * same launch, with the append kernel's exact rounding.  A slot that is not
- * the block table's slot for position context_lens[s] - 1 (or a context of
- * 0 with a slot) is not written and flags PKV_DEV_BAD_SLOT, and the
- * attention then reads the cache as it was.  Elsewhere the call runs the two
- * kernels.  Arguments and errors otherwise as the two calls'. */
+ * Where the transposed tensor-core kernel runs on a bf16 cache (head_dim 64
+ * or 128, G <= 8, block_size >= 8), that kernel copies each sequence's new
+ * row for its KV head into the cache before it reads the block, in the same
+ * launch.  A slot that is not the block table's slot for position
+ * context_lens[s] - 1 (or a context of 0 with a slot) is then not written and
+ * flags PKV_DEV_BAD_SLOT, and the attention reads the cache as it was.
+ * Elsewhere (8-bit caches, whose quantisation stays in the append kernel, and
+ * the other decode kernels) the call runs the two kernels in order.
+ * Arguments and errors otherwise as the two calls'. */
 pkv_status paged_attention_decode_append(
     const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
     int32_t src_dtype, void* k_cache, void* v_cache, const int32_t* block_tables,

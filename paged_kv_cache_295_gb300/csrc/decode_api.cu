@@ -244,7 +244,11 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   if (fa) {
-    if (use_mma2) {   // the transposed kernel writes the new rows itself
+    // The transposed kernel copies 16-bit rows itself.  8-bit caches keep the
+    // append kernel: quantising in front of a warp's first copy cost more on
+    // the ragged FP8 step (871.7 against 852.9 + the append, us per layer) and
+    // was even on the INT8 layer.
+    if (use_mma2 && kv_dtype == PKV_BF16) {
       p.k_new = fa->k_new;
       p.v_new = fa->v_new;
       p.new_slots = fa->slots;

@@ -30,7 +30,6 @@
 #include <type_traits>
 
 #include "decode_mma_fp8.cuh"
-#include "quant.cuh"
 
 namespace pkv {
 
@@ -60,6 +59,40 @@ struct Mma2Smem {
     return 1024 + static_cast<size_t>(NW) * kWarpBytes + static_cast<size_t>(table_entries) * 4;
   }
 };
+
+// Fused append (16-bit caches): the new token of sequence s, KV head g, is at
+// position ctx - 1, inside this CTA's last chunk.  One warp copies its K and V
+// rows (16 bytes per lane) into the cache and orders the writes before that
+// warp's TMA reads.  Only the slot the block table gives that position is
+// accepted, so no other CTA reads the row.
+template <int D>
+__device__ __forceinline__ void fused_append_row16(const DecodeParams& p, int s, int g, int ctx,
+                                                   int lb0, const int32_t* sbt, int lane) {
+  const int64_t slot = __ldg(p.new_slots + s);
+  if (slot >= 0) {
+    const int32_t blk = sbt[((ctx - 1) >> p.bs_log2) - lb0];
+    const int64_t want =
+        blk < 0 ? -1
+                : (static_cast<int64_t>(blk) << p.bs_log2) + ((ctx - 1) & ((1 << p.bs_log2) - 1));
+    if (slot != want) {
+      if (lane == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
+    } else {
+      constexpr int SEGS = D * 2 / 16;   // 16-byte segments per row
+      static_assert(2 * SEGS <= 32, "one warp copies the K and V rows");
+      if (lane < 2 * SEGS) {
+        const bool is_v = lane >= SEGS;
+        const int seg = lane % SEGS;
+        const int64_t row = static_cast<int64_t>(s) * p.num_kv_heads + g;
+        const uint4 val =
+            __ldg(reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row * SEGS + seg);
+        uint8_t* cache = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
+        *reinterpret_cast<uint4*>(cache + (slot * p.num_kv_heads + g) * (SEGS * 16) + seg * 16) = val;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  __syncwarp();
+}
 
 // Largest log2 gap between a head's reference max and a chunk's max before
 // the running state is rescaled (p = 2^(s - m) < 2^8 in the P operands).
@@ -128,47 +161,6 @@ __global__ void __launch_bounds__(NW * 32)
   }
   fence_proxy_async();
   __syncthreads();
-  if (p.k_new != nullptr && part == nparts - 1) {
-    // Fused append: this CTA's partition holds position ctx - 1, the new token;
-    // write its K and V rows for KV head g (16 bytes per thread), then order
-    // the writes before the TMA reads of the block.  Only the slot the block
-    // table gives that position is accepted, so no other CTA reads the row.
-    const int64_t slot = __ldg(p.new_slots + s);
-    if (slot >= 0) {
-      const int32_t blk = sbt[((ctx - 1) >> p.bs_log2) - lb0];
-      const int64_t want =
-          blk < 0 ? -1
-                  : (static_cast<int64_t>(blk) << p.bs_log2) + ((ctx - 1) & ((1 << p.bs_log2) - 1));
-      if (slot != want) {
-        if (threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
-      } else {
-        constexpr int SEGS = D * KV::kBytes / 16;   // 16-byte segments per row
-        const int i = threadIdx.x;
-        if (i < 2 * SEGS) {
-          const bool is_v = i >= SEGS;
-          const int seg = i % SEGS;
-          const int64_t row = static_cast<int64_t>(s) * p.num_kv_heads + g;   // source row
-          uint4 val;
-          if (!F8) {
-            val = __ldg(reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row * SEGS + seg);
-          } else {
-            const float sc = __ldg((is_v ? p.v_scale : p.k_scale) + g);
-            const void* src = is_v ? p.v_new : p.k_new;
-            if (p.new_src_dtype == PKV_F32)
-              val = quant16<float, KV>(static_cast<const float*>(src) + (row * SEGS + seg) * 16, sc);
-            else
-              val = quant16<__nv_bfloat16, KV>(
-                  static_cast<const __nv_bfloat16*>(src) + (row * SEGS + seg) * 16, sc);
-          }
-          uint8_t* cache = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
-          *reinterpret_cast<uint4*>(cache + (slot * p.num_kv_heads + g) * (SEGS * 16) + seg * 16) =
-              val;
-        }
-      }
-    }
-    asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    __syncthreads();
-  }
 
   // q^T as B fragments: b0 = q[gid][k 2tig..], b1 = q[gid][k 2tig+8..] of each k-step
   // (FP8: logical k 2tig+e (+8) of k-step ks <-> dim 32*tig + 4*ks + e (+2)).
@@ -228,6 +220,12 @@ __global__ void __launch_bounds__(NW * 32)
   const int nbox = kMmaChunk / box_rows;
   bool alive = true;
 
+  // Fused append (16-bit caches): the partition's last chunk holds position
+  // ctx - 1, the new token; the warp that owns that chunk copies the token's
+  // rows before its first copy, while the other warps start streaming.
+  const bool fuse_here = !F8 && p.k_new != nullptr && part == nparts - 1 && my_n > 0 &&
+                         warp == (nchunks - 1) % NW;
+
   // Lane 0 arms the stage's barrier and loads K, lane 1 loads V (in parallel).
   auto issue = [&](int it) {
     if (it >= my_n || lane > 1) return;
@@ -258,6 +256,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
 
+  if (!F8 && fuse_here) fused_append_row16<D>(p, s, g, ctx, lb0, sbt, lane);   // warp-uniform
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) issue(st);
 
