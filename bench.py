@@ -232,6 +232,22 @@ def append_alg_bytes(w) -> int:
         w.num_seqs * 8
 
 
+# layers of the model each single-layer workload is shaped after
+MODEL_LAYERS = {"llama7b_layer_bf16": ("LLaMA-7B", 32), "llama7b_layer_int8": ("LLaMA-7B", 32),
+                "llama70b_gqa8_bf16": ("LLaMA-70B", 80)}
+
+
+def model_tokens_per_s(w, step_s_per_layer):
+    """Decode tokens/s of the whole model the layer is shaped after: the batch
+    over (per-layer step time x the model's layers); attention and append only,
+    extrapolated from one layer (None for workloads that are not one layer)."""
+    if w.name not in MODEL_LAYERS:
+        return None
+    model, layers = MODEL_LAYERS[w.name]
+    return {"value": round(w.num_seqs / (step_s_per_layer * layers), 1), "model": model,
+            "layers": layers, "note": "extrapolated: one layer's append + attention x layers"}
+
+
 def decode_kernel_name(w) -> str:
     """The decode kernel the library picks for this workload's shape."""
     forced = os.environ.get("PKV_DECODE_PATH")
@@ -457,7 +473,10 @@ def run_ours(args):
         "value_unique_gbs": round(sum_over_ranks(kv_uni * K, world, dev) / dt / 1e9, 2),
         "decode_tokens_per_s": round(world * w.num_seqs * K / dt, 1),
         "attention_us_per_layer": round(attn_avg * 1e6, 3),
+        "attention_us_p10_median_p90": [round(float(np.percentile(attn_s, q)) * 1e6, 3)
+                                        for q in (10, 50, 90)],
         "append_plus_attention_us_per_layer": round(dt_local / K / L * 1e6, 3),
+        "decode_tokens_per_s_model": model_tokens_per_s(w, dt_local / K / L),
         "append": "fused into the decode kernel" if st.fused() else "append kernel, then decode",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

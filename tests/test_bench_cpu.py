@@ -26,3 +26,12 @@ def test_prefill_workloads_respect_the_chunked_scheduler_limits():
         if w.chunk_tokens:
             assert (n == w.chunk_tokens).all() and n.sum() <= 8192
             assert ((ctx - n) % w.chunk_tokens == 0).all()
+
+
+def test_model_tokens_per_s_extrapolates_from_one_layer():
+    import bench
+    import workloads as W
+    r = bench.model_tokens_per_s(W.LLAMA7B_LAYER, 200e-6)      # 200 us per layer step
+    assert r["layers"] == 32 and abs(r["value"] - 32 / (200e-6 * 32)) < 1e-6
+    assert bench.model_tokens_per_s(W.LLAMA70B_GQA, 200e-6)["layers"] == 80
+    assert bench.model_tokens_per_s(W.RAGGED_FP8, 1e-3) is None   # already 32 layers
