@@ -47,6 +47,54 @@ pkv_status pad_rows(const pkv_decode_graph_config& c, int32_t from, int32_t to, 
   return cuda_status(cudaGetLastError());
 }
 
+// One strided host -> device copy: `rows` rows of `row_bytes`, the source rows
+// `src_stride` apart in mapped page-locked host memory, the destination rows
+// `dst_stride` apart on the device.
+struct StageSeg {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t row_bytes, src_stride, dst_stride;
+  int32_t rows;
+};
+constexpr int kStageSegs = 6;
+struct StageArgs {
+  StageSeg seg[kStageSegs];
+};
+
+// The step's inputs gathered in one launch (blockIdx.y = segment): a kernel
+// reading host memory over the host link replaces one DMA copy per buffer.
+// 16-byte words where the segment's addresses and sizes allow, else 4-byte.
+__global__ void stage_inputs_kernel(const StageArgs a) {
+  const StageSeg sg = a.seg[blockIdx.y];
+  const bool v16 = ((reinterpret_cast<uintptr_t>(sg.src) | reinterpret_cast<uintptr_t>(sg.dst) |
+                     static_cast<uintptr_t>(sg.row_bytes) | static_cast<uintptr_t>(sg.src_stride) |
+                     static_cast<uintptr_t>(sg.dst_stride)) & 15u) == 0;
+  const int64_t unit = v16 ? 16 : 4;
+  const int64_t per_row = sg.row_bytes / unit;
+  const int64_t total = per_row * sg.rows;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row, k = i % per_row;
+    const uint8_t* src = sg.src + r * sg.src_stride + k * unit;
+    uint8_t* dst = sg.dst + r * sg.dst_stride + k * unit;
+    if (v16)
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+  }
+}
+
+// Device address of page-locked host memory, or nullptr when the pointer is
+// not mapped (pageable memory, or no mapping): the caller then copies instead.
+const uint8_t* mapped(const void* host) {
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<const uint8_t*>(d);
+}
+
 // The step for a batch of B rows: every layer's append and decode (one fused
 // call per layer; one launch per layer where the transposed kernel runs).
 pkv_status record_step(const pkv_decode_graph& g, int32_t B, cudaStream_t st) {
@@ -220,7 +268,31 @@ extern "C" pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool
   const size_t kvrow = static_cast<size_t>(c.num_kv_heads) * c.head_dim * elem_bytes(c.src_dtype);
   const size_t orow = static_cast<size_t>(c.num_q_heads) * c.head_dim * sizeof(float);
   const size_t L = static_cast<size_t>(c.num_layers);
-  bool ok =
+  // Inputs: one staging kernel when every host buffer is mapped page-locked
+  // memory, else one copy per buffer.
+  const uint8_t* m_tab = mapped(tables);
+  const uint8_t* m_q = mapped(q_host);
+  const uint8_t* m_k = mapped(k_new_host);
+  const uint8_t* m_v = mapped(v_new_host);
+  const uint8_t* m_sl = mapped(slots_host);
+  if (m_tab && m_q && m_k && m_v && m_sl) {
+    StageArgs a{};
+    const int64_t tb = static_cast<int64_t>(batch) * mb * 4;
+    a.seg[0] = {m_tab, reinterpret_cast<uint8_t*>(c.block_tables), tb, tb, tb, 1};
+    const int64_t lb = static_cast<int64_t>(batch) * 4;
+    a.seg[1] = {m_tab + static_cast<size_t>(Bmax) * mb * sizeof(int32_t),
+                reinterpret_cast<uint8_t*>(c.context_lens), lb, lb, lb, 1};
+    const int64_t sb = static_cast<int64_t>(batch) * 8;
+    a.seg[2] = {m_sl, reinterpret_cast<uint8_t*>(c.slot_mapping), sb, sb, sb, 1};
+    const int64_t qr = static_cast<int64_t>(qrow), kr = static_cast<int64_t>(kvrow);
+    const int64_t qb = batch * qr, kb = batch * kr;
+    a.seg[3] = {m_q, static_cast<uint8_t*>(c.q), qb, qb, Bmax * qr, static_cast<int32_t>(L)};
+    a.seg[4] = {m_k, static_cast<uint8_t*>(c.k_new), kb, kb, Bmax * kr, static_cast<int32_t>(L)};
+    a.seg[5] = {m_v, static_cast<uint8_t*>(c.v_new), kb, kb, Bmax * kr, static_cast<int32_t>(L)};
+    stage_inputs_kernel<<<dim3(2 * device_sm_count(), kStageSegs), 256, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  } else {
+    bool ok =
       cudaMemcpyAsync(c.block_tables, tables, static_cast<size_t>(batch) * mb * sizeof(int32_t),
                       cudaMemcpyHostToDevice, st) == cudaSuccess &&
       cudaMemcpyAsync(c.context_lens, lens, static_cast<size_t>(batch) * sizeof(int32_t),
@@ -233,9 +305,10 @@ extern "C" pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool
                         cudaMemcpyHostToDevice, st) == cudaSuccess &&
       cudaMemcpy2DAsync(c.v_new, Bmax * kvrow, v_new_host, batch * kvrow, batch * kvrow, L,
                         cudaMemcpyHostToDevice, st) == cudaSuccess;
-  if (!ok) {
-    cudaGetLastError();
-    return PKV_ERR_CUDA;
+    if (!ok) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
   }
   s = decode_graph_launch(g, batch, nullptr, stream);
   if (s != PKV_OK) return s;
