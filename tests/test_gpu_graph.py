@@ -140,3 +140,29 @@ def test_step_from_host_memory_equals_graph_launch(lib):
         g.step_host(eng.pool, [0, 99], q_h[:, :2].contiguous(), kn_h[:, :2].contiguous(),
                     vn_h[:, :2].contiguous(), slots_h[:2].contiguous(), out_h[:, :2].contiguous())
     g.close()
+
+
+def test_step_from_pageable_host_memory_equals_page_locked(lib):
+    """Page-locked inputs are gathered by the staging kernel; pageable ones go
+    through one copy per buffer.  Both give the same cache and output bytes."""
+    import torch
+    import paged_kv_cache_295_gb300 as pkv
+    results = []
+    for pinned in (True, False):
+        eng, op, host, r = _setup(seed=4)
+        L, hq, hkv, d = eng.num_layers, 8, eng.num_kv_heads, eng.head_dim
+        g = pkv.DecodeGraph(eng, hq, 16, [1, 2, 4, 8])
+        sids = [1, 4, 6, 7]
+        slots = eng.pool.append_slots(sids)
+        r2 = np.random.default_rng(11)
+        mk = lambda shape: torch.from_numpy(W_store(r2, shape).view(np.int16)).view(torch.bfloat16)
+        q, kn, vn = mk((L, 4, hq, d)), mk((L, 4, hkv, d)), mk((L, 4, hkv, d))
+        sl = torch.from_numpy(slots)
+        out = torch.empty((L, 4, hq, d), dtype=torch.float32)
+        if pinned:
+            q, kn, vn, sl, out = (x.pin_memory() for x in (q, kn, vn, sl, out))
+        g.step_host(eng.pool, sids, q, kn, vn, sl, out)
+        results.append((out.numpy().copy(), eng.storage.view(torch.int16).cpu().numpy()))
+        g.close()
+    assert results[0][0].tobytes() == results[1][0].tobytes()
+    assert results[0][1].tobytes() == results[1][1].tobytes()
