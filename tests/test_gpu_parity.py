@@ -80,6 +80,9 @@ SMALL = {
                                                 seed=20, ctx_law="fixed"), [2, 31, 900]),
     "d64_int8_g4_bs8": (W.DecodeWorkload("i8d64", 3, 8, 2, 64, 8, "int8", "bf16", seed=21,
                                          ctx_law="fixed"), [3, 64, 513]),
+    # the largest block size: contexts inside, at and across 4096-token blocks
+    "d128_bf16_g4_bs4096": (W.DecodeWorkload("bs4096", 4, 8, 2, 128, 4096, "bf16", "bf16",
+                                             seed=22, ctx_law="fixed"), [1, 4096, 4097, 9000]),
 }
 
 

@@ -34,6 +34,7 @@ CASES = [  # (Hq, Hkv, bs, chunk lens, cached prefix lens)
     (16, 1, 32, [9, 40], [64, 3]),                     # G=16 (MQA-like), 8 tokens per tile
     (6, 2, 16, [50, 43], [7, 200]),                    # G=3: 42 tokens x 3 heads = 126 rows
     (4, 4, 64, [128, 0, 1], [128, 5, 0]),              # an empty chunk; exact tile sizes
+    (8, 2, 4096, [70, 300], [4090, 4000]),             # the largest block: chunks across it
 ]
 
 
