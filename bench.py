@@ -234,6 +234,7 @@ def append_alg_bytes(w) -> int:
 
 # layers of the model each single-layer workload is shaped after
 MODEL_LAYERS = {"llama7b_layer_bf16": ("LLaMA-7B", 32), "llama7b_layer_int8": ("LLaMA-7B", 32),
+                "llama7b_layer_fp8": ("LLaMA-7B", 32),
                 "llama70b_gqa8_bf16": ("LLaMA-70B", 80)}
 
 

@@ -40,7 +40,8 @@ def _sample_seqs(w, lens):
     return sorted(pick)
 
 
-@pytest.mark.parametrize("name", [w.name for w in W.ALL] + ["llama7b_layer_int8"])
+@pytest.mark.parametrize("name", [w.name for w in W.ALL] + ["llama7b_layer_int8",
+                                                             "llama7b_layer_fp8"])
 def test_fullsize_sampled_parity(lib, name):
     import torch
     import bench
@@ -54,10 +55,11 @@ def test_fullsize_sampled_parity(lib, name):
     bs = w.block_size
     checked = 0
     for layer in layers:
-        # the bench's step for this layer: append the new token, attend
-        eng.append(layer, st.kn[layer][0], st.vn[layer][0], st.slots, device_status=st.status)
-        out = eng.attend(layer, st.q[layer][0], st.tables, st.ctx, st.max_ctx, workspace=st.ws,
-                         device_status=st.status)
+        # the bench's step for this layer: append the new token and attend, as
+        # the bench times it (one paged_attention_decode_append call)
+        out = eng.append_attend(layer, st.q[layer][0], st.kn[layer][0], st.vn[layer][0],
+                                st.slots, st.tables, st.ctx, st.max_ctx, workspace=st.ws,
+                                device_status=st.status)
         torch.cuda.synchronize()
         assert int(st.status.item()) == 0
         got = out.cpu().numpy()

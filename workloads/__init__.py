@@ -80,11 +80,15 @@ RAGGED_FP8_LAYER = DecodeWorkload("ragged_fp8_1layer", 256, 32, 32, 128, 16, FP8
 # The 7B layer with an INT8 cache (section 3.1 symmetric codes, per-head scale).
 LLAMA7B_LAYER_INT8 = DecodeWorkload("llama7b_layer_int8", 32, 32, 32, 128, 16, INT8, BF16,
                                     seed=1, ctx_lo=512, ctx_hi=4096)
+# The same layer with an FP8-E4M3 cache: the in-register dequantisation measured
+# on plain (unshared) contexts.
+LLAMA7B_LAYER_FP8 = DecodeWorkload("llama7b_layer_fp8", 32, 32, 32, 128, 16, FP8, BF16,
+                                   seed=1, ctx_lo=512, ctx_hi=4096)
 # Small-batch decode of all 32 layers of the 7B shape with short contexts, where
 # launch cost matters: timed as a CUDA-graph replay (and eagerly, for contrast).
 LLAMA7B_B8_GRAPH = DecodeWorkload("llama7b_32layer_b8_graph", 8, 32, 32, 128, 16, BF16, BF16,
                                   seed=9, num_layers=32, ctx_lo=256, ctx_hi=1024, graph=True)
-EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8, LLAMA7B_B8_GRAPH)
+EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8, LLAMA7B_LAYER_FP8, LLAMA7B_B8_GRAPH)
 
 
 @dataclass(frozen=True)
