@@ -47,12 +47,15 @@ __device__ __forceinline__ void byte4_to_f16x2x2(uint32_t w, uint32_t& lo, uint3
     e4m3x4_to_f16x2x2(w, lo, hi);
 }
 
-template <typename KV, int D, int NW, int STAGES>
+// Shared memory of one CTA: per warp a ring of STAGES chunks of CH tokens (K
+// then V, each kBoxes tiles of [CH rows][128 B]) and a 1 KiB scratch for P^T.
+template <typename KV, int D, int NW, int STAGES, int CH>
 struct Mma2Smem {
   static constexpr int kBoxes = D * KV::kBytes / 128;             // 128-byte TMA boxes per row
-  static constexpr int kBoxBytes = kMmaChunk * 128;               // [16 rows][128 B]
+  static constexpr int kBoxBytes = CH * 128;                      // [CH rows][128 B]
   static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;      // K + V
-  static constexpr int kScratch = 512;                            // P^T hi + lo (8 x 16 x 2 B each)
+  static constexpr int kScratch = 8 * CH * 2 * 2;                 // P^T hi + lo, [8][CH] each
+  static_assert(kScratch <= 1024, "P^T scratch fits its 1 KiB");
   static constexpr int kWarpBytes = STAGES * kStageBytes + 1024;  // + scratch, 1 KiB aligned
   static_assert(STAGES * kStageBytes >= 8 * (D + 3) * 4, "combine area fits a warp ring");
   static size_t bytes(int table_entries) {
@@ -98,14 +101,20 @@ __device__ __forceinline__ void fused_append_row16(const DecodeParams& p, int s,
 // the running state is rescaled (p = 2^(s - m) < 2^8 in the P operands).
 constexpr float kLazyLog2 = 8.f;
 
-template <typename KV, int D, bool QF32, int NW, int STAGES>
+template <typename KV, int D, bool QF32, int NW, int STAGES, int CH>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma2_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const MmaParams mp) {
-  using SM = Mma2Smem<KV, D, NW, STAGES>;
+  using SM = Mma2Smem<KV, D, NW, STAGES, CH>;
   constexpr bool F8 = KV::kBytes == 1;                      // 8-bit codes (FP8 or INT8)
   constexpr bool I8 = std::is_same<KV, INT8>::value;
   static_assert(!F8 || D == 128, "the 8-bit path is built for head_dim 128");
+  // Tokens per chunk: 16 for 16-bit rows; 32 (two 16-token row tiles, RT = 2)
+  // for 8-bit rows, so a chunk carries the same 8 KiB and the per-chunk work
+  // (barrier wait, copies, softmax reductions, P^T round trip) is paid once
+  // per 32 tokens.
+  constexpr int RT = CH / 16;
+  static_assert(CH == 16 || (F8 && CH == 32), "16-token chunks, or 32 for 8-bit rows");
   constexpr int H = SM::kBoxes;
   constexpr int KSTEPS = D / 16;   // QK k-steps
   constexpr int MT = D / 16;       // PV m-tiles (16 output dims each)
@@ -212,12 +221,12 @@ __global__ void __launch_bounds__(NW * 32)
   const float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
 
   uint8_t* ring = smem + warp * SM::kWarpBytes;
-  uint8_t* scratch = ring + STAGES * SM::kStageBytes;      // P^T hi [8][16], lo [8][16]
+  uint8_t* scratch = ring + STAGES * SM::kStageBytes;      // P^T hi [8][CH], lo [8][CH]
   const uint32_t ring_a = smem_u32(ring);
-  const int nchunks = (t_end - t_begin + kMmaChunk - 1) / kMmaChunk;
+  const int nchunks = (t_end - t_begin + CH - 1) / CH;
   const int my_n = warp < nchunks ? (nchunks - warp + NW - 1) / NW : 0;
   const int box_rows = mp.box_rows;
-  const int nbox = kMmaChunk / box_rows;
+  const int nbox = CH / box_rows;
   bool alive = true;
 
   // Fused append (16-bit caches): the partition's last chunk holds position
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(NW * 32)
   auto issue = [&](int it) {
     if (it >= my_n || lane > 1) return;
     const int stage = it % STAGES;
-    const int t0 = t_begin + (warp + it * NW) * kMmaChunk;
+    const int t0 = t_begin + (warp + it * NW) * CH;
     const uint32_t bar = smem_u32(&bars[warp][stage]);
     if (lane == 0) {
       uint32_t bytes = 0;
@@ -272,19 +281,19 @@ __global__ void __launch_bounds__(NW * 32)
         mbar_wait(smem_u32(&bars[warp][k % STAGES]), (k / STAGES) & 1);
       break;
     }
-    const int t0 = t_begin + (warp + it * NW) * kMmaChunk;
-    const int valid = min(kMmaChunk, ctx - t0);
+    const int t0 = t_begin + (warp + it * NW) * CH;
+    const int valid = min(CH, ctx - t0);
     uint8_t* kb = ring + stage * SM::kStageBytes;
     uint8_t* vb = kb + H * SM::kBoxBytes;
-    bool hole = valid < kMmaChunk;
+    bool hole = valid < CH;
     if (!hole) {
       for (int bx = 0; bx < nbox; ++bx)
         if (sbt[((t0 + bx * box_rows) >> p.bs_log2) - lb0] < 0) hole = true;
     }
     if (hole) {   // rows the TMA did not fill become zero
-      for (int i = lane; i < kMmaChunk * 8 * H * 2; i += 32) {
-        const int r = (i >> 3) % kMmaChunk;
-        const int rest = i / (8 * kMmaChunk);
+      for (int i = lane; i < CH * 8 * H * 2; i += 32) {
+        const int r = (i >> 3) % CH;
+        const int rest = i / (8 * CH);
         const int bx = r / box_rows;
         const bool filled = r < valid && sbt[((t0 + bx * box_rows) >> p.bs_log2) - lb0] >= 0;
         if (!filled) {
@@ -297,27 +306,33 @@ __global__ void __launch_bounds__(NW * 32)
     }
     const uint32_t kb_a = smem_u32(kb), vb_a = smem_u32(vb);
 
-    // ---- S^T = K q^T: tokens gid, gid+8 x heads 2tig, 2tig+1 -------------------
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (F8) {
-      uint32_t wa[8], wb[8];   // 32-byte slices [32*tig, +32) of token rows gid, gid+8
-      {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(kb + swz(gid, 2 * tig));
-        const uint4 a1 = *reinterpret_cast<const uint4*>(kb + swz(gid, 2 * tig + 1));
-        const uint4 b0 = *reinterpret_cast<const uint4*>(kb + swz(gid + 8, 2 * tig));
-        const uint4 b1 = *reinterpret_cast<const uint4*>(kb + swz(gid + 8, 2 * tig + 1));
-        wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
-        wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
-        wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
-        wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
-      }
+    // ---- S^T = K q^T: tokens 16rt + gid, 16rt + gid + 8 x heads 2tig, 2tig+1 --------
+    float sacc[RT][4];
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        uint32_t a[4];   // {row gid k, row gid+8 k, row gid k+8, row gid+8 k+8}
-        byte4_to_f16x2x2<KV>(wa[ks], a[0], a[2]);
-        byte4_to_f16x2x2<KV>(wb[ks], a[1], a[3]);
-        mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
-        if (QF32) mma_f16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
+    for (int rt = 0; rt < RT; ++rt) sacc[rt][0] = sacc[rt][1] = sacc[rt][2] = sacc[rt][3] = 0.f;
+    if (F8) {
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt) {
+        uint32_t wa[8], wb[8];   // 32-byte slices [32*tig, +32) of token rows gid, gid+8
+        {
+          const int ra = 16 * rt + gid, rb = ra + 8;
+          const uint4 a0 = *reinterpret_cast<const uint4*>(kb + swz(ra, 2 * tig));
+          const uint4 a1 = *reinterpret_cast<const uint4*>(kb + swz(ra, 2 * tig + 1));
+          const uint4 b0 = *reinterpret_cast<const uint4*>(kb + swz(rb, 2 * tig));
+          const uint4 b1 = *reinterpret_cast<const uint4*>(kb + swz(rb, 2 * tig + 1));
+          wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
+          wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+          wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
+          wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+        }
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          uint32_t a[4];   // {row gid k, row gid+8 k, row gid k+8, row gid+8 k+8}
+          byte4_to_f16x2x2<KV>(wa[ks], a[0], a[2]);
+          byte4_to_f16x2x2<KV>(wb[ks], a[1], a[3]);
+          mma_f16(sacc[rt], a, qb[ks][0], qb[ks][1]);
+          if (QF32) mma_f16(sacc[rt], a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
+        }
       }
     } else {
 #pragma unroll
@@ -327,17 +342,22 @@ __global__ void __launch_bounds__(NW * 32)
         const int u = ((16 * ks) % 64) / 8 + (i >> 1);
         uint32_t a[4];
         ldsm_x4(kb_a + hh * SM::kBoxBytes + swz(r, u), a[0], a[1], a[2], a[3]);
-        mma_bf16(sacc, a, qb[ks][0], qb[ks][1]);
-        if (QF32) mma_bf16(sacc, a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
+        mma_bf16(sacc[0], a, qb[ks][0], qb[ks][1]);
+        if (QF32) mma_bf16(sacc[0], a, qblo[QF32 ? ks : 0][0], qblo[QF32 ? ks : 0][1]);
       }
     }
-    // ---- online softmax (columns = heads 2tig, 2tig+1; rows = tokens gid, gid+8) ----
-    const bool t0ok = gid < valid, t1ok = gid + 8 < valid;
-    sacc[0] = (t0ok && h0ok) ? sacc[0] * sl2 : -CUDART_INF_F;
-    sacc[1] = (t0ok && h1ok) ? sacc[1] * sl2 : -CUDART_INF_F;
-    sacc[2] = (t1ok && h0ok) ? sacc[2] * sl2 : -CUDART_INF_F;
-    sacc[3] = (t1ok && h1ok) ? sacc[3] * sl2 : -CUDART_INF_F;
-    float mx0 = fmaxf(sacc[0], sacc[2]), mx1 = fmaxf(sacc[1], sacc[3]);
+    // ---- online softmax (columns = heads 2tig, 2tig+1; rows = tokens) ------------
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const bool t0ok = 16 * rt + gid < valid, t1ok = 16 * rt + gid + 8 < valid;
+      sacc[rt][0] = (t0ok && h0ok) ? sacc[rt][0] * sl2 : -CUDART_INF_F;
+      sacc[rt][1] = (t0ok && h1ok) ? sacc[rt][1] * sl2 : -CUDART_INF_F;
+      sacc[rt][2] = (t1ok && h0ok) ? sacc[rt][2] * sl2 : -CUDART_INF_F;
+      sacc[rt][3] = (t1ok && h1ok) ? sacc[rt][3] * sl2 : -CUDART_INF_F;
+      mx0 = fmaxf(mx0, fmaxf(sacc[rt][0], sacc[rt][2]));
+      mx1 = fmaxf(mx1, fmaxf(sacc[rt][1], sacc[rt][3]));
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -369,13 +389,7 @@ __global__ void __launch_bounds__(NW * 32)
       m0 = mn0;
       m1 = mn1;
     }
-    const float p00 = h0ok && t0ok ? exp2f(sacc[0] - m0) : 0.f;   // (token gid, head 2tig)
-    const float p01 = h1ok && t0ok ? exp2f(sacc[1] - m1) : 0.f;
-    const float p10 = h0ok && t1ok ? exp2f(sacc[2] - m0) : 0.f;   // (token gid+8, head 2tig)
-    const float p11 = h1ok && t1ok ? exp2f(sacc[3] - m1) : 0.f;
-    l0 += p00 + p10;
-    l1 += p01 + p11;
-    // P^T to B fragments via scratch: [head][token] (hi; lo for 16-bit caches)
+    // P^T to B fragments via scratch: [head][CH tokens] (hi; lo for 16-bit caches)
     {
       auto put = [&](int off, float v, float& psum) {
         if (F8) {
@@ -385,46 +399,66 @@ __global__ void __launch_bounds__(NW * 32)
         } else {
           const __nv_bfloat16 hv = __float2bfloat16_rn(v);
           *reinterpret_cast<__nv_bfloat16*>(scratch + off) = hv;
-          *reinterpret_cast<__nv_bfloat16*>(scratch + 256 + off) =
+          *reinterpret_cast<__nv_bfloat16*>(scratch + 16 * CH + off) =
               __float2bfloat16_rn(v - __bfloat162float(hv));
         }
       };
-      put(((2 * tig) * 16 + gid) * 2, p00, ps0);
-      put(((2 * tig + 1) * 16 + gid) * 2, p01, ps1);
-      put(((2 * tig) * 16 + gid + 8) * 2, p10, ps0);
-      put(((2 * tig + 1) * 16 + gid + 8) * 2, p11, ps1);
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt) {
+        const bool t0ok = 16 * rt + gid < valid, t1ok = 16 * rt + gid + 8 < valid;
+        // (token 16rt + gid (+8), head 2tig (+1)); masked entries are 0
+        const float p00 = h0ok && t0ok ? exp2f(sacc[rt][0] - m0) : 0.f;
+        const float p01 = h1ok && t0ok ? exp2f(sacc[rt][1] - m1) : 0.f;
+        const float p10 = h0ok && t1ok ? exp2f(sacc[rt][2] - m0) : 0.f;
+        const float p11 = h1ok && t1ok ? exp2f(sacc[rt][3] - m1) : 0.f;
+        l0 += p00 + p10;
+        l1 += p01 + p11;
+        const int tk = 16 * rt + gid;
+        put(((2 * tig) * CH + tk) * 2, p00, ps0);
+        put(((2 * tig + 1) * CH + tk) * 2, p01, ps1);
+        put(((2 * tig) * CH + tk + 8) * 2, p10, ps0);
+        put(((2 * tig + 1) * CH + tk + 8) * 2, p11, ps1);
+      }
     }
     __syncwarp();
-    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(scratch + (gid * 16 + 2 * tig) * 2);
-    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(scratch + (gid * 16 + 2 * tig + 8) * 2);
+    uint32_t pb0[RT], pb1[RT];   // P^T of k-step kk: tokens 16kk + 2tig (+8) of head gid
+#pragma unroll
+    for (int kk = 0; kk < RT; ++kk) {
+      pb0[kk] = *reinterpret_cast<const uint32_t*>(scratch + (gid * CH + 16 * kk + 2 * tig) * 2);
+      pb1[kk] = *reinterpret_cast<const uint32_t*>(scratch + (gid * CH + 16 * kk + 2 * tig + 8) * 2);
+    }
     uint32_t pl0 = 0, pl1 = 0;
     if (!F8) {
-      pl0 = *reinterpret_cast<const uint32_t*>(scratch + 256 + (gid * 16 + 2 * tig) * 2);
-      pl1 = *reinterpret_cast<const uint32_t*>(scratch + 256 + (gid * 16 + 2 * tig + 8) * 2);
+      pl0 = *reinterpret_cast<const uint32_t*>(scratch + 16 * CH + (gid * CH + 2 * tig) * 2);
+      pl1 = *reinterpret_cast<const uint32_t*>(scratch + 16 * CH + (gid * CH + 2 * tig + 8) * 2);
     }
 
     // ---- O^T += V^T P^T -----------------------------------------------------------
     if (F8) {
-      // lane owns output dims 16*gid + 2*mt + (0 | 1); tokens 2tig, 2tig+1, 2tig+8, 2tig+9
-      const uint4 va = *reinterpret_cast<const uint4*>(vb + swz(2 * tig, gid));
-      const uint4 vv = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 1, gid));
-      const uint4 vc = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 8, gid));
-      const uint4 vd = *reinterpret_cast<const uint4*>(vb + swz(2 * tig + 9, gid));
-      const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vv.x, vv.y, vv.z, vv.w};
-      const uint32_t Cw[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t lo01 = __byte_perm(A[w], B[w], 0x5140);   // bytes 4w, 4w+1 of 2tig / 2tig+1
-        const uint32_t hi01 = __byte_perm(A[w], B[w], 0x7362);   // bytes 4w+2, 4w+3
-        const uint32_t lo89 = __byte_perm(Cw[w], Dw[w], 0x5140);
-        const uint32_t hi89 = __byte_perm(Cw[w], Dw[w], 0x7362);
-        uint32_t aA[4], aB[4];   // m-tiles 2w and 2w+1
-        byte4_to_f16x2x2<KV>(lo01, aA[0], aA[1]);
-        byte4_to_f16x2x2<KV>(lo89, aA[2], aA[3]);
-        byte4_to_f16x2x2<KV>(hi01, aB[0], aB[1]);
-        byte4_to_f16x2x2<KV>(hi89, aB[2], aB[3]);
-        mma_f16(o[2 * w], aA, pb0, pb1);
-        mma_f16(o[2 * w + 1], aB, pb0, pb1);
+      for (int kk = 0; kk < RT; ++kk) {
+        // lane owns output dims 16*gid + 2*mt + (0 | 1); tokens 16kk + 2tig, +1, +8, +9
+        const int r0 = 16 * kk + 2 * tig;
+        const uint4 va = *reinterpret_cast<const uint4*>(vb + swz(r0, gid));
+        const uint4 vv = *reinterpret_cast<const uint4*>(vb + swz(r0 + 1, gid));
+        const uint4 vc = *reinterpret_cast<const uint4*>(vb + swz(r0 + 8, gid));
+        const uint4 vd = *reinterpret_cast<const uint4*>(vb + swz(r0 + 9, gid));
+        const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vv.x, vv.y, vv.z, vv.w};
+        const uint32_t Cw[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t lo01 = __byte_perm(A[w], B[w], 0x5140);   // bytes 4w, 4w+1 of r0 / r0+1
+          const uint32_t hi01 = __byte_perm(A[w], B[w], 0x7362);   // bytes 4w+2, 4w+3
+          const uint32_t lo89 = __byte_perm(Cw[w], Dw[w], 0x5140);
+          const uint32_t hi89 = __byte_perm(Cw[w], Dw[w], 0x7362);
+          uint32_t aA[4], aB[4];   // m-tiles 2w and 2w+1
+          byte4_to_f16x2x2<KV>(lo01, aA[0], aA[1]);
+          byte4_to_f16x2x2<KV>(lo89, aA[2], aA[3]);
+          byte4_to_f16x2x2<KV>(hi01, aB[0], aB[1]);
+          byte4_to_f16x2x2<KV>(hi89, aB[2], aB[3]);
+          mma_f16(o[2 * w], aA, pb0[kk], pb1[kk]);
+          mma_f16(o[2 * w + 1], aB, pb0[kk], pb1[kk]);
+        }
       }
     } else {
 #pragma unroll
@@ -434,7 +468,7 @@ __global__ void __launch_bounds__(NW * 32)
         const int u = ((16 * mt) % 64) / 8 + (i & 1);
         uint32_t a[4];
         ldsm_x4_t(vb_a + hh * SM::kBoxBytes + swz(r, u), a[0], a[1], a[2], a[3]);
-        mma_bf16(o[mt], a, pb0, pb1);
+        mma_bf16(o[mt], a, pb0[0], pb1[0]);
         mma_bf16(o[mt], a, pl0, pl1);
       }
     }

@@ -77,15 +77,16 @@ pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPara
   return PKV_OK;
 }
 
-// Transposed mma.sync kernel with NW warps and STAGES-deep rings per warp.
-template <typename KV, int D, bool QF32, int NW, int STAGES>
+// Transposed mma.sync kernel with NW warps and STAGES-deep rings of CH-token
+// chunks per warp.
+template <typename KV, int D, bool QF32, int NW, int STAGES, int CH>
 pkv_status launch_mma2_shape(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
                              int num_seqs, cudaStream_t stream) {
-  using SM = Mma2Smem<KV, D, NW, STAGES>;
+  using SM = Mma2Smem<KV, D, NW, STAGES, CH>;
   const int bs = 1 << mp.p.bs_log2;
   const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
   const size_t smem = SM::bytes(table_entries);
-  auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES>;
+  auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES, CH>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
   dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
@@ -94,23 +95,28 @@ pkv_status launch_mma2_shape(const CUtensorMap& tk, const CUtensorMap& tv, const
   return PKV_OK;
 }
 
-// CTA shape of the transposed kernel: 4 warps, each its own TMA ring of
-// 16-token stages.  Rows of 256 bytes (16-bit, head_dim 128; 8 KiB stages) run
-// 2 stages deep so 3 CTAs share an SM (12 warps): while one CTA is in its
-// start-up (context, block table, first TMA round trip) or its epilogue, two
-// others keep streaming.  Rows of 128 bytes (FP8, INT8, or 16-bit head_dim 64;
-// 4 KiB stages) run 3 deep, 4 CTAs per SM (16 warps, the register limit at
-// 128 registers), for the per-chunk conversion and MMA work that dominates
-// small rows.  Measured on the 7B / 70B-shaped layers against 4x3 (2 CTAs per
-// SM): 93.5 -> 97.7 % and 87.7 -> 92.3 % of HBM; 8-bit against 8x3: INT8
-// 68 -> 75 %.
+// Tokens per chunk of the transposed kernel: 32 for 8-bit rows, 16 otherwise.
+int mma2_chunk(int32_t kv_dtype) { return kv_dtype == PKV_BF16 ? 16 : 32; }
+
+// CTA shape of the transposed kernel: 4 warps, each its own TMA ring.
+// 256-byte rows (16-bit, head_dim 128; 8 KiB stages of 16 tokens) run 2 stages
+// deep so 3 CTAs share an SM (12 warps): while one CTA is in its start-up
+// (context, block table, first TMA round trip) or its epilogue, two others
+// keep streaming.  Against 4 x 3 (2 CTAs per SM) the 7B / 70B-shaped layers
+// went from 93.5 to 96.7 % and from 87.7 to 91.3 % of HBM.  8-bit rows take
+// 32-token chunks (8 KiB stages, the same 3 CTAs per SM): against 16-token
+// chunks at 4 CTAs per SM, INT8 121.2 -> 119.2 us per call on the 7B layer and the
+// ragged FP8 layer 853 -> 833 us; 2 CTAs per SM lost 15-20 %.  16-bit
+// head_dim 64 rows (128 bytes) run 4 x 3 with 16-token chunks.
 template <typename KV, int D, bool QF32>
 pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
                        int num_seqs, cudaStream_t stream) {
   if constexpr (D * KV::kBytes == 256)
-    return launch_mma2_shape<KV, D, QF32, 4, 2>(tk, tv, mp, num_seqs, stream);
+    return launch_mma2_shape<KV, D, QF32, 4, 2, 16>(tk, tv, mp, num_seqs, stream);
+  else if constexpr (KV::kBytes == 1)
+    return launch_mma2_shape<KV, D, QF32, 4, 2, 32>(tk, tv, mp, num_seqs, stream);
   else
-    return launch_mma2_shape<KV, D, QF32, 4, 3>(tk, tv, mp, num_seqs, stream);
+    return launch_mma2_shape<KV, D, QF32, 4, 3, 16>(tk, tv, mp, num_seqs, stream);
 }
 
 }  // namespace
@@ -134,7 +140,8 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
                               int head_dim, int64_t num_blocks, bool q_f32, int32_t kv_dtype) {
   const DecodeParams& p = a.p;
   const int bs = 1 << p.bs_log2;
-  MmaParams mp{p, bs < kMmaChunk ? bs : kMmaChunk};
+  const int ch = mma2_chunk(kv_dtype);
+  MmaParams mp{p, bs < ch ? bs : ch};
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * bs;
   const bool byte_codes = kv_dtype != PKV_BF16;
