@@ -648,7 +648,8 @@ class PrefillStep:
         self.n, self.lens = W.prefill_lens(w)
         S, hq, hkv, d, bs = len(self.n), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
         nb = W.prefill_num_blocks(w, self.lens)
-        self.eng = eng = PagedKVCache(1, hkv, d, bs, nb, pkv.BF16, device=device,
+        code = {"bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3}[w.kv_dtype]
+        self.eng = eng = PagedKVCache(1, hkv, d, bs, nb, code, device=device,
                                       initial_free_order=W.free_order(w, nb))
         pre, chk = [], []
         for s in range(S):
@@ -670,6 +671,9 @@ class PrefillStep:
         k_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         v_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         self.q = torch.randn((T, hq, d), generator=gen, device=device).to(torch.bfloat16)
+        if w.kv_dtype == "fp8_e4m3":   # static per-head scales: absmax / 448
+            eng.k_scale[0] = k_src.float().abs().amax(dim=(0, 2)) / 448.0
+            eng.v_scale[0] = v_src.float().abs().amax(dim=(0, 2)) / 448.0
         pre_i = torch.from_numpy(pre_idx).to(device)
         if pre_idx.size:
             eng.append(0, k_src[pre_i], v_src[pre_i],
@@ -837,6 +841,13 @@ class OraclePrefillStep:
                            "bf16")
         self.q = OA.to_f64(W.store(r.standard_normal((int(self.n[s]), w.num_q_heads, d),
                                                      dtype=np.float32), "bf16"), "bf16")
+        if w.kv_dtype == "fp8_e4m3":   # the cache holds E4M3 codes: their dequantised values
+            from oracle import fp8
+            for name in ("K", "V"):
+                x = getattr(self, name).astype(np.float32)
+                sc = (np.abs(x).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+                codes = fp8.encode_f32(x / sc[None, :, None])
+                setattr(self, name, OA.fp8_dequant(codes, sc))
 
     def run(self, i):
         from oracle import prefill as OPF

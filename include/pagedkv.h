@@ -402,7 +402,11 @@ pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_byte
  *                  = 0 and query_start[num_seqs] <= num_tokens; sequence s owns
  *                  rows query_start[s] .. query_start[s+1]-1 (n_s of them, 0
  *                  allowed) of q and out.
- *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, 128] bf16.
+ *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, 128],
+ *                  kv_dtype bf16 or fp8_e4m3.
+ *   k_scale, v_scale : device [num_kv_heads] float32 dequant scales for an FP8
+ *                  cache (value = e4m3 * scale[kv_head], as in decode); else
+ *                  ignored.
  *   block_tables : device [num_seqs, max_blocks_per_seq] int32 (as in decode).
  *   context_lens : device [num_seqs] int32, the context INCLUDING the chunk;
  *                  n_s <= context_lens[s] <= max_context_len.
@@ -414,8 +418,12 @@ pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_byte
  *                  every chunk are not written.
  * Computes out[query_start[s]+i, h, :] = softmax(scale * q . K_g^T) V_g over
  * the visible keys, g = h / G, with float32 accumulation.  Runs on tcgen05
- * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).
- * Supported: head_dim 128, bf16 q and caches, G = num_q_heads / num_kv_heads
+ * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).  FP8
+ * tiles are widened to fp16 in shared memory (exact), so the contractions run
+ * in fp16 (q rounded to fp16, P as fp16 hi + lo), the K scale folded into the
+ * logit scale and the V scale into the output.
+ * Supported: head_dim 128, bf16 q, bf16 or FP8-E4M3 caches (FP8 needs both
+ * scales), G = num_q_heads / num_kv_heads
  * <= 16, block_size a power of two in [8, 4096], 16-byte aligned q, caches and
  * out.  Device-side problems (a bad query_start or context, a bad block) are
  * flagged in device_status; bad rows are skipped or zeroed. */
@@ -427,7 +435,8 @@ pkv_status paged_attention_prefill(const void* q, const int32_t* query_start,
                                    int32_t block_size, int64_t num_blocks,
                                    int32_t max_blocks_per_seq, int32_t max_context_len,
                                    float scale, int32_t causal, int32_t q_dtype,
-                                   int32_t kv_dtype, float* out, int32_t* device_status,
+                                   int32_t kv_dtype, const float* k_scale,
+                                   const float* v_scale, float* out, int32_t* device_status,
                                    pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

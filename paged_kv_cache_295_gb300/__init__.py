@@ -111,7 +111,7 @@ _SIGS = {
     "paged_attention_decode_noalloc": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I64, I32,
                                              I32, FL, I32, I32, P, P, P, I32, P, P]),
     "paged_attention_prefill": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, I64,
-                                      I32, I32, FL, I32, I32, I32, P, P, P]),
+                                      I32, I32, FL, I32, I32, I32, P, P, P, P, P]),
     "pkv_copy_kernel": (I32, [P, P, SZ, P]),
     "pkv_read_kernel": (I32, [P, SZ, P, P]),
     "pkv_read_kernel_sink_floats": (I32, []),
@@ -482,10 +482,11 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_le
 
 def paged_attention_prefill(q, query_start, k_cache, v_cache, block_tables, context_lens,
                             scale, max_query_len, max_context_len, causal=True, out=None,
-                            device_status=None, stream=None):
+                            k_scale=None, v_scale=None, device_status=None, stream=None):
     """Chunked prefill attention; returns ``out [T, Hq, D]`` float32 (allocated
     if None).  ``query_start`` is int32 ``[S + 1]`` on the device;
-    ``max_query_len`` and ``max_context_len`` are host ints (upper bounds)."""
+    ``max_query_len`` and ``max_context_len`` are host ints (upper bounds);
+    ``k_scale`` / ``v_scale`` (``[Hkv]`` float32) for an FP8 cache."""
     torch = _torch()
     T, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
@@ -497,8 +498,8 @@ def paged_attention_prefill(q, query_start, k_cache, v_cache, block_tables, cont
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"),
         _dev(context_lens, "context_lens"), S, T, int(max_query_len), hq, hkv, d, bs, nb,
         block_tables.shape[1], int(max_context_len), float(scale), 1 if causal else 0,
-        _dtype_code(q), _dtype_code(k_cache), _dev(out, "out"),
-        _dev(device_status, "device_status"), _stream(stream))
+        _dtype_code(q), _dtype_code(k_cache), _dev(k_scale, "k_scale"), _dev(v_scale, "v_scale"),
+        _dev(out, "out"), _dev(device_status, "device_status"), _stream(stream))
     _check(st, "paged_attention_prefill")
     return out
 

@@ -24,7 +24,8 @@ extern "C" pkv_status paged_attention_prefill(
     int32_t num_tokens, int32_t max_query_len, int32_t num_q_heads, int32_t num_kv_heads,
     int32_t head_dim, int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
     int32_t max_context_len, float scale, int32_t causal, int32_t q_dtype, int32_t kv_dtype,
-    float* out, int32_t* device_status, pkv_stream_t stream) {
+    const float* k_scale, const float* v_scale, float* out, int32_t* device_status,
+    pkv_stream_t stream) {
   using namespace pkv;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
@@ -33,7 +34,8 @@ extern "C" pkv_status paged_attention_prefill(
   if (causal != 0 && causal != 1) return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  if (head_dim != kPfD || q_dtype != PKV_BF16 || kv_dtype != PKV_BF16 || G > 16)
+  const bool fp8 = kv_dtype == PKV_FP8_E4M3;
+  if (head_dim != kPfD || q_dtype != PKV_BF16 || (kv_dtype != PKV_BF16 && !fp8) || G > 16)
     return PKV_ERR_UNSUPPORTED;
   if (!pow2(block_size) || block_size < 8 || block_size > 4096) return PKV_ERR_UNSUPPORTED;
   if (num_blocks * block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
@@ -50,6 +52,7 @@ extern "C" pkv_status paged_attention_prefill(
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (!encode_fn()) return PKV_ERR_CUDA;
 
@@ -71,20 +74,25 @@ extern "C" pkv_status paged_attention_prefill(
   p.max_context_len = max_context_len;
   p.num_tokens = num_tokens;
   p.qk_scale_log2 = scale * 1.4426950408889634f;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
 
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * block_size;
-  if (!make_map(&tk, k_cache, kPfD, num_kv_heads, rows, p.box_rows, false) ||
-      !make_map(&tv, v_cache, kPfD, num_kv_heads, rows, p.box_rows, false))
+  if (!make_map(&tk, k_cache, kPfD, num_kv_heads, rows, p.box_rows, fp8) ||
+      !make_map(&tv, v_cache, kPfD, num_kv_heads, rows, p.box_rows, fp8))
     return PKV_ERR_CUDA;
 
-  constexpr int STAGES = kPfStages;
-  const size_t smem = PfLayout::bytes(STAGES);
-  auto kern = paged_prefill_tc_kernel<STAGES>;
-  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
-    return PKV_ERR_CUDA;
   const int pairs = (max_query_len + 2 * p.tile_tokens - 1) / (2 * p.tile_tokens);
   dim3 grid(pairs, num_kv_heads, num_seqs);
-  kern<<<grid, kPfThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  auto launch = [&](auto kern, size_t smem) {
+    if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
+      return PKV_ERR_CUDA;
+    kern<<<grid, kPfThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  };
+  if (fp8)
+    return launch(paged_prefill_tc_kernel<kPfStagesFp8, true>,
+                  PfLayout::bytes(kPfStagesFp8, true));
+  return launch(paged_prefill_tc_kernel<kPfStages, false>, PfLayout::bytes(kPfStages, false));
 }

@@ -40,6 +40,7 @@
 // TMEM is released before the CTA exits.
 #pragma once
 
+#include "decode_mma_fp8.cuh"
 #include "decode_tc.cuh"
 
 namespace pkv {
@@ -49,7 +50,9 @@ constexpr int kPfKeys = 64;    // keys per tile (N of QK, K of PV)
 constexpr int kPfD = 128;
 constexpr int kPfThreads = 384;   // 2 softmax warpgroups, K producer, QK issuer, PV issuer,
                                   // V producer
-constexpr int kPfStages = 5;
+constexpr int kPfStages = 5;       // 16-bit caches
+constexpr int kPfStagesFp8 = 3;    // FP8 caches: two stages' room holds the raw tiles
+constexpr int kPfRawBufs = 4;      // FP8 raw tiles in flight per tensor
 
 struct PrefillParams {
   const __nv_bfloat16* q;        // [T, Hq, D]
@@ -69,6 +72,8 @@ struct PrefillParams {
   int32_t max_context_len;       // host bound: larger context_lens are flagged
   int32_t num_tokens;            // T: rows of q and out
   float qk_scale_log2;
+  const float* k_scale;          // FP8 caches: [num_kv_heads] dequant scales
+  const float* v_scale;
 };
 
 // 2^x with the MUFU instruction (relative error about 2^-22; 2^-inf = +0,
@@ -102,29 +107,37 @@ __device__ __forceinline__ void pf_ld64(uint32_t taddr, float* v) {
 }
 
 struct PfLayout {
-  // [P_A: hi 16 KB, lo 16 KB][P_B][stages: K 16 KB, V 16 KB]
+  // [P_A: hi 16 KB, lo 16 KB][P_B][FP8 only: raw tiles, K x4 then V x4, 8 KB each]
+  // [stages: K 16 KB, V 16 KB]
   static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
   static constexpr int kPBuf = 2 * kPPart;             // hi + lo
   static constexpr int kP = 0;                         // P_A, then P_B
   static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
   static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
-  static constexpr int kStages = kP + 2 * kPBuf;       // offset of the stage ring
-  static constexpr size_t bytes(int stages) {
-    return 1024 + static_cast<size_t>(kStages) + static_cast<size_t>(stages) * kStage;
+  static constexpr int kRaw = kP + 2 * kPBuf;          // FP8 raw tiles
+  static constexpr int kRawTile = kPfKeys * 128;       // [64 keys][128 codes]
+  static constexpr int kRawBytes = 2 * kPfRawBufs * kRawTile;   // (K, V) x buffers
+  __host__ __device__ static constexpr int ring(bool fp8) { return kRaw + (fp8 ? kRawBytes : 0); }
+  static constexpr size_t bytes(int stages, bool fp8) {
+    return 1024 + static_cast<size_t>(ring(fp8)) + static_cast<size_t>(stages) * kStage;
   }
 };
 
-template <int STAGES>
+template <int STAGES, bool FP8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   using LY = PfLayout;
+  // FP8 caches: the tiles are widened to fp16 in shared memory, so both
+  // contractions run as f16 MMAs (q and P in fp16 too); bf16 caches run bf16.
+  constexpr int kRing = LY::ring(FP8);
   const int G = p.num_q_heads / p.num_kv_heads;
   const int TQ = p.tile_tokens;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[STAGES], full_v[STAGES], empty[STAGES];
   __shared__ __align__(8) uint64_t s_full[2], s_free[2], q_ready[2], p_full[2], o_done[2], drain[2];
+  __shared__ __align__(8) uint64_t raw_full[2][kPfRawBufs];   // FP8: [K | V][buffer] landed
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -181,6 +194,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(smem_u32(&drain[0]), 1);
     mbar_init(smem_u32(&drain[1]), 1);
+    for (int i = 0; i < 2 * kPfRawBufs; ++i)
+      mbar_init(smem_u32(&raw_full[i / kPfRawBufs][i % kPfRawBufs]), 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -207,8 +222,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool is_v = warp == 11;
     const int box_rows = p.box_rows;
     const int nbox = kPfKeys / box_rows;
-    const int bx = lane >> 1, hh = lane & 1;
     bool flagged = false;
+    if constexpr (!FP8) {
+    const int bx = lane >> 1, hh = lane & 1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % STAGES;
       const int k0 = j * kPfKeys;
@@ -244,10 +260,96 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       __syncwarp();
       if (blk >= 0) {
-        const uint32_t dst = sma + LY::kStages + st * LY::kStage + (is_v ? 2 * LY::kKVHalf : 0) +
+        const uint32_t dst = sma + kRing + st * LY::kStage + (is_v ? 2 * LY::kKVHalf : 0) +
                              hh * LY::kKVHalf + bx * box_rows * 128;
         const int z = (blk << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
         tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, hh * 64, g, z, bar);
+      }
+    }
+    } else {
+      // FP8 caches.  TMA brings a key tile's codes, [64 keys][128 B] in one
+      // 128-byte box per row block, into one of kPfRawBufs raw buffers (lane i
+      // looks up box i's block); the warp widens them to fp16 (exact for E4M3)
+      // into the stage, in the swizzled K-major halves the MMAs read, and
+      // arrives on the stage's barrier.  Tile j + kPfRawBufs's copy goes into
+      // the raw buffer tile j has just left, so kPfRawBufs copies are in flight.
+      const uint32_t raw_a = sma + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
+      const uint8_t* raw_p = sm + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
+      auto issue_raw = [&](int jj) -> uint32_t {   // bit i of the result: box i has data
+        const int kb = jj * kPfKeys + lane * box_rows;
+        int32_t blk = -1;
+        if (lane < nbox && kb < ctx) {
+          const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
+          blk = (b >= 0 && b < p.num_blocks) ? b : -2;
+        }
+        const uint32_t valid = __ballot_sync(0xffffffffu, blk >= 0);
+        if (!is_v && __ballot_sync(0xffffffffu, blk == -2) && !flagged) {
+          if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+          flagged = true;
+        }
+        const uint32_t rbar = smem_u32(&raw_full[is_v ? 1 : 0][jj % kPfRawBufs]);
+        if (lane == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(__popc(valid)) * box_rows * 128u);
+        __syncwarp();
+        if (blk >= 0) {
+          const int z = (blk << p.bs_log2) + (kb & ((1 << p.bs_log2) - 1));
+          tma_load_3d(raw_a + (jj % kPfRawBufs) * LY::kRawTile + lane * box_rows * 128,
+                      is_v ? &tmap_v : &tmap_k, 0, g, z, rbar);
+        }
+        return valid;
+      };
+      uint32_t valids[kPfRawBufs];
+#pragma unroll
+      for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b) : 0u;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % STAGES;
+        const int k0 = j * kPfKeys;
+        if (j >= STAGES) {
+          bool ok = true;
+          if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        // every lane waits, so the copied codes are visible to all of them
+        const int rb = j % kPfRawBufs;
+        if (!__all_sync(0xffffffffu, tc_wait(smem_u32(&raw_full[is_v ? 1 : 0][rb]),
+                                             (j / kPfRawBufs) & 1, abort_flag)))
+          break;
+        const uint8_t* raw = raw_p + rb * LY::kRawTile;
+        uint8_t* dst = sm + kRing + st * LY::kStage + (is_v ? 2 * LY::kKVHalf : 0);
+        // raw row r, 16-byte chunk u = dims 16u .. 16u+15 -> fp16 half u / 4,
+        // 16-byte chunks 2 (u % 4) and 2 (u % 4) + 1 of row r.  Lane = row and
+        // one chunk per step: the swizzle then spreads each step's 32 loads and
+        // 32 stores evenly over the banks (lanes on different chunks of the same
+        // rows, or the two halves 8 KiB apart, would collide 4 ways).
+#pragma unroll 4
+        for (int it = 0; it < (kPfKeys / 32) * 8; ++it) {
+          const int r = (it >> 3) * 32 + lane, u = it & 7;
+          const uint4 c = *reinterpret_cast<const uint4*>(raw + swz(r, u));
+          uint32_t h[8];
+          e4m3x4_to_f16x2x2(c.x, h[0], h[1]);
+          e4m3x4_to_f16x2x2(c.y, h[2], h[3]);
+          e4m3x4_to_f16x2x2(c.z, h[4], h[5]);
+          e4m3x4_to_f16x2x2(c.w, h[6], h[7]);
+          uint8_t* half = dst + (u >> 2) * LY::kKVHalf;
+          const int uu = 2 * (u & 3);
+          *reinterpret_cast<uint4*>(half + swz(r, uu)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(half + swz(r, uu + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_proxy_async();   // the stage's generic writes before the MMAs' reads; the
+        __syncwarp();          // raw buffer's reads before the next copy into it
+        if (lane == 0) {
+          if (!is_v) {
+            uint64_t m = 0;
+            for (int i = 0; i < nbox; ++i) {
+              if (!((valids[rb] >> i) & 1u)) continue;
+              const int rows = min(box_rows, ctx - (k0 + i * box_rows));
+              const uint64_t run = rows >= 64 ? ~0ull : ((1ull << rows) - 1ull);
+              m |= run << (i * box_rows);
+            }
+            key_mask[st] = m;
+          }
+          mbar_arrive(smem_u32(is_v ? &full_v[st] : &full[st]));
+        }
+        if (j + kPfRawBufs < ntiles) valids[rb] = issue_raw(j + kPfRawBufs);
       }
     }
   } else if (warp == 9) {
@@ -256,10 +358,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // buffer is free (the softmax has loaded the previous S; Q is in TMEM
     // before the first).  Its commits cover only its own MMAs (s_full).
     if (lane == 0) {
-      const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, true);
+      const uint32_t idesc_qk = tc_idesc(kPfRows, kPfKeys, false, false, !FP8);
       for (int j = 0; j < ntiles; ++j) {
         if (!tc_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
-        const uint32_t kb = sma + LY::kStages + (j % STAGES) * LY::kStage;
+        const uint32_t kb = sma + kRing + (j % STAGES) * LY::kStage;
         bool ok = true;
         for (int t = 0; t < 2; ++t) {
           if (j >= (t == 0 ? nt_a : nt_b)) continue;
@@ -294,9 +396,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // that reads a stage, the stage is released (its QK finished before its P
     // could be written).
     if (lane == 0) {
-      const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, true);
+      const uint32_t idesc_pv = tc_idesc(kPfRows, kPfD, false, true, !FP8);
       for (int j = 0; j < ntiles; ++j) {
-        const uint32_t vb = sma + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf;
+        const uint32_t vb = sma + kRing + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf;
         if (!tc_wait(smem_u32(&full_v[j % STAGES]), (j / STAGES) & 1, abort_flag)) break;
         bool ok = true;
         for (int t = 0; t < 2; ++t) {
@@ -334,7 +436,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int tl = r / G;
     const bool row_ok = r < TQ * G && tok0 + t * TQ + tl < n;
     {   // this row of Q_t (token tok0 + t*TQ + r/G, head g*G + r%G; 0 past the
-        // chunk) into TMEM, bf16 pairs per column: the A operand of every QK
+        // chunk) into TMEM, bf16 pairs per column (fp16 for FP8 caches): the A
+        // operand of every QK
       float w[64];
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads + g * G + r % G) *
@@ -342,10 +445,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint4 v = row_ok ? src[i] : make_uint4(0, 0, 0, 0);
-        w[4 * i] = __uint_as_float(v.x);
-        w[4 * i + 1] = __uint_as_float(v.y);
-        w[4 * i + 2] = __uint_as_float(v.z);
-        w[4 * i + 3] = __uint_as_float(v.w);
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)   // FP8 caches: the bf16 pair rounded to an fp16 pair
+          w[4 * i + e] = __uint_as_float(
+              FP8 ? pack_f16(__uint_as_float(x[e] << 16), __uint_as_float(x[e] & 0xFFFF0000u))
+                  : x[e]);
       }
       tc_st32(tQ + lane_q, w);
       tc_st32(tQ + lane_q + 32, w + 32);
@@ -355,7 +460,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     const int qpos = ctx - n + tok0 + t * TQ + tl;      // this row's position
     const int last = p.causal ? qpos : ctx - 1;         // last key it sees
-    const float sl2 = p.qk_scale_log2;
+    const float sl2 = FP8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
     const bool pos_scale = sl2 > 0.f;
     uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
     float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units
@@ -429,11 +534,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {   // bf16 hi part, then the bf16 of what it left
+        for (int e = 0; e < 4; ++e) {   // hi part, then what it left (bf16; fp16 for FP8)
           const float a = sv[8 * u + 2 * e], b = sv[8 * u + 2 * e + 1];
-          wh[e] = pack_bf16(a, b);
-          wl[e] = pack_bf16(a - __uint_as_float(wh[e] << 16),
-                            b - __uint_as_float(wh[e] & 0xFFFF0000u));
+          if (FP8) {
+            wh[e] = pack_f16(a, b);
+            const __half2 hv = *reinterpret_cast<const __half2*>(&wh[e]);
+            wl[e] = pack_f16(a - __low2float(hv), b - __high2float(hv));
+          } else {
+            wh[e] = pack_bf16(a, b);
+            wl[e] = pack_bf16(a - __uint_as_float(wh[e] << 16),
+                              b - __uint_as_float(wh[e] & 0xFFFF0000u));
+          }
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
@@ -458,7 +569,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           !tc_wait(smem_u32(&full_v[j % STAGES]), (j / STAGES) & 1, abort_flag))
         alive = false;
       if (zeroer && alive && r < kPfKeys && !((vmask >> r) & 1ull)) {
-        uint8_t* vrow = sm + LY::kStages + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf + r * 128;
+        uint8_t* vrow = sm + kRing + (j % STAGES) * LY::kStage + 2 * LY::kKVHalf + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           *reinterpret_cast<uint4*>(vrow + (u << 4)) = make_uint4(0, 0, 0, 0);
@@ -475,7 +586,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_wait(smem_u32(&o_done[t]), (my_nt - 1) & 1, abort_flag);
     if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // 1 / l, times the V scale for FP8 caches
+      const float inv = l > 0.f ? (FP8 ? __ldg(p.v_scale + g) : 1.f) / l : 0.f;
       float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads +
                              g * G + r % G) * kPfD;
 #pragma unroll

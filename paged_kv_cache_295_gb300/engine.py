@@ -136,10 +136,12 @@ class PagedKVCache:
 
     def prefill(self, layer, q, query_start, block_tables, context_lens, max_query_len,
                 max_context_len, causal=True, out=None, device_status=None, stream=None):
+        ks = None if self.k_scale is None else self.k_scale[layer]
+        vs = None if self.v_scale is None else self.v_scale[layer]
         return paged_attention_prefill(q, query_start, self.k_cache(layer), self.v_cache(layer),
                                        block_tables, context_lens, self.scale, max_query_len,
-                                       max_context_len, causal=causal, out=out,
-                                       device_status=device_status, stream=stream)
+                                       max_context_len, causal=causal, out=out, k_scale=ks,
+                                       v_scale=vs, device_status=device_status, stream=stream)
 
     def workspace_for(self, num_seqs, num_q_heads, max_context_len, partition=0, device="cuda"):
         torch = _torch()

@@ -198,10 +198,11 @@ def run_gpu(case: SmallCase, partition=0, layers=None, tables=None):
     return eng, outs, int(status.item())
 
 
-def make_prefill(w, chunk, prefix, seed=0, bad_block=None):
+def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16"):
     """A seeded chunked-prefill step: the oracle pool and the C pool hand out the
     same slots; the cached prefix rows are placed by the oracle's append; the
-    chunk's rows are left for the GPU append.  Returns (device tensors, the
+    chunk's rows are left for the GPU append.  ``kv`` is the cache type (bf16,
+    or fp8_e4m3 with per-head absmax / 448 scales).  Returns (device tensors, the
     oracle's host arrays after the chunk's append, max chunk, max context)."""
     import torch
     import paged_kv_cache_295_gb300 as pkv
@@ -210,8 +211,8 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None):
     S, hq, hkv, d, bs = len(n), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     nb = W.prefill_num_blocks(w, ctx) + 2
     order = W.rng(w.seed + seed, 2).permutation(nb).astype(np.int32)
-    op = OP.Pool(1, hkv, d, bs, 2, nb, initial_free_order=order.tolist())
-    cp = pkv.Pool(1, hkv, d, bs, 1, num_blocks=nb, initial_free_order=order)
+    op = OP.Pool(1, hkv, d, bs, W.ELEM_BYTES[kv], nb, initial_free_order=order.tolist())
+    cp = pkv.Pool(1, hkv, d, bs, CODE[kv], num_blocks=nb, initial_free_order=order)
     pre_slots, chunk_slots = [], []
     for s in range(S):
         op.seq_create(s)
@@ -240,20 +241,27 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None):
     chk_idx = np.concatenate([np.arange(off[s] + ctx[s] - n[s], off[s + 1]) for s in range(S)])
     ps = np.concatenate(pre_slots) if pre_slots else np.zeros(0, np.int64)
     cs = np.concatenate(chunk_slots)
-    kc = np.full((nb, bs, hkv, d), POISON["bf16"][1], dtype=np.uint16)
+    ks = vs = None
+    if kv == "fp8_e4m3":
+        ks = W.fp8_scale_from_absmax(np.abs(OA.to_f64(k_rows, "bf16")).max((0, 2)))
+        vs = W.fp8_scale_from_absmax(np.abs(OA.to_f64(v_rows, "bf16")).max((0, 2)))
+    dt, pz = POISON[kv]
+    kc = np.full((nb, bs, hkv, d), pz, dtype=dt)
     vc = kc.copy()
-    OA.reshape_and_cache(k_rows[pre_idx], v_rows[pre_idx], ps, kc, vc, "bf16", "bf16")
+    OA.reshape_and_cache(k_rows[pre_idx], v_rows[pre_idx], ps, kc, vc, "bf16", kv, ks, vs)
     dev = {
-        "kc": to_torch(kc, "bf16"), "vc": to_torch(vc, "bf16"),
+        "kc": to_torch(kc, kv), "vc": to_torch(vc, kv),
+        "ks": None if ks is None else torch.from_numpy(ks).cuda(),
+        "vs": None if vs is None else torch.from_numpy(vs).cuda(),
         "kn": to_torch(k_rows[chk_idx], "bf16"), "vn": to_torch(v_rows[chk_idx], "bf16"),
         "slots": torch.from_numpy(cs).cuda(), "q": to_torch(q, "bf16"),
         "tables": torch.from_numpy(tables).cuda(),
         "ctx": torch.from_numpy(ctx.astype(np.int32)).cuda(),
         "qs": torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).cuda(),
     }
-    OA.reshape_and_cache(k_rows[chk_idx], v_rows[chk_idx], cs, kc, vc, "bf16", "bf16")
+    OA.reshape_and_cache(k_rows[chk_idx], v_rows[chk_idx], cs, kc, vc, "bf16", kv, ks, vs)
     host = {"kc": kc, "vc": vc, "q": q, "tables": tables, "ctx": ctx,
-            "qs": np.concatenate([[0], np.cumsum(n)])}
+            "qs": np.concatenate([[0], np.cumsum(n)]), "kv": kv, "ks": ks, "vs": vs}
     return dev, host, int(n.max()), int(ctx.max())
 
 
@@ -262,11 +270,12 @@ def run_prefill_gpu(w, dev, max_q, max_ctx, causal=True, status=None):
     import torch
     import paged_kv_cache_295_gb300 as pkv
     pkv.reshape_and_cache(dev["kn"], dev["vn"], dev["slots"], dev["kc"], dev["vc"],
-                          device_status=status)
+                          k_scale=dev.get("ks"), v_scale=dev.get("vs"), device_status=status)
     out = torch.full((dev["q"].shape[0], w.num_q_heads, w.head_dim), float("nan"),
                      dtype=torch.float32, device="cuda")
     pkv.paged_attention_prefill(dev["q"], dev["qs"], dev["kc"], dev["vc"], dev["tables"],
                                 dev["ctx"], w.scale, max_q, max_ctx, causal=causal, out=out,
+                                k_scale=dev.get("ks"), v_scale=dev.get("vs"),
                                 device_status=status)
     torch.cuda.synchronize()
     return out.cpu().numpy()

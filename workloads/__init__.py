@@ -131,7 +131,10 @@ PREFILL_70B = PrefillWorkload("chunked_prefill_70b_gqa8_bf16", 16, 512, 15, 64, 
 # Small ragged case the oracle finishes in seconds.
 PREFILL_TINY = PrefillWorkload("tiny_prefill_bf16", 3, 0, 0, 8, 2, 128, 16, seed=7,
                                chunk_fixed=(5, 130, 64), prefix_fixed=(0, 37, 300))
-PREFILL = (PREFILL_TINY, PREFILL_7B, PREFILL_70B)
+# The 7B-shaped step with an FP8-E4M3 cache (tiles widened to fp16 in the kernel).
+PREFILL_7B_FP8 = PrefillWorkload("chunked_prefill_7b_fp8", 16, 512, 7, 32, 32, 128, 16, seed=5,
+                                 kv_dtype=FP8)
+PREFILL = (PREFILL_TINY, PREFILL_7B, PREFILL_70B, PREFILL_7B_FP8)
 
 
 def prefill_lens(w: PrefillWorkload):
