@@ -17,7 +17,7 @@
 // byte).  The lane that holds S^T for heads 2*tig, 2*tig+1 also holds O^T for
 // the same two heads, so the online-softmax rescale is lane-local.  P^T moves
 // from the accumulator layout to the B-fragment layout through 512 bytes of
-// per-warp shared memory.
+// per-warp shared memory: packed pairs in, one ldmatrix.trans out.
 //
 // 16-bit caches: fragments come from the swizzled tiles with ldmatrix
 // (ldmatrix.trans for V^T); P is split into bf16 hi + lo parts.  8-bit caches
@@ -54,7 +54,7 @@ struct Mma2Smem {
   static constexpr int kBoxes = D * KV::kBytes / 128;             // 128-byte TMA boxes per row
   static constexpr int kBoxBytes = CH * 128;                      // [CH rows][128 B]
   static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;      // K + V
-  static constexpr int kScratch = 8 * CH * 2 * 2;                 // P^T hi + lo, [8][CH] each
+  static constexpr int kScratch = 32 * 16;                         // P^T rows [32][8 heads]
   static_assert(kScratch <= 1024, "P^T scratch fits its 1 KiB");
   static constexpr int kWarpBytes = STAGES * kStageBytes + 1024;  // + scratch, 1 KiB aligned
   static_assert(STAGES * kStageBytes >= 8 * (D + 3) * 4, "combine area fits a warp ring");
@@ -95,6 +95,13 @@ __device__ __forceinline__ void fused_append_row16(const DecodeParams& p, int s,
   }
   asm volatile("fence.proxy.async.global;\n" ::: "memory");
   __syncwarp();
+}
+
+// 2^x on the SFU (ex2.approx: relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Largest log2 gap between a head's reference max and a chunk's max before
@@ -173,6 +180,14 @@ __global__ void __launch_bounds__(NW * 32)
 
   // q^T as B fragments: b0 = q[gid][k 2tig..], b1 = q[gid][k 2tig+8..] of each k-step
   // (FP8: logical k 2tig+e (+8) of k-step ks <-> dim 32*tig + 4*ks + e (+2)).
+  // log2-domain logit scale.  A negative scale is folded into q (exact sign
+  // flip) and a zero one raised to the smallest normal (every logit is then
+  // 0 as far as fp32 can tell), so sl2 > 0: the max of the scaled logits is
+  // sl2 times the max of the raw ones, and a masked -inf stays -inf.
+  float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
+  const float qsign = sl2 < 0.f ? -1.f : 1.f;
+  sl2 = fmaxf(fabsf(sl2), 1.17549435e-38f);
+
   uint32_t qb[KSTEPS][2];
   uint32_t qblo[QF32 ? KSTEPS : 1][2];
   {
@@ -187,12 +202,12 @@ __global__ void __launch_bounds__(NW * 32)
         if (real) {
           if (QF32) {
             const float* qf = static_cast<const float*>(p.q) + row * D + col;
-            x0 = qf[0];
-            x1 = qf[1];
+            x0 = qsign * qf[0];
+            x1 = qsign * qf[1];
           } else {
             const __nv_bfloat16* qh = static_cast<const __nv_bfloat16*>(p.q) + row * D + col;
-            x0 = __bfloat162float(qh[0]);
-            x1 = __bfloat162float(qh[1]);
+            x0 = qsign * __bfloat162float(qh[0]);
+            x1 = qsign * __bfloat162float(qh[1]);
           }
         }
         uint32_t hi, lo;
@@ -217,11 +232,9 @@ __global__ void __launch_bounds__(NW * 32)
   // softmax state of heads 2*tig and 2*tig+1
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   float ps0 = 0.f, ps1 = 0.f;   // INT8: sum of P as rounded to fp16 (the V offset's weight)
-  const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
-  const float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
 
   uint8_t* ring = smem + warp * SM::kWarpBytes;
-  uint8_t* scratch = ring + STAGES * SM::kStageBytes;      // P^T hi [8][CH], lo [8][CH]
+  uint8_t* scratch = ring + STAGES * SM::kStageBytes;      // P^T [32 rows][8 heads]
   const uint32_t ring_a = smem_u32(ring);
   const int nchunks = (t_end - t_begin + CH - 1) / CH;
   const int my_n = warp < nchunks ? (nchunks - warp + NW - 1) / NW : 0;
@@ -235,33 +248,26 @@ __global__ void __launch_bounds__(NW * 32)
   const bool fuse_here = !F8 && p.k_new != nullptr && part == nparts - 1 && my_n > 0 &&
                          warp == (nchunks - 1) % NW;
 
-  // Lane 0 arms the stage's barrier and loads K, lane 1 loads V (in parallel).
+  // One box per lane: K (even lanes) or V (odd), 128-byte column hh, row group
+  // bx (at most 2 x 4 boxes: block_size >= 8).  Lane 0 arms the barrier with
+  // the bytes of every box that is issued; a block-table hole or the rows past
+  // the context issue none.
   auto issue = [&](int it) {
-    if (it >= my_n || lane > 1) return;
+    if (it >= my_n) return;   // warp-uniform
     const int stage = it % STAGES;
     const int t0 = t_begin + (warp + it * NW) * CH;
     const uint32_t bar = smem_u32(&bars[warp][stage]);
-    if (lane == 0) {
-      uint32_t bytes = 0;
-      for (int bx = 0; bx < nbox; ++bx) {
-        const int tb = t0 + bx * box_rows;
-        if (tb >= ctx) break;
-        if (sbt[(tb >> p.bs_log2) - lb0] >= 0) bytes += 2 * H * box_rows * 128;
-      }
-      mbar_arrive_expect_tx(bar, bytes);
-    }
-    const uint32_t sbase = ring_a + stage * SM::kStageBytes + lane * H * SM::kBoxBytes;
-    const CUtensorMap* map = lane ? &tmap_v : &tmap_k;
-    for (int bx = 0; bx < nbox; ++bx) {
-      const int tb = t0 + bx * box_rows;
-      if (tb >= ctx) break;
-      const int32_t b = sbt[(tb >> p.bs_log2) - lb0];
-      if (b < 0) continue;
+    const int kv = lane & 1, hh = (lane >> 1) % H, bx = (lane >> 1) / H;
+    const int tb = t0 + bx * box_rows;
+    int32_t b = -1;
+    if (bx < nbox && tb < ctx) b = sbt[(tb >> p.bs_log2) - lb0];
+    const uint32_t n = __popc(__ballot_sync(0xffffffffu, b >= 0));
+    if (lane == 0) mbar_arrive_expect_tx(bar, n * box_rows * 128);
+    if (b >= 0) {
       const int z = (b << p.bs_log2) + (tb & ((1 << p.bs_log2) - 1));
-#pragma unroll
-      for (int hh = 0; hh < H; ++hh)
-        tma_load_3d(sbase + hh * SM::kBoxBytes + bx * box_rows * 128, map,
-                    hh * (128 / KV::kBytes), g, z, bar);
+      tma_load_3d(ring_a + stage * SM::kStageBytes + (kv * H + hh) * SM::kBoxBytes +
+                      bx * box_rows * 128,
+                  kv ? &tmap_v : &tmap_k, hh * (128 / KV::kBytes), g, z, bar);
     }
   };
 
@@ -285,11 +291,8 @@ __global__ void __launch_bounds__(NW * 32)
     const int valid = min(CH, ctx - t0);
     uint8_t* kb = ring + stage * SM::kStageBytes;
     uint8_t* vb = kb + H * SM::kBoxBytes;
-    bool hole = valid < CH;
-    if (!hole) {
-      for (int bx = 0; bx < nbox; ++bx)
-        if (sbt[((t0 + bx * box_rows) >> p.bs_log2) - lb0] < 0) hole = true;
-    }
+    const bool hole = __any_sync(
+        0xffffffffu, valid < CH || (lane < nbox && sbt[((t0 + lane * box_rows) >> p.bs_log2) - lb0] < 0));
     if (hole) {   // rows the TMA did not fill become zero
       for (int i = lane; i < CH * 8 * H * 2; i += 32) {
         const int r = (i >> 3) % CH;
@@ -347,14 +350,19 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
     // ---- online softmax (columns = heads 2tig, 2tig+1; rows = tokens) ------------
-    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+    // Columns of heads past the group are 0 (their q^T columns are 0): they stay
+    // finite and are never written out, so only tokens past the context (a
+    // partial chunk) are masked.
+    if (valid < CH) {   // warp-uniform
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-      const bool t0ok = 16 * rt + gid < valid, t1ok = 16 * rt + gid + 8 < valid;
-      sacc[rt][0] = (t0ok && h0ok) ? sacc[rt][0] * sl2 : -CUDART_INF_F;
-      sacc[rt][1] = (t0ok && h1ok) ? sacc[rt][1] * sl2 : -CUDART_INF_F;
-      sacc[rt][2] = (t1ok && h0ok) ? sacc[rt][2] * sl2 : -CUDART_INF_F;
-      sacc[rt][3] = (t1ok && h1ok) ? sacc[rt][3] * sl2 : -CUDART_INF_F;
+      for (int rt = 0; rt < RT; ++rt) {
+        if (16 * rt + gid >= valid) sacc[rt][0] = sacc[rt][1] = -CUDART_INF_F;
+        if (16 * rt + gid + 8 >= valid) sacc[rt][2] = sacc[rt][3] = -CUDART_INF_F;
+      }
+    }
+    float mx0 = fmaxf(sacc[0][0], sacc[0][2]), mx1 = fmaxf(sacc[0][1], sacc[0][3]);
+#pragma unroll
+    for (int rt = 1; rt < RT; ++rt) {
       mx0 = fmaxf(mx0, fmaxf(sacc[rt][0], sacc[rt][2]));
       mx1 = fmaxf(mx1, fmaxf(sacc[rt][1], sacc[rt][3]));
     }
@@ -363,16 +371,18 @@ __global__ void __launch_bounds__(NW * 32)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
+    mx0 *= sl2;   // sl2 > 0: the max of the scaled logits
+    mx1 *= sl2;
     // Lazy rescale: a head's reference max moves only when the chunk's max is
     // more than 2^kLazyLog2 above it, so p = 2^(s - m) stays below 256 and the
     // O rescale runs about once per partition instead of on most chunks (with
     // 8 heads one of them sets a new max in most chunks).  l and O share m, so
-    // the normalised result is unchanged.  m = -inf first: every real head moves.
+    // the normalised result is unchanged.  m = -inf first: every head moves.
     const bool up0 = mx0 > m0 + kLazyLog2, up1 = mx1 > m1 + kLazyLog2;
     if (__any_sync(0xffffffffu, up0 || up1)) {
       const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
-      const float a0 = up0 ? exp2f(m0 - mn0) : 1.f;   // exp2(-inf) = 0
-      const float a1 = up1 ? exp2f(m1 - mn1) : 1.f;
+      const float a0 = fast_ex2(m0 - mn0);   // 2^-inf = 0; 2^0 = 1
+      const float a1 = fast_ex2(m1 - mn1);
       l0 *= a0;
       l1 *= a1;
       if (I8) {
@@ -389,48 +399,57 @@ __global__ void __launch_bounds__(NW * 32)
       m0 = mn0;
       m1 = mn1;
     }
-    // P^T to B fragments via scratch: [head][CH tokens] (hi; lo for 16-bit caches)
-    {
-      auto put = [&](int off, float v, float& psum) {
-        if (F8) {
-          const __half hv = __float2half_rn(v);
-          *reinterpret_cast<__half*>(scratch + off) = hv;
-          if (I8) psum += __half2float(hv);
-        } else {
-          const __nv_bfloat16 hv = __float2bfloat16_rn(v);
-          *reinterpret_cast<__nv_bfloat16*>(scratch + off) = hv;
-          *reinterpret_cast<__nv_bfloat16*>(scratch + 16 * CH + off) =
-              __float2bfloat16_rn(v - __bfloat162float(hv));
-        }
-      };
+    // P^T to B fragments via scratch laid out [token][8 heads] (16-byte rows):
+    // each lane stores (token, heads 2tig, 2tig+1) as one packed pair, and one
+    // ldmatrix.trans hands every lane its (tokens 2tig, 2tig+1; head gid) pairs.
+    // 16-bit caches: bf16 hi rows 0..15, lo rows 16..31; 8-bit: fp16 rows 0..31.
 #pragma unroll
-      for (int rt = 0; rt < RT; ++rt) {
-        const bool t0ok = 16 * rt + gid < valid, t1ok = 16 * rt + gid + 8 < valid;
-        // (token 16rt + gid (+8), head 2tig (+1)); masked entries are 0
-        const float p00 = h0ok && t0ok ? exp2f(sacc[rt][0] - m0) : 0.f;
-        const float p01 = h1ok && t0ok ? exp2f(sacc[rt][1] - m1) : 0.f;
-        const float p10 = h0ok && t1ok ? exp2f(sacc[rt][2] - m0) : 0.f;
-        const float p11 = h1ok && t1ok ? exp2f(sacc[rt][3] - m1) : 0.f;
-        l0 += p00 + p10;
-        l1 += p01 + p11;
-        const int tk = 16 * rt + gid;
-        put(((2 * tig) * CH + tk) * 2, p00, ps0);
-        put(((2 * tig + 1) * CH + tk) * 2, p01, ps1);
-        put(((2 * tig) * CH + tk + 8) * 2, p10, ps0);
-        put(((2 * tig + 1) * CH + tk + 8) * 2, p11, ps1);
+    for (int rt = 0; rt < RT; ++rt) {
+      const float p00 = fast_ex2(fmaf(sacc[rt][0], sl2, -m0));   // token 16rt+gid, head 2tig
+      const float p01 = fast_ex2(fmaf(sacc[rt][1], sl2, -m1));   // head 2tig+1
+      const float p10 = fast_ex2(fmaf(sacc[rt][2], sl2, -m0));   // token 16rt+gid+8
+      const float p11 = fast_ex2(fmaf(sacc[rt][3], sl2, -m1));
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      uint8_t* row0 = scratch + (16 * rt + gid) * 16 + 4 * tig;
+      uint8_t* row1 = row0 + 8 * 16;
+      if (F8) {
+        const uint32_t h0 = pack_f16(p00, p01), h1 = pack_f16(p10, p11);
+        *reinterpret_cast<uint32_t*>(row0) = h0;
+        *reinterpret_cast<uint32_t*>(row1) = h1;
+        if (I8) {   // P as the MMA sees it (rounded to fp16)
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+          ps0 += f0.x + f1.x;
+          ps1 += f0.y + f1.y;
+        }
+      } else {
+        const uint32_t h0 = pack_bf16(p00, p01), h1 = pack_bf16(p10, p11);
+        *reinterpret_cast<uint32_t*>(row0) = h0;
+        *reinterpret_cast<uint32_t*>(row1) = h1;
+        *reinterpret_cast<uint32_t*>(row0 + 16 * 16) =
+            pack_bf16(p00 - bf16_lo(h0), p01 - bf16_hi(h0));
+        *reinterpret_cast<uint32_t*>(row1 + 16 * 16) =
+            pack_bf16(p10 - bf16_lo(h1), p11 - bf16_hi(h1));
       }
     }
     __syncwarp();
-    uint32_t pb0[RT], pb1[RT];   // P^T of k-step kk: tokens 16kk + 2tig (+8) of head gid
-#pragma unroll
-    for (int kk = 0; kk < RT; ++kk) {
-      pb0[kk] = *reinterpret_cast<const uint32_t*>(scratch + (gid * CH + 16 * kk + 2 * tig) * 2);
-      pb1[kk] = *reinterpret_cast<const uint32_t*>(scratch + (gid * CH + 16 * kk + 2 * tig + 8) * 2);
-    }
+    // matrix j = rows 8j..8j+7: 8-bit caches pb0/pb1 of k-steps 0 and 1; 16-bit
+    // caches hi (k 0..7, 8..15) then lo
+    uint32_t pb0[RT], pb1[RT];
     uint32_t pl0 = 0, pl1 = 0;
-    if (!F8) {
-      pl0 = *reinterpret_cast<const uint32_t*>(scratch + 16 * CH + (gid * CH + 2 * tig) * 2);
-      pl1 = *reinterpret_cast<const uint32_t*>(scratch + 16 * CH + (gid * CH + 2 * tig + 8) * 2);
+    {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(smem_u32(scratch) + lane * 16, r0, r1, r2, r3);
+      pb0[0] = r0;
+      pb1[0] = r1;
+      if constexpr (RT == 2) {
+        pb0[RT - 1] = r2;
+        pb1[RT - 1] = r3;
+      } else {
+        pl0 = r2;
+        pl1 = r3;
+      }
     }
 
     // ---- O^T += V^T P^T -----------------------------------------------------------
