@@ -271,6 +271,13 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
 
+  // 8-bit tiles: a lane reads K rows 16rt + gid (+8) at 16-byte units 2tig and
+  // 2tig+1, and V rows 16kk + 2tig (+1, +8, +9) at unit gid.  Row r's swizzle
+  // term depends on r mod 8 only, which is gid for the K rows and 2tig (+1)
+  // for the V rows, so each read is one of these offsets plus a constant.
+  const uint32_t k_swz0 = swz(gid, 2 * tig), k_swz1 = swz(gid, 2 * tig + 1);
+  const uint32_t v_swz0 = swz(2 * tig, gid), v_swz1 = swz(2 * tig + 1, gid);
+
   if (!F8 && fuse_here) fused_append_row16<D>(p, s, g, ctx, lb0, sbt, lane);   // warp-uniform
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) issue(st);
@@ -318,11 +325,11 @@ __global__ void __launch_bounds__(NW * 32)
       for (int rt = 0; rt < RT; ++rt) {
         uint32_t wa[8], wb[8];   // 32-byte slices [32*tig, +32) of token rows gid, gid+8
         {
-          const int ra = 16 * rt + gid, rb = ra + 8;
-          const uint4 a0 = *reinterpret_cast<const uint4*>(kb + swz(ra, 2 * tig));
-          const uint4 a1 = *reinterpret_cast<const uint4*>(kb + swz(ra, 2 * tig + 1));
-          const uint4 b0 = *reinterpret_cast<const uint4*>(kb + swz(rb, 2 * tig));
-          const uint4 b1 = *reinterpret_cast<const uint4*>(kb + swz(rb, 2 * tig + 1));
+          const uint8_t* ka = kb + rt * 2048;   // rows 16rt + gid (+8): swizzle term k_swz*
+          const uint4 a0 = *reinterpret_cast<const uint4*>(ka + k_swz0);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(ka + k_swz1);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(ka + 1024 + k_swz0);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(ka + 1024 + k_swz1);
           wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
           wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
           wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
@@ -457,11 +464,11 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int kk = 0; kk < RT; ++kk) {
         // lane owns output dims 16*gid + 2*mt + (0 | 1); tokens 16kk + 2tig, +1, +8, +9
-        const int r0 = 16 * kk + 2 * tig;
-        const uint4 va = *reinterpret_cast<const uint4*>(vb + swz(r0, gid));
-        const uint4 vv = *reinterpret_cast<const uint4*>(vb + swz(r0 + 1, gid));
-        const uint4 vc = *reinterpret_cast<const uint4*>(vb + swz(r0 + 8, gid));
-        const uint4 vd = *reinterpret_cast<const uint4*>(vb + swz(r0 + 9, gid));
+        const uint8_t* va_row = vb + kk * 2048;   // rows 16kk + 2tig, +1, +8, +9
+        const uint4 va = *reinterpret_cast<const uint4*>(va_row + v_swz0);
+        const uint4 vv = *reinterpret_cast<const uint4*>(va_row + v_swz1);
+        const uint4 vc = *reinterpret_cast<const uint4*>(va_row + 1024 + v_swz0);
+        const uint4 vd = *reinterpret_cast<const uint4*>(va_row + 1024 + v_swz1);
         const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vv.x, vv.y, vv.z, vv.w};
         const uint32_t Cw[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
