@@ -275,13 +275,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // the raw buffer tile j has just left, so kPfRawBufs copies are in flight.
       const uint32_t raw_a = sma + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
       const uint8_t* raw_p = sm + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
-      auto issue_raw = [&](int jj) -> uint32_t {   // bit i of the result: box i has data
+      // Lane i's block of box i of tile jj: -1 past the context, -2 out of range.
+      // Looked up one tile ahead of its copy, so the table load's latency
+      // overlaps the widening of the tile in between.
+      auto lookup = [&](int jj) -> int32_t {
         const int kb = jj * kPfKeys + lane * box_rows;
-        int32_t blk = -1;
-        if (lane < nbox && kb < ctx) {
-          const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
-          blk = (b >= 0 && b < p.num_blocks) ? b : -2;
-        }
+        if (jj >= ntiles || lane >= nbox || kb >= ctx) return -1;
+        const int32_t b = __ldg(bt_row + (kb >> p.bs_log2));
+        return (b >= 0 && b < p.num_blocks) ? b : -2;
+      };
+      auto issue_raw = [&](int jj, int32_t blk) -> uint32_t {   // bit i: box i has data
+        const int kb = jj * kPfKeys + lane * box_rows;
         const uint32_t valid = __ballot_sync(0xffffffffu, blk >= 0);
         if (!is_v && __ballot_sync(0xffffffffu, blk == -2) && !flagged) {
           if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
@@ -297,12 +301,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         return valid;
       };
+      // valids[i]: the boxes of tile j + i that have data (a window that moves
+      // with j, so it stays in registers)
       uint32_t valids[kPfRawBufs];
 #pragma unroll
-      for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b) : 0u;
+      for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b, lookup(b)) : 0u;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % STAGES;
         const int k0 = j * kPfKeys;
+        const int32_t next_blk = lookup(j + kPfRawBufs);   // used after this tile's widening
         if (j >= STAGES) {
           bool ok = true;
           if (lane == 0) ok = tc_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, abort_flag);
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (!is_v) {
             uint64_t m = 0;
             for (int i = 0; i < nbox; ++i) {
-              if (!((valids[rb] >> i) & 1u)) continue;
+              if (!((valids[0] >> i) & 1u)) continue;
               const int rows = min(box_rows, ctx - (k0 + i * box_rows));
               const uint64_t run = rows >= 64 ? ~0ull : ((1ull << rows) - 1ull);
               m |= run << (i * box_rows);
@@ -349,7 +356,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           mbar_arrive(smem_u32(is_v ? &full_v[st] : &full[st]));
         }
-        if (j + kPfRawBufs < ntiles) valids[rb] = issue_raw(j + kPfRawBufs);
+#pragma unroll
+        for (int b = 0; b + 1 < kPfRawBufs; ++b) valids[b] = valids[b + 1];
+        valids[kPfRawBufs - 1] = j + kPfRawBufs < ntiles ? issue_raw(j + kPfRawBufs, next_blk) : 0u;
       }
     }
   } else if (warp == 9) {
