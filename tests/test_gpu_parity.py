@@ -74,6 +74,8 @@ SMALL = {
                                                seed=17, ctx_law="fixed"), [2, 31, 900]),
     "d128_fp8_g16_bs8": (W.DecodeWorkload("fp8g16", 2, 32, 2, 128, 8, "fp8_e4m3", "bf16",
                                           seed=18, ctx_law="fixed"), [9, 1300]),
+    "d128_fp8_mha_bs16_qf32": (W.DecodeWorkload("fp8g1", 4, 4, 4, 128, 16, "fp8_e4m3", "f32",
+                                                seed=23, ctx_law="fixed"), [1, 32, 33, 700]),
     "d128_int8_mha_bs16": (W.DecodeWorkload("i8g1", 4, 4, 4, 128, 16, "int8", "bf16", seed=19,
                                             ctx_law="fixed"), [1, 17, 300, 1000]),
     "d128_int8_g8_bs32_qf32": (W.DecodeWorkload("i8g8", 3, 16, 2, 128, 32, "int8", "f32",
