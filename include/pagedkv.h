@@ -519,7 +519,7 @@ void decode_graph_destroy(pkv_decode_graph* g);
  *               (seq_append_slots; the pool's lengths already include them).
  *   out_host  : host [num_layers][batch][num_q_heads][head_dim] float32.
  * Page-locked host buffers make the copies asynchronous; pageable ones work
- * but are staged by the driver.  Returns INVALID_ARG for a bad batch, an
+ * but are staged by the CUDA driver.  Returns INVALID_ARG for a bad batch, an
  * unknown or swapped-out sequence or a table longer than max_blocks_per_seq,
  * CUDA if a copy or the launch fails. */
 pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool* pool,
