@@ -444,6 +444,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tQ = tm + 256 * t, tS = tQ + kPfKeys, tO = tQ + 2 * kPfKeys;
     const int tl = r / G;
     const bool row_ok = r < TQ * G && tok0 + t * TQ + tl < n;
+    // FP8 caches: the row goes to fp16 scaled by 2^qsh, which puts its largest
+    // |q| in [2^14, 2^15): inside fp16's range whatever q's magnitude, and
+    // exact for every element within 2^-24 of that max (a bf16 has 8
+    // significant bits).  The logit scale takes 2^-qsh back.
+    float q_unscale = 1.f;
     {   // this row of Q_t (token tok0 + t*TQ + r/G, head g*G + r%G; 0 past the
         // chunk) into TMEM, bf16 pairs per column (fp16 for FP8 caches): the A
         // operand of every QK
@@ -451,14 +456,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads + g * G + r % G) *
                     kPfD);
+      float qmul = 1.f;
+      if constexpr (FP8) {
+        uint32_t mbits = 0;   // the largest |bf16| of the row, as its bit pattern
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = row_ok ? src[i] : make_uint4(0, 0, 0, 0);
+          const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            mbits = max(mbits, max(x[e] & 0x7FFFu, (x[e] >> 16) & 0x7FFFu));
+        }
+        // exponent of the max (bf16 keeps fp32's); none for a zero row
+        const int ex = mbits >= 0x0080u ? static_cast<int>(mbits >> 7) - 127 : 0;
+        const int qsh = min(max(14 - ex, -126), 126);
+        qmul = __uint_as_float(static_cast<uint32_t>(127 + qsh) << 23);
+        q_unscale = __uint_as_float(static_cast<uint32_t>(127 - qsh) << 23);
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint4 v = row_ok ? src[i] : make_uint4(0, 0, 0, 0);
         const uint32_t x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)   // FP8 caches: the bf16 pair rounded to an fp16 pair
+        for (int e = 0; e < 4; ++e)   // FP8 caches: the scaled bf16 pair as an fp16 pair
           w[4 * i + e] = __uint_as_float(
-              FP8 ? pack_f16(__uint_as_float(x[e] << 16), __uint_as_float(x[e] & 0xFFFF0000u))
+              FP8 ? pack_f16(qmul * __uint_as_float(x[e] << 16),
+                             qmul * __uint_as_float(x[e] & 0xFFFF0000u))
                   : x[e]);
       }
       tc_st32(tQ + lane_q, w);
@@ -469,7 +492,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     const int qpos = ctx - n + tok0 + t * TQ + tl;      // this row's position
     const int last = p.causal ? qpos : ctx - 1;         // last key it sees
-    const float sl2 = FP8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
+    const float sl2 = FP8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) * q_unscale : p.qk_scale_log2;
     const bool pos_scale = sl2 > 0.f;
     uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
     float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units

@@ -198,11 +198,12 @@ def run_gpu(case: SmallCase, partition=0, layers=None, tables=None):
     return eng, outs, int(status.item())
 
 
-def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16"):
+def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None):
     """A seeded chunked-prefill step: the oracle pool and the C pool hand out the
     same slots; the cached prefix rows are placed by the oracle's append; the
     chunk's rows are left for the GPU append.  ``kv`` is the cache type (bf16,
-    or fp8_e4m3 with per-head absmax / 448 scales).  Returns (device tensors, the
+    or fp8_e4m3 with per-head absmax / 448 scales); ``q_mul`` cycles per-token
+    multipliers over q before its bf16 rounding.  Returns (device tensors, the
     oracle's host arrays after the chunk's append, max chunk, max context)."""
     import torch
     import paged_kv_cache_295_gb300 as pkv
@@ -235,7 +236,10 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16"):
     k_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
     v_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
     T = int(n.sum())
-    q = W.store(r.standard_normal((T, hq, d), dtype=np.float32), "bf16")
+    qf = r.standard_normal((T, hq, d), dtype=np.float32)
+    if q_mul is not None:
+        qf *= np.resize(np.asarray(q_mul, dtype=np.float32), T)[:, None, None]
+    q = W.store(qf, "bf16")
     off = np.concatenate([[0], np.cumsum(ctx)])
     pre_idx = np.concatenate([np.arange(off[s], off[s] + ctx[s] - n[s]) for s in range(S)])
     chk_idx = np.concatenate([np.arange(off[s] + ctx[s] - n[s], off[s + 1]) for s in range(S)])

@@ -86,6 +86,25 @@ def test_fp8_prefill_matches_oracle(lib, hq, hkv, bs, chunk, prefix, causal):
     assert err <= 1e-2, err
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_prefill_q_far_outside_fp16_range(lib, kv):
+    """q rows of magnitude 3e5 (past fp16's 65504), 1e-5 (fp16 subnormal) and 1:
+    the FP8 path carries q in fp16 scaled per row by a power of two, so every
+    row stays finite and exact; both paths match the oracle."""
+    import torch
+    w = _w(8, 2, 16)
+    dev, host, max_q, max_ctx = build(w, [40, 17], [100, 3], kv=kv, q_mul=[3e5, 1e-5, 1.0])
+    assert np.abs(OA.to_f64(host["q"], "bf16")).max() > 65504.0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_gpu(w, dev, max_q, max_ctx, causal=True, status=status)
+    assert int(status.item()) == 0
+    ref = OPF.paged_attention_prefill(host["q"], host["qs"], host["kc"], host["vc"],
+                                      host["tables"], host["ctx"], w.scale, "bf16", kv,
+                                      causal=True, k_scale=host["ks"], v_scale=host["vs"])
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= (TOL if kv == "bf16" else 1e-2)
+
+
 def test_single_token_chunks_match_decode_kernel(lib):
     """A chunk of one token is a decode step: both kernels, both within tolerance
     of the oracle, on the same cache."""
