@@ -52,11 +52,11 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "4c0c737569439d04", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239813 GB read + 4.746 MB
+NCU_TRAFFIC = {"sources_sha": "73c96296143abde4", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239850 GB read + 4.790 MB
                # written, plus the reduce kernel's 1.434 MB
                # (profiles/decode_mma2_llama7b_bf16.md)
-               "bytes_per_launch": 1239812608 + 4746496 + 1433856}
+               "bytes_per_launch": 1239849984 + 4789760 + 1433856}
 
 
 def parse_args(argv=None):

@@ -184,31 +184,56 @@ __global__ void __launch_bounds__(NW * 32)
   // flip) and a zero one raised to the smallest normal (every logit is then
   // 0 as far as fp32 can tell), so sl2 > 0: the max of the scaled logits is
   // sl2 times the max of the raw ones, and a masked -inf stays -inf.
+  // 8-bit caches carry q as fp16: the group's q is scaled by a power of two
+  // into fp16's range (q_fp16_scale) and the logit scale takes it back.
   float sl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
   const float qsign = sl2 < 0.f ? -1.f : 1.f;
-  sl2 = fmaxf(fabsf(sl2), 1.17549435e-38f);
 
   uint32_t qb[KSTEPS][2];
   uint32_t qblo[QF32 ? KSTEPS : 1][2];
+  float q_unscale = 1.f;
   {
     const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + hq0 + gid;
     const bool real = gid < G;
+    auto qpair = [&](int ks, int half, float& x0, float& x1) {
+      const int col = F8 ? 32 * tig + 4 * ks + 2 * half : 16 * ks + 8 * half + 2 * tig;
+      x0 = x1 = 0.f;
+      if (real) {
+        if (QF32) {
+          const float* qf = static_cast<const float*>(p.q) + row * D + col;
+          x0 = qsign * qf[0];
+          x1 = qsign * qf[1];
+        } else {
+          const __nv_bfloat16* qh = static_cast<const __nv_bfloat16*>(p.q) + row * D + col;
+          x0 = qsign * __bfloat162float(qh[0]);
+          x1 = qsign * __bfloat162float(qh[1]);
+        }
+      }
+    };
+    float qmul = 1.f;
+    if constexpr (F8) {   // the group's largest |q| (the lanes cover every head and dim)
+      float mx = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float x0, x1;
+          qpair(ks, half, x0, x1);
+          mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      qmul = q_fp16_scale(mx, q_unscale);
+    }
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int col = F8 ? 32 * tig + 4 * ks + 2 * half : 16 * ks + 8 * half + 2 * tig;
-        float x0 = 0.f, x1 = 0.f;
-        if (real) {
-          if (QF32) {
-            const float* qf = static_cast<const float*>(p.q) + row * D + col;
-            x0 = qsign * qf[0];
-            x1 = qsign * qf[1];
-          } else {
-            const __nv_bfloat16* qh = static_cast<const __nv_bfloat16*>(p.q) + row * D + col;
-            x0 = qsign * __bfloat162float(qh[0]);
-            x1 = qsign * __bfloat162float(qh[1]);
-          }
+        float x0, x1;
+        qpair(ks, half, x0, x1);
+        if (F8) {
+          x0 *= qmul;   // exact: a power of two
+          x1 *= qmul;
         }
         uint32_t hi, lo;
         if (F8) {
@@ -225,6 +250,8 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
+
+  sl2 = fmaxf(fabsf(sl2) * q_unscale, 1.17549435e-38f);
 
   float o[MT][4];
 #pragma unroll

@@ -36,6 +36,17 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// fp16 operands for q: the power of two 2^k that puts the largest |q| `mx` in
+// [2^14, 2^15), so any finite q stays finite and a bf16 q exact down to 2^-24
+// of that max; `unscale` = 2^-k goes into the logit scale.
+__device__ __forceinline__ float q_fp16_scale(float mx, float& unscale) {
+  const uint32_t b = __float_as_uint(mx);
+  const int ex = b >= 0x00800000u ? static_cast<int>(b >> 23) - 127 : 0;
+  const int k = min(max(14 - ex, -126), 126);
+  unscale = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);   // .x = lo (low half)
   return *reinterpret_cast<uint32_t*>(&v);
@@ -152,28 +163,49 @@ __global__ void __launch_bounds__(NW * 32)
   // logical k = 2*tig + e (+8) of k-step ks  <->  dim 32*tig + 4*ks + e (+2).
   uint32_t qa[KSTEPS][4];
   uint32_t qlo[QF32 ? KSTEPS : 1][4];
+  float q_unscale = 1.f;
   {
     const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + hq0;
+    auto qpair = [&](int ks, int half, int rh, float& x0, float& x1) {
+      const int h = gid + 8 * rh;
+      const int col = 32 * tig + 4 * ks + 2 * half;
+      x0 = x1 = 0.f;
+      if (h < G && (ROWS16 || rh == 0)) {
+        if (QF32) {
+          const float* qf = static_cast<const float*>(p.q) + (row0 + h) * D + col;
+          x0 = qf[0];
+          x1 = qf[1];
+        } else {
+          const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) + (row0 + h) * D + col;
+          x0 = __bfloat162float(qb[0]);
+          x1 = __bfloat162float(qb[1]);
+        }
+      }
+    };
+    float mx = 0.f;   // the group's largest |q| (the lanes cover every head and dim)
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          float x0, x1;
+          qpair(ks, half, rh, x0, x1);
+          mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float qmul = q_fp16_scale(mx, q_unscale);
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {
-          const int h = gid + 8 * rh;
-          const int col = 32 * tig + 4 * ks + 2 * half;
-          float x0 = 0.f, x1 = 0.f;
-          if (h < G && (ROWS16 || rh == 0)) {
-            if (QF32) {
-              const float* qf = static_cast<const float*>(p.q) + (row0 + h) * D + col;
-              x0 = qf[0];
-              x1 = qf[1];
-            } else {
-              const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) + (row0 + h) * D + col;
-              x0 = __bfloat162float(qb[0]);
-              x1 = __bfloat162float(qb[1]);
-            }
-          }
+          float x0, x1;
+          qpair(ks, half, rh, x0, x1);
+          x0 *= qmul;   // exact: a power of two
+          x1 *= qmul;
           const uint32_t hi = pack_f16(x0, x1);
           qa[ks][half * 2 + rh] = hi;
           if (QF32) {
@@ -190,7 +222,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-  const float sl2 = p.qk_scale_log2 * __ldg(p.k_scale + g);
+  const float sl2 = p.qk_scale_log2 * __ldg(p.k_scale + g) * q_unscale;
 
   uint8_t* ring = smem + warp * SM::kWarpBytes;
   const uint32_t ring_a = smem_u32(ring);

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import workloads as W
+from oracle import attention as OA
 from tests import gpu_cases as GC
 
 pytestmark = pytest.mark.gpu
@@ -109,6 +110,27 @@ def test_small_parity(torch_cuda, name, partition, decode_path):
         pytest.skip("the CUDA-core kernel is built for groups of 1, 2, 4 and 8")
     case, _ = GC.make_small(w, lens=lens)
     eng, outs, st = GC.run_gpu(case, partition=partition)
+    assert st == 0
+    for layer in range(len(outs)):
+        _check_layer(case, eng, outs, layer)
+
+
+@pytest.mark.parametrize("name", ["ragged_fp8_prefix", "d128_int8_mha_bs16",
+                                  "d128_fp8_g8_bs32_qf32", "llama70b_gqa8_bf16"])
+def test_q_far_outside_fp16_range(torch_cuda, name, decode_path):
+    """Sequences whose q is scaled by 3e5 (past fp16's 65504), 1e-5 (fp16
+    subnormal) or 1.  The 8-bit paths carry q in fp16, scaled by a power of two
+    into its range; every path must match the oracle on the same q."""
+    w, lens = SMALL[name]
+    if decode_path == "simt" and w.group > 8:
+        pytest.skip("the CUDA-core kernel is built for groups of 1, 2, 4 and 8")
+    case, _ = GC.make_small(w, lens=lens)
+    mul = np.resize(np.array([3e5, 1e-5, 1.0]), len(case.lens))[:, None, None]
+    for layer in range(len(case.q)):
+        q = OA.to_f64(case.q[layer], w.q_dtype) * mul
+        case.q[layer] = W.store(q.astype(np.float32), w.q_dtype)
+    assert np.abs(OA.to_f64(case.q[0], w.q_dtype)).max() > 65504.0
+    eng, outs, st = GC.run_gpu(case)
     assert st == 0
     for layer in range(len(outs)):
         _check_layer(case, eng, outs, layer)
