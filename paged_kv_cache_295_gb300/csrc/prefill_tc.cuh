@@ -544,21 +544,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         m = mt;
       }
       const float mu = m == -CUDART_INF_F ? 0.f : m;   // rows with nothing seen yet: p = 0
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      // Key pairs go through the packed fp32 pipe (fma / add .f32x2: each lane
+      // rounds as the scalar op would); ls[i] holds the partial sums of keys
+      // 4k + 2i and 4k + 2i + 1.
+      const float2 nmu = make_float2(-mu, -mu);
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       if (dense) {
+        const float2 s2 = make_float2(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-          sv[c] = pf_ex2(fmaf(sv[c], sl2, -mu));
-          ls4[c & 3] += sv[c];
+        for (int c = 0; c < kPfKeys; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), s2, nmu);
+          sv[c] = pf_ex2(x.x);
+          sv[c + 1] = pf_ex2(x.y);
+          ls[(c >> 1) & 1] = __fadd2_rn(ls[(c >> 1) & 1], make_float2(sv[c], sv[c + 1]));
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-          sv[c] = pf_ex2(sv[c] - mu);   // 2^-inf = 0 for masked keys
-          ls4[c & 3] += sv[c];
+        for (int c = 0; c < kPfKeys; c += 2) {
+          const float2 x = __fadd2_rn(make_float2(sv[c], sv[c + 1]), nmu);
+          sv[c] = pf_ex2(x.x);   // 2^-inf = 0 for masked keys
+          sv[c + 1] = pf_ex2(x.y);
+          ls[(c >> 1) & 1] = __fadd2_rn(ls[(c >> 1) & 1], make_float2(sv[c], sv[c + 1]));
         }
       }
-      l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+      l = l * alpha + ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y));
       // PV(j-1) must be finished before P is overwritten and before O is scaled
       if (j >= 1 && !tc_wait(smem_u32(&o_done[t]), (j - 1) & 1, abort_flag)) alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
@@ -567,16 +576,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {   // hi part, then what it left (bf16; fp16 for FP8)
-          const float a = sv[8 * u + 2 * e], b = sv[8 * u + 2 * e + 1];
+          const float2 ab = make_float2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
+          float2 hi;
           if (FP8) {
-            wh[e] = pack_f16(a, b);
-            const __half2 hv = *reinterpret_cast<const __half2*>(&wh[e]);
-            wl[e] = pack_f16(a - __low2float(hv), b - __high2float(hv));
+            wh[e] = pack_f16(ab.x, ab.y);
+            hi = __half22float2(*reinterpret_cast<const __half2*>(&wh[e]));
           } else {
-            wh[e] = pack_bf16(a, b);
-            wl[e] = pack_bf16(a - __uint_as_float(wh[e] << 16),
-                              b - __uint_as_float(wh[e] & 0xFFFF0000u));
+            wh[e] = pack_bf16(ab.x, ab.y);
+            hi = make_float2(__uint_as_float(wh[e] << 16), __uint_as_float(wh[e] & 0xFFFF0000u));
           }
+          const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f), ab);   // ab - hi, exact
+          wl[e] = FP8 ? pack_f16(lo.x, lo.y) : pack_bf16(lo.x, lo.y);
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
