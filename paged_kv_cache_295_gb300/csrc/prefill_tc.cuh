@@ -78,6 +78,13 @@ struct PrefillParams {
 
 // 2^x with the MUFU instruction (relative error about 2^-22; 2^-inf = +0,
 // results below 2^-126 flush to 0, which only drops terms that small).
+// max(a, b, c) in one instruction (sm_100 and later)
+__device__ __forceinline__ float pf_max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 __device__ __forceinline__ float pf_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -519,10 +526,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if ((lane & 31) == 0) mbar_arrive(smem_u32(&s_free[t]));
       float mt;
       if (dense) {   // warp-uniform: nothing masked; max of the raw logits, then scale
-        float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+        static_assert(kPfKeys % 4 == 0, "two three-input max chains");
+        float ma = sv[0], mb = sv[1];
 #pragma unroll
-        for (int c = 4; c < kPfKeys; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
-        mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+        for (int c = 2; c + 3 < kPfKeys; c += 4) {
+          ma = pf_max3(ma, sv[c], sv[c + 1]);
+          mb = pf_max3(mb, sv[c + 2], sv[c + 3]);
+        }
+        mt = fmaxf(pf_max3(ma, sv[kPfKeys - 2], sv[kPfKeys - 1]), mb) * sl2;
       } else {
         const uint32_t mlo = static_cast<uint32_t>(rmask), mhi = static_cast<uint32_t>(rmask >> 32);
         float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
