@@ -313,6 +313,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint32_t valids[kPfRawBufs];
 #pragma unroll
       for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b, lookup(b)) : 0u;
+      uint32_t unit_off[8];   // where 16-byte unit u sits in a row r = lane (mod 8): swz(r, u) - 128 r
+#pragma unroll
+      for (int u = 0; u < 8; ++u) unit_off[u] = static_cast<uint32_t>((u ^ (lane & 7)) << 4);
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % STAGES;
         const int k0 = j * kPfKeys;
@@ -334,19 +337,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // one chunk per step: the swizzle then spreads each step's 32 loads and
         // 32 stores evenly over the banks (lanes on different chunks of the same
         // rows, or the two halves 8 KiB apart, would collide 4 ways).
-#pragma unroll 4
+        // Row r = 32k + lane: its swizzle term depends on lane mod 8 only, so
+        // every address is a per-lane offset (unit_off) plus a constant.
+        const uint8_t* raw_l = raw + lane * 128;
+        uint8_t* dst_l = dst + lane * 128;
+#pragma unroll
         for (int it = 0; it < (kPfKeys / 32) * 8; ++it) {
-          const int r = (it >> 3) * 32 + lane, u = it & 7;
-          const uint4 c = *reinterpret_cast<const uint4*>(raw + swz(r, u));
+          const int rk = (it >> 3) * 32 * 128, u = it & 7;
+          const uint4 c = *reinterpret_cast<const uint4*>(raw_l + rk + unit_off[u]);
           uint32_t h[8];
           e4m3x4_to_f16x2x2(c.x, h[0], h[1]);
           e4m3x4_to_f16x2x2(c.y, h[2], h[3]);
           e4m3x4_to_f16x2x2(c.z, h[4], h[5]);
           e4m3x4_to_f16x2x2(c.w, h[6], h[7]);
-          uint8_t* half = dst + (u >> 2) * LY::kKVHalf;
+          uint8_t* half = dst_l + (u >> 2) * LY::kKVHalf + rk;
           const int uu = 2 * (u & 3);
-          *reinterpret_cast<uint4*>(half + swz(r, uu)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(half + swz(r, uu + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+          *reinterpret_cast<uint4*>(half + unit_off[uu]) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(half + unit_off[uu + 1]) = make_uint4(h[4], h[5], h[6], h[7]);
         }
         fence_proxy_async();   // the stage's generic writes before the MMAs' reads; the
         __syncwarp();          // raw buffer's reads before the next copy into it
