@@ -648,7 +648,7 @@ class PrefillStep:
         self.n, self.lens = W.prefill_lens(w)
         S, hq, hkv, d, bs = len(self.n), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
         nb = W.prefill_num_blocks(w, self.lens)
-        code = {"bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3}[w.kv_dtype]
+        code = {"bf16": pkv.BF16, "fp8_e4m3": pkv.FP8_E4M3, "int8": pkv.INT8}[w.kv_dtype]
         self.eng = eng = PagedKVCache(1, hkv, d, bs, nb, code, device=device,
                                       initial_free_order=W.free_order(w, nb))
         pre, chk = [], []
@@ -671,9 +671,10 @@ class PrefillStep:
         k_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         v_src = torch.randn((U, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         self.q = torch.randn((T, hq, d), generator=gen, device=device).to(torch.bfloat16)
-        if w.kv_dtype == "fp8_e4m3":   # static per-head scales: absmax / 448
-            eng.k_scale[0] = k_src.float().abs().amax(dim=(0, 2)) / 448.0
-            eng.v_scale[0] = v_src.float().abs().amax(dim=(0, 2)) / 448.0
+        if w.kv_dtype in ("fp8_e4m3", "int8"):   # static per-head scales: absmax / 448 or / 127
+            qmax = 448.0 if w.kv_dtype == "fp8_e4m3" else 127.0
+            eng.k_scale[0] = k_src.float().abs().amax(dim=(0, 2)) / qmax
+            eng.v_scale[0] = v_src.float().abs().amax(dim=(0, 2)) / qmax
         pre_i = torch.from_numpy(pre_idx).to(device)
         if pre_idx.size:
             eng.append(0, k_src[pre_i], v_src[pre_i],
@@ -848,6 +849,11 @@ class OraclePrefillStep:
                 sc = (np.abs(x).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
                 codes = fp8.encode_f32(x / sc[None, :, None])
                 setattr(self, name, OA.fp8_dequant(codes, sc))
+        elif w.kv_dtype == "int8":   # INT8 codes: their dequantised values
+            for name in ("K", "V"):
+                x = getattr(self, name).astype(np.float32)
+                sc = (np.abs(x).max(axis=(0, 2)) / np.float32(127.0)).astype(np.float32)
+                setattr(self, name, OA.int8_dequant(OA.int8_encode(x, sc), sc))
 
     def run(self, i):
         from oracle import prefill as OPF

@@ -403,10 +403,10 @@ pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_byte
  *                  rows query_start[s] .. query_start[s+1]-1 (n_s of them, 0
  *                  allowed) of q and out.
  *   k_cache, v_cache : device [num_blocks, block_size, num_kv_heads, 128],
- *                  kv_dtype bf16 or fp8_e4m3.
+ *                  kv_dtype bf16, fp8_e4m3 or int8.
  *   k_scale, v_scale : device [num_kv_heads] float32 dequant scales for an FP8
- *                  cache (value = e4m3 * scale[kv_head], as in decode); else
- *                  ignored.
+ *                  or INT8 cache (value = code * scale[kv_head], as in
+ *                  decode); else ignored.
  *   block_tables : device [num_seqs, max_blocks_per_seq] int32 (as in decode).
  *   context_lens : device [num_seqs] int32, the context INCLUDING the chunk;
  *                  n_s <= context_lens[s] <= max_context_len.
@@ -418,12 +418,13 @@ pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_byte
  *                  every chunk are not written.
  * Computes out[query_start[s]+i, h, :] = softmax(scale * q . K_g^T) V_g over
  * the visible keys, g = h / G, with float32 accumulation.  Runs on tcgen05
- * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).  FP8
- * tiles are widened to fp16 in shared memory (exact), so the contractions run
- * in fp16 (q rounded to fp16, P as fp16 hi + lo), the K scale folded into the
- * logit scale and the V scale into the output.
- * Supported: head_dim 128, bf16 q, bf16 or FP8-E4M3 caches (FP8 needs both
- * scales), G = num_q_heads / num_kv_heads
+ * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).  FP8 and
+ * INT8 tiles are widened to fp16 in shared memory (exact), so the
+ * contractions run in fp16 (each q row scaled by a power of two into fp16's
+ * range, P as fp16 hi + lo), the K scale folded into the logit scale and the
+ * V scale into the output.
+ * Supported: head_dim 128, bf16 q, bf16, FP8-E4M3 or INT8 caches (8-bit
+ * caches need both scales), G = num_q_heads / num_kv_heads
  * <= 16, block_size a power of two in [8, 4096], 16-byte aligned q, caches and
  * out.  Device-side problems (a bad query_start or context, a bad block) are
  * flagged in device_status; bad rows are skipped or zeroed. */

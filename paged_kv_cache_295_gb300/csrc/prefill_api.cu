@@ -34,8 +34,9 @@ extern "C" pkv_status paged_attention_prefill(
   if (causal != 0 && causal != 1) return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  const bool fp8 = kv_dtype == PKV_FP8_E4M3;
-  if (head_dim != kPfD || q_dtype != PKV_BF16 || (kv_dtype != PKV_BF16 && !fp8) || G > 16)
+  const bool fp8 = kv_dtype == PKV_FP8_E4M3, i8 = kv_dtype == PKV_INT8;
+  const bool codes8 = fp8 || i8;   // 8-bit caches: widened to fp16 in the kernel
+  if (head_dim != kPfD || q_dtype != PKV_BF16 || (kv_dtype != PKV_BF16 && !codes8) || G > 16)
     return PKV_ERR_UNSUPPORTED;
   if (!pow2(block_size) || block_size < 8 || block_size > 4096) return PKV_ERR_UNSUPPORTED;
   if (num_blocks * block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
@@ -52,7 +53,7 @@ extern "C" pkv_status paged_attention_prefill(
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_INVALID_ARG;
-  if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+  if (codes8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (!encode_fn()) return PKV_ERR_CUDA;
 
@@ -74,13 +75,13 @@ extern "C" pkv_status paged_attention_prefill(
   p.max_context_len = max_context_len;
   p.num_tokens = num_tokens;
   p.qk_scale_log2 = scale * 1.4426950408889634f;
-  p.k_scale = fp8 ? k_scale : nullptr;
-  p.v_scale = fp8 ? v_scale : nullptr;
+  p.k_scale = codes8 ? k_scale : nullptr;
+  p.v_scale = codes8 ? v_scale : nullptr;
 
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * block_size;
-  if (!make_map(&tk, k_cache, kPfD, num_kv_heads, rows, p.box_rows, fp8) ||
-      !make_map(&tv, v_cache, kPfD, num_kv_heads, rows, p.box_rows, fp8))
+  if (!make_map(&tk, k_cache, kPfD, num_kv_heads, rows, p.box_rows, codes8) ||
+      !make_map(&tv, v_cache, kPfD, num_kv_heads, rows, p.box_rows, codes8))
     return PKV_ERR_CUDA;
 
   const int pairs = (max_query_len + 2 * p.tile_tokens - 1) / (2 * p.tile_tokens);
@@ -92,7 +93,8 @@ extern "C" pkv_status paged_attention_prefill(
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   };
   if (fp8)
-    return launch(paged_prefill_tc_kernel<kPfStagesFp8, true>,
-                  PfLayout::bytes(kPfStagesFp8, true));
-  return launch(paged_prefill_tc_kernel<kPfStages, false>, PfLayout::bytes(kPfStages, false));
+    return launch(paged_prefill_tc_kernel<kPfStagesFp8, 1>, PfLayout::bytes(kPfStagesFp8, true));
+  if (i8)
+    return launch(paged_prefill_tc_kernel<kPfStagesFp8, 2>, PfLayout::bytes(kPfStagesFp8, true));
+  return launch(paged_prefill_tc_kernel<kPfStages, 0>, PfLayout::bytes(kPfStages, false));
 }

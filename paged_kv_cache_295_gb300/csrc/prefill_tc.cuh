@@ -130,13 +130,17 @@ struct PfLayout {
   }
 };
 
-template <int STAGES, bool FP8>
+// KIND: 0 bf16 cache; 1 FP8-E4M3 codes; 2 INT8 codes.  Both 8-bit kinds take
+// the widening path (FP8 below means "8-bit codes").
+template <int STAGES, int KIND>
 __global__ void __launch_bounds__(kPfThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   using LY = PfLayout;
   // FP8 caches: the tiles are widened to fp16 in shared memory, so both
   // contractions run as f16 MMAs (q and P in fp16 too); bf16 caches run bf16.
+  constexpr bool FP8 = KIND != 0;
+  constexpr bool I8 = KIND == 2;
   constexpr int kRing = LY::ring(FP8);
   const int G = p.num_q_heads / p.num_kv_heads;
   const int TQ = p.tile_tokens;
@@ -313,6 +317,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint32_t valids[kPfRawBufs];
 #pragma unroll
       for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b, lookup(b)) : 0u;
+      // Four codes -> two f16x2.  E4M3: exact.  INT8: V exact; K as code + 1152,
+      // which adds the same 1152 * sum(q) to every logit of a row (its softmax
+      // cancels it) and costs one PRMT pair instead of two more half subtractions.
+      auto widen4 = [&](uint32_t w, uint32_t& lo, uint32_t& hi) {
+        if constexpr (I8) {
+          if (is_v)
+            s8x4_to_f16x2x2(w, lo, hi);
+          else
+            s8x4_to_f16x2x2_biased(w, lo, hi);
+        } else {
+          e4m3x4_to_f16x2x2(w, lo, hi);
+        }
+      };
       uint32_t unit_off[8];   // where 16-byte unit u sits in a row r = lane (mod 8): swz(r, u) - 128 r
 #pragma unroll
       for (int u = 0; u < 8; ++u) unit_off[u] = static_cast<uint32_t>((u ^ (lane & 7)) << 4);
@@ -346,10 +363,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int rk = (it >> 3) * 32 * 128, u = it & 7;
           const uint4 c = *reinterpret_cast<const uint4*>(raw_l + rk + unit_off[u]);
           uint32_t h[8];
-          e4m3x4_to_f16x2x2(c.x, h[0], h[1]);
-          e4m3x4_to_f16x2x2(c.y, h[2], h[3]);
-          e4m3x4_to_f16x2x2(c.z, h[4], h[5]);
-          e4m3x4_to_f16x2x2(c.w, h[6], h[7]);
+          widen4(c.x, h[0], h[1]);
+          widen4(c.y, h[2], h[3]);
+          widen4(c.z, h[4], h[5]);
+          widen4(c.w, h[6], h[7]);
           uint8_t* half = dst_l + (u >> 2) * LY::kKVHalf + rk;
           const int uu = 2 * (u & 3);
           *reinterpret_cast<uint4*>(half + unit_off[uu]) = make_uint4(h[0], h[1], h[2], h[3]);

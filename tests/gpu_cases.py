@@ -202,7 +202,7 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None
     """A seeded chunked-prefill step: the oracle pool and the C pool hand out the
     same slots; the cached prefix rows are placed by the oracle's append; the
     chunk's rows are left for the GPU append.  ``kv`` is the cache type (bf16,
-    or fp8_e4m3 with per-head absmax / 448 scales); ``q_mul`` cycles per-token
+    or fp8_e4m3 / int8 with per-head absmax / 448 or / 127 scales); ``q_mul`` cycles per-token
     multipliers over q before its bf16 rounding.  Returns (device tensors, the
     oracle's host arrays after the chunk's append, max chunk, max context)."""
     import torch
@@ -246,9 +246,10 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None
     ps = np.concatenate(pre_slots) if pre_slots else np.zeros(0, np.int64)
     cs = np.concatenate(chunk_slots)
     ks = vs = None
-    if kv == "fp8_e4m3":
-        ks = W.fp8_scale_from_absmax(np.abs(OA.to_f64(k_rows, "bf16")).max((0, 2)))
-        vs = W.fp8_scale_from_absmax(np.abs(OA.to_f64(v_rows, "bf16")).max((0, 2)))
+    if kv in ("fp8_e4m3", "int8"):
+        rule = W.fp8_scale_from_absmax if kv == "fp8_e4m3" else W.int8_scale_from_absmax
+        ks = rule(np.abs(OA.to_f64(k_rows, "bf16")).max((0, 2)))
+        vs = rule(np.abs(OA.to_f64(v_rows, "bf16")).max((0, 2)))
     dt, pz = POISON[kv]
     kc = np.full((nb, bs, hkv, d), pz, dtype=dt)
     vc = kc.copy()

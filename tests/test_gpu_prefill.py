@@ -65,28 +65,30 @@ FP8_CASES = [  # (Hq, Hkv, bs, chunk lens, cached prefix lens)
 ]
 
 
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "int8"])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("hq,hkv,bs,chunk,prefix", FP8_CASES)
-def test_fp8_prefill_matches_oracle(lib, hq, hkv, bs, chunk, prefix, causal):
-    """FP8-E4M3 caches: the chunk's codes bit-exact with the oracle's append,
-    the output within the FP8 bound (the oracle dequantises the same codes)."""
+def test_8bit_prefill_matches_oracle(lib, hq, hkv, bs, chunk, prefix, causal, kv):
+    """FP8-E4M3 and INT8 caches: the chunk's codes bit-exact with the oracle's
+    append, the output within the 8-bit bound (the oracle dequantises the same
+    codes)."""
     import torch
     w = _w(hq, hkv, bs)
-    dev, host, max_q, max_ctx = build(w, chunk, prefix, kv="fp8_e4m3")
+    dev, host, max_q, max_ctx = build(w, chunk, prefix, kv=kv)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = run_gpu(w, dev, max_q, max_ctx, causal=causal, status=status)
     assert int(status.item()) == 0
-    assert np.array_equal(from_torch(dev["kc"], "fp8_e4m3"), host["kc"])
-    assert np.array_equal(from_torch(dev["vc"], "fp8_e4m3"), host["vc"])
+    assert np.array_equal(from_torch(dev["kc"], kv), host["kc"])
+    assert np.array_equal(from_torch(dev["vc"], kv), host["vc"])
     ref = OPF.paged_attention_prefill(host["q"], host["qs"], host["kc"], host["vc"],
-                                      host["tables"], host["ctx"], w.scale, "bf16", "fp8_e4m3",
+                                      host["tables"], host["ctx"], w.scale, "bf16", kv,
                                       causal=causal, k_scale=host["ks"], v_scale=host["vs"])
     assert np.isfinite(got).all()
     err = np.abs(got - ref).max() if got.size else 0.0
     assert err <= 1e-2, err
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "int8"])
 def test_prefill_q_far_outside_fp16_range(lib, kv):
     """q rows of magnitude 3e5 (past fp16's 65504), 1e-5 (fp16 subnormal) and 1:
     the FP8 path carries q in fp16 scaled per row by a power of two, so every
@@ -184,17 +186,17 @@ def test_fullsize_sampled_rows(lib, name):
     assert int(st.status.item()) == 0
     k_src, v_src, off = st.src
     got = st.out
-    fp8 = w.kv_dtype == "fp8_e4m3"
+    codes8 = w.kv_dtype in ("fp8_e4m3", "int8")
     for s in sorted({int(np.argmin(st.lens)), int(np.argmax(st.lens))}):
         L, n = int(st.lens[s]), int(st.n[s])
         rows = sorted({0, n // 2, n - 1})
-        if fp8:   # the cache's codes through the block table, dequantised by the oracle
+        if codes8:   # the cache's codes through the block table, dequantised by the oracle
             blocks = torch.from_numpy(st.tables_h[s, :-(-L // w.block_size)]).cuda()
             ks, vs = (x[0].cpu().numpy() for x in (st.eng.k_scale, st.eng.v_scale))
-            kc = from_torch(st.eng.k_cache(0)[blocks], "fp8_e4m3").reshape(-1, *k_src.shape[1:])
-            vc = from_torch(st.eng.v_cache(0)[blocks], "fp8_e4m3").reshape(-1, *v_src.shape[1:])
-            K = OA.fp8_dequant(kc[:L], ks)
-            V = OA.fp8_dequant(vc[:L], vs)
+            kc = from_torch(st.eng.k_cache(0)[blocks], w.kv_dtype).reshape(-1, *k_src.shape[1:])
+            vc = from_torch(st.eng.v_cache(0)[blocks], w.kv_dtype).reshape(-1, *v_src.shape[1:])
+            K = OA.decode_kv(kc[:L], w.kv_dtype, ks)
+            V = OA.decode_kv(vc[:L], w.kv_dtype, vs)
         else:
             K = OA.to_f64(from_torch(k_src[off[s]:off[s] + L], "bf16"), "bf16")
             V = OA.to_f64(from_torch(v_src[off[s]:off[s] + L], "bf16"), "bf16")
@@ -202,4 +204,4 @@ def test_fullsize_sampled_rows(lib, name):
         q = OA.to_f64(from_torch(st.q[a:a + n], "bf16"), "bf16")
         ref = OPF.attend_rows(q[rows], K, V, w.scale, [L - n + i for i in rows])
         g = got[[a + i for i in rows]].cpu().numpy()
-        assert np.abs(g - ref).max() <= (1e-2 if fp8 else TOL)
+        assert np.abs(g - ref).max() <= (1e-2 if codes8 else TOL)

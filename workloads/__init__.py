@@ -134,7 +134,10 @@ PREFILL_TINY = PrefillWorkload("tiny_prefill_bf16", 3, 0, 0, 8, 2, 128, 16, seed
 # The 7B-shaped step with an FP8-E4M3 cache (tiles widened to fp16 in the kernel).
 PREFILL_7B_FP8 = PrefillWorkload("chunked_prefill_7b_fp8", 16, 512, 7, 32, 32, 128, 16, seed=5,
                                  kv_dtype=FP8)
-PREFILL = (PREFILL_TINY, PREFILL_7B, PREFILL_70B, PREFILL_7B_FP8)
+# The same step with an INT8 cache (section 3.1 symmetric codes, per-head scales).
+PREFILL_7B_INT8 = PrefillWorkload("chunked_prefill_7b_int8", 16, 512, 7, 32, 32, 128, 16, seed=5,
+                                  kv_dtype=INT8)
+PREFILL = (PREFILL_TINY, PREFILL_7B, PREFILL_70B, PREFILL_7B_FP8, PREFILL_7B_INT8)
 
 
 def prefill_lens(w: PrefillWorkload):
