@@ -317,18 +317,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint32_t valids[kPfRawBufs];
 #pragma unroll
       for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b, lookup(b)) : 0u;
-      // Four codes -> two f16x2.  E4M3: exact.  INT8: V exact; K as code + 1152,
-      // which adds the same 1152 * sum(q) to every logit of a row (its softmax
-      // cancels it) and costs one PRMT pair instead of two more half subtractions.
+      // Four codes -> two f16x2.  E4M3: exact.  INT8: code + 1152 (one XOR and
+      // two PRMT): in K it adds the same 1152 * sum(q) to every logit of a row,
+      // which its softmax cancels; in V the epilogue takes 1152 back off O / l.
       auto widen4 = [&](uint32_t w, uint32_t& lo, uint32_t& hi) {
-        if constexpr (I8) {
-          if (is_v)
-            s8x4_to_f16x2x2(w, lo, hi);
-          else
-            s8x4_to_f16x2x2_biased(w, lo, hi);
-        } else {
+        if constexpr (I8)
+          s8x4_to_f16x2x2_biased(w, lo, hi);
+        else
           e4m3x4_to_f16x2x2(w, lo, hi);
-        }
       };
       uint32_t unit_off[8];   // where 16-byte unit u sits in a row r = lane (mod 8): swz(r, u) - 128 r
 #pragma unroll
@@ -663,8 +659,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_wait(smem_u32(&o_done[t]), (my_nt - 1) & 1, abort_flag);
     if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
-      // 1 / l, times the V scale for FP8 caches
-      const float inv = l > 0.f ? (FP8 ? __ldg(p.v_scale + g) : 1.f) / l : 0.f;
+      // 1 / l, times the V scale for 8-bit caches.  INT8: V went in as
+      // code + 1152 and O and l share every rescale, so O / l carries + 1152
+      // exactly once (P as the MMA saw it, hi + lo, matches l to about 2^-22).
+      const float vsc = FP8 ? __ldg(p.v_scale + g) : 1.f;
+      const float inv = l > 0.f ? vsc / l : 0.f;
+      const float off = (I8 && l > 0.f) ? 1152.f * vsc : 0.f;
       float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads +
                              g * G + r % G) * kPfD;
 #pragma unroll
@@ -675,7 +675,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(orow + c + e) =
-                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+                make_float4(fmaf(o[e], inv, -off), fmaf(o[e + 1], inv, -off),
+                            fmaf(o[e + 2], inv, -off), fmaf(o[e + 3], inv, -off));
         }
       }
     }
