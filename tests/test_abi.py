@@ -295,3 +295,24 @@ def test_auto_partition_small_batches_fill_one_wave(lib):
     assert lib.partition_tokens(8, 32, 32, 974, 0) == 512          # 512 items at 512
     assert lib.partition_tokens(32, 32, 32, 974, 0) == 1024        # one partition each
     assert lib.partition_tokens(32, 32, 32, 4085, 0) == 1024       # large work: unchanged
+
+
+def test_prefill_argument_checks(lib):
+    """paged_attention_prefill's checks, all before any device work: an fp32 cache
+    is unsupported; an INT8 cache is accepted (an empty chunk returns OK right
+    after the type checks); 8-bit caches (FP8 and INT8) need both scales.  Every
+    call returns before a launch, so the 16-byte aligned placeholder addresses
+    are never used."""
+    so = lib.library()
+    fake = 0x100000
+
+    def call(kv, scales, max_q=8):
+        ks = fake if scales else None
+        return so.paged_attention_prefill(fake, fake, fake, fake, fake, fake, 1, 8, max_q, 8, 2,
+                                          128, 16, 64, 4, 64, 0.1, 1, lib.BF16, kv, ks, ks, fake,
+                                          None, None)
+
+    assert call(lib.F32, True) == 5                       # UNSUPPORTED
+    assert call(lib.INT8, True, max_q=0) == 0             # accepted: nothing to do
+    assert call(lib.FP8_E4M3, False) == 1                 # INVALID_ARG: scales required
+    assert call(lib.INT8, False) == 1
