@@ -87,3 +87,21 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("name", ["tiny_prefill_bf16", "chunked_prefill_7b_fp8",
+                                  "chunked_prefill_7b_int8"])
+def test_prefill_reference_arm(name):
+    """The prefill reference arm (the oracle on sampled query rows; 8-bit caches
+    through their codes) prints one TFLOP/s line."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1",
+               OPENBLAS_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", name, "--steps", "2", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["config"]["workload"] == name and d["cpu_baseline"]["kind"] == "oracle"
