@@ -332,6 +332,38 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   int32_t partition_tokens, int32_t* device_status,
                                   pkv_stream_t stream);
 
+/* Decode kernel choice, for tests and profiles.  paged_attention_decode and
+ * paged_attention_decode_append pick one kernel by shape: the transposed
+ * mma.sync kernel for G <= 8 (bf16 head_dim 64 / 128, 8-bit head_dim 128,
+ * block_size >= 8), else the heads-as-rows mma.sync kernel (bf16 head_dim
+ * 64 / 128, FP8 head_dim 128, G <= 16, block_size >= 8), else the CUDA-core
+ * kernel.  pkv_test_force_decode_kernel(k) makes every later call in the
+ * process skip to kernel k where k supports the shape (falling back down the
+ * same order where it does not); PKV_DECODE_KERNEL_AUTO restores the choice
+ * by shape.  It exists so that tests can run every kernel on the same inputs.
+ * The setting is process-wide: calls racing with a change may take either
+ * kernel.  An unknown value returns INVALID_ARG and changes nothing.  Not a
+ * paged-attention operation of the source pages. */
+typedef enum {
+  PKV_DECODE_KERNEL_AUTO = 0,
+  PKV_DECODE_KERNEL_HEADS_AS_ROWS = 1,
+  PKV_DECODE_KERNEL_CUDA_CORE = 2
+} pkv_decode_kernel;
+pkv_status pkv_test_force_decode_kernel(int32_t kernel);
+
+/* Test of the bounded device waits, not a paged-attention operation of the
+ * source pages.  pkv_test_decode_stall(bytes) with bytes > 0 makes every
+ * later launch of the transposed decode kernel (the one chosen for G <= 8)
+ * arm one barrier phase - warp 0, first stage, CTA (sequence 0, KV head 0,
+ * partition 0) - for `bytes` more than its copies bring, before issuing them.
+ * The copies land, the phase never completes, and after the 2 s bound the
+ * warp flags PKV_DEV_TIMEOUT in device_status, waits (bounded) for its other
+ * copies in flight and leaves its share out of the output; the call itself
+ * returns PKV_OK and the context stays usable.  bytes = 0 restores normal
+ * launches.  bytes must be a multiple of 16 and at most 65536, else
+ * INVALID_ARG.  Process-wide, like pkv_test_force_decode_kernel. */
+pkv_status pkv_test_decode_stall(uint32_t bytes);
+
 /* One decode step with the append fused in: the same as
  *   reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, num_seqs, ...)
  *   paged_attention_decode(q, k_cache, v_cache, ...)
@@ -552,8 +584,11 @@ pkv_status decode_graph_step_host(pkv_decode_graph* g, const pkv_pool* pool,
  *   - The array keeps the previous call's contents; nothing in it needs to
  *     start at zero, since a call writes every partial before reading it.
  *   - The first call on each device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture begins. */
+ *     that device current) and caches it, keyed by the unique id of the
+ *     device's current context; make that first call before any stream
+ *     capture begins.  A call that finds a different context (the previous
+ *     one was destroyed, e.g. by cudaDeviceReset) looks the address up again,
+ *     so after such a reset, too, call once before capturing. */
 pkv_status paged_attention_decode_noalloc(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

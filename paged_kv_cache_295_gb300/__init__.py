@@ -112,6 +112,8 @@ _SIGS = {
                                              I32, FL, I32, I32, P, P, P, I32, P, P]),
     "paged_attention_prefill": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, I64,
                                       I32, I32, FL, I32, I32, I32, P, P, P, P, P]),
+    "pkv_test_force_decode_kernel": (I32, [I32]),
+    "pkv_test_decode_stall": (I32, [C.c_uint32]),
     "pkv_copy_kernel": (I32, [P, P, SZ, P]),
     "pkv_read_kernel": (I32, [P, SZ, P, P]),
     "pkv_read_kernel_sink_floats": (I32, []),
@@ -402,6 +404,23 @@ def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_l
                     partition=0) -> int:
     return int(library().paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
                                                          head_dim, max_context_len, partition))
+
+
+DECODE_KERNELS = {"auto": 0, "mma": 1, "simt": 2}
+
+
+def force_decode_kernel(name: str = "auto"):
+    """Tests and profiles: make later decode calls skip to the heads-as-rows
+    mma.sync kernel ("mma") or the CUDA-core kernel ("simt") where it supports
+    the shape; "auto" restores the choice by shape (pkv_test_force_decode_kernel)."""
+    _check(library().pkv_test_force_decode_kernel(DECODE_KERNELS[name]),
+           "pkv_test_force_decode_kernel")
+
+
+def stall_decode_for_test(nbytes: int = 0):
+    """Tests of the bounded waits: later launches of the transposed decode
+    kernel wait in vain for ``nbytes`` on one barrier phase (0 = normal)."""
+    _check(library().pkv_test_decode_stall(int(nbytes)), "pkv_test_decode_stall")
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -1,9 +1,8 @@
 // Host entry points of the decode path: argument validation, split-KV
 // partition choice, workspace layout and dispatch to the kernel instantiation
 // for (KV type, head_dim, query-group size).
+#include <atomic>
 #include <cmath>
-#include <cstdlib>
-#include <cstring>
 
 #include "decode_kernel.cuh"
 
@@ -31,17 +30,17 @@ namespace {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
-// Kernel choice.  Unset: the transposed mma.sync kernel (decode_mma2.cuh) for
-// groups of up to 8 heads, the heads-as-rows mma.sync kernel (decode_mma.cuh)
-// for groups of up to 16, else the CUDA-core kernel - the fastest measured
-// order.  PKV_DECODE_PATH=mma skips the transposed kernel, =tc selects the
-// tcgen05 kernel where it applies, =simt forces the CUDA-core kernel; the tests
-// check every kernel on the same inputs.
-bool force_path(const char* name) {
-  const char* v = std::getenv("PKV_DECODE_PATH");
-  return v && std::strcmp(v, name) == 0;
-}
-bool force_simt() { return force_path("simt"); }
+// Kernel choice.  By shape: the transposed mma.sync kernel (decode_mma2.cuh)
+// for groups of up to 8 heads, the heads-as-rows mma.sync kernel
+// (decode_mma.cuh) for groups of up to 16, else the CUDA-core kernel - the
+// fastest measured order.  pkv_test_force_decode_kernel lets tests and
+// profiles run the other kernels on the same inputs; the hot path reads that
+// setting with one relaxed atomic load.
+std::atomic<int32_t> g_forced_kernel{PKV_DECODE_KERNEL_AUTO};
+int32_t forced_kernel() { return g_forced_kernel.load(std::memory_order_relaxed); }
+// Bytes a test makes the next transposed-kernel launches wait for in vain
+// (pkv_test_decode_stall); 0 otherwise.
+std::atomic<uint32_t> g_stall_bytes{0};
 
 int log2i(int64_t x) {
   int r = 0;
@@ -189,14 +188,13 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  const bool use_tc =
-      force_path("tc") && tc_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
-  const bool use_mma2 = !use_tc && !force_simt() && !force_path("mma") &&
+  const int32_t forced = forced_kernel();
+  const bool use_mma2 = forced == PKV_DECODE_KERNEL_AUTO &&
                         mma2_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
-  const bool use_mma = !use_tc && !use_mma2 && !force_simt() &&
+  const bool use_mma = !use_mma2 && forced != PKV_DECODE_KERNEL_CUDA_CORE &&
                        mma_path_supported(kv_dtype, head_dim, G, block_size, num_blocks);
   LaunchFn fn = pick(kv_dtype, head_dim, G);
-  if (!use_tc && !use_mma2 && !use_mma && !fn) return PKV_ERR_UNSUPPORTED;
+  if (!use_mma2 && !use_mma && !fn) return PKV_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
@@ -241,6 +239,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.max_parts = parts;
   p.q_is_bf16 = q_dtype == PKV_BF16;
   p.qk_scale_log2 = scale * 1.4426950408889634f;
+  p.test_stall_bytes = g_stall_bytes.load(std::memory_order_relaxed);
   a.num_seqs = num_seqs;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   if (fa) {
@@ -261,7 +260,6 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
       if (st != PKV_OK) return st;
     }
   }
-  if (use_tc) return launch_decode_tc(a, k_cache, v_cache, num_blocks, q_dtype == PKV_F32);
   if (use_mma2)
     return launch_decode_mma2(a, k_cache, v_cache, head_dim, num_blocks, q_dtype == PKV_F32,
                               kv_dtype);
@@ -310,4 +308,18 @@ extern "C" pkv_status paged_attention_decode_append(
                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
                      max_context_len, scale, q_dtype, kv_dtype, k_scale, v_scale, out, workspace,
                      workspace_bytes, partition_tokens, device_status, stream, &fa);
+}
+
+extern "C" pkv_status pkv_test_force_decode_kernel(int32_t kernel) {
+  if (kernel != PKV_DECODE_KERNEL_AUTO && kernel != PKV_DECODE_KERNEL_HEADS_AS_ROWS &&
+      kernel != PKV_DECODE_KERNEL_CUDA_CORE)
+    return PKV_ERR_INVALID_ARG;
+  pkv::g_forced_kernel.store(kernel, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_test_decode_stall(uint32_t bytes) {
+  if (bytes % 16 != 0 || bytes > 65536) return PKV_ERR_INVALID_ARG;
+  pkv::g_stall_bytes.store(bytes, std::memory_order_relaxed);
+  return PKV_OK;
 }

@@ -69,6 +69,10 @@ struct DecodeParams {
   const void* v_new;
   const int64_t* new_slots;
   int32_t new_src_dtype;
+  // Tests of the bounded waits (pkv_test_decode_stall): bytes the transposed
+  // kernel's CTA (0, 0, 0) adds to warp 0's first barrier phase and never
+  // copies, so that wait runs out; 0 in every normal call.
+  uint32_t test_stall_bytes;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr, int src_bytes) {
@@ -412,10 +416,4 @@ bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_si
                          int64_t num_blocks);
 pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
                               int head_dim, int64_t num_blocks, bool q_f32, int32_t kv_dtype);
-// 5th-generation tensor-core (tcgen05 + TMEM) path; see decode_tc.cuh.
-bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
-                       int64_t num_blocks);
-pkv_status launch_decode_tc(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                            int64_t num_blocks, bool q_f32);
-
 }  // namespace pkv

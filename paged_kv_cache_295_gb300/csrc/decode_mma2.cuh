@@ -306,6 +306,13 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t v_swz0 = swz(2 * tig, gid), v_swz1 = swz(2 * tig + 1, gid);
 
   if (!F8 && fuse_here) fused_append_row16<D>(p, s, g, ctx, lb0, sbt, lane);   // warp-uniform
+  // Tests of the bounded waits: the first phase of warp 0's stage 0 in CTA
+  // (0, 0, 0) expects bytes no copy brings, before any copy is issued, so its
+  // wait runs out and the timeout path below runs.
+  if (p.test_stall_bytes != 0 && warp == 0 && lane == 0 && my_n > 0 && blockIdx.x == 0 &&
+      blockIdx.y == 0 && blockIdx.z == 0)
+    mbar_expect_tx(smem_u32(&bars[0][0]), p.test_stall_bytes);
+  __syncwarp();
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) issue(st);
 

@@ -6,7 +6,6 @@
 
 #include "decode_mma.cuh"
 #include "decode_mma_fp8.cuh"
-#include "decode_tc.cuh"
 #include "decode_mma2.cuh"
 #include "tmap.cuh"
 
@@ -56,23 +55,6 @@ pkv_status launch_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPar
     return PKV_ERR_CUDA;
   dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
   kern<<<grid, NW * 32, smem, stream>>>(tk, tv, mp);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  return PKV_OK;
-}
-
-// tcgen05 path (bf16, head_dim 128): 4 warps per CTA, 3 TMA stages of 64-token tiles.
-template <bool QF32>
-pkv_status launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const MmaParams& mp,
-                     int num_seqs, cudaStream_t stream) {
-  constexpr int STAGES = 3;
-  const int bs = 1 << mp.p.bs_log2;
-  const int table_entries = (mp.p.partition_tokens + bs - 1) / bs + 2;
-  const size_t smem = TcLayout::bytes(STAGES, table_entries);
-  auto kern = paged_decode_tc_kernel<QF32, STAGES>;
-  if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
-    return PKV_ERR_CUDA;
-  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
-  kern<<<grid, kTcThreads, smem, stream>>>(tk, tv, mp);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }
@@ -168,36 +150,6 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
         head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(128), 0, a.stream, p)
                         : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(128), 0, a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-  }
-  return PKV_OK;
-}
-
-bool tc_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
-                       int64_t num_blocks) {
-  if (kv_dtype != PKV_BF16 || head_dim != kTcD) return false;
-  if (group < 1 || group > 16) return false;
-  if (block_size < 8) return false;
-  if (num_blocks * block_size > 0x7fffffffLL) return false;
-  return encode_fn() != nullptr;
-}
-
-pkv_status launch_decode_tc(const DecodeLaunch& a, const void* k_cache, const void* v_cache,
-                            int64_t num_blocks, bool q_f32) {
-  const DecodeParams& p = a.p;
-  const int bs = 1 << p.bs_log2;
-  MmaParams mp{p, bs < kTcTile ? bs : kTcTile};
-  CUtensorMap tk, tv;
-  const int64_t rows = num_blocks * bs;
-  if (!make_map(&tk, k_cache, kTcD, p.num_kv_heads, rows, mp.box_rows, false) ||
-      !make_map(&tv, v_cache, kTcD, p.num_kv_heads, rows, mp.box_rows, false))
-    return PKV_ERR_CUDA;
-  const pkv_status st = q_f32 ? launch_tc<true>(tk, tv, mp, a.num_seqs, a.stream)
-                              : launch_tc<false>(tk, tv, mp, a.num_seqs, a.stream);
-  if (st != PKV_OK) return st;
-  if (p.max_parts > 1) {
-    if (launch_pdl(paged_decode_reduce_kernel<kTcD>, dim3(a.num_seqs * p.num_q_heads), dim3(128),
-                   0, a.stream, p) != cudaSuccess)
-      return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

@@ -19,3 +19,12 @@ def lib():
     _build.build_library()
     import paged_kv_cache_295_gb300 as pkv
     return pkv
+
+
+@pytest.fixture
+def decode_kernel(lib):
+    """Selects the decode kernel for one test: call it with "auto" (the choice
+    by shape), "mma" (the heads-as-rows mma.sync kernel) or "simt" (the
+    CUDA-core kernel).  The choice by shape is restored afterwards."""
+    yield lib.force_decode_kernel
+    lib.force_decode_kernel("auto")

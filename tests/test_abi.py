@@ -300,19 +300,42 @@ def test_auto_partition_small_batches_fill_one_wave(lib):
 def test_prefill_argument_checks(lib):
     """paged_attention_prefill's checks, all before any device work: an fp32 cache
     is unsupported; an INT8 cache is accepted (an empty chunk returns OK right
-    after the type checks); 8-bit caches (FP8 and INT8) need both scales.  Every
-    call returns before a launch, so the 16-byte aligned placeholder addresses
-    are never used."""
+    after the type checks); 8-bit caches (FP8 and INT8) need both scales.  The
+    calls run in a child process that sees no GPU, so the 16-byte aligned
+    placeholder addresses could never reach a kernel even if a check moved
+    behind a launch (that call would return CUDA instead)."""
+    import subprocess
+    import sys
+    code = f"""
+import sys
+sys.path.insert(0, {ROOT!r})
+import paged_kv_cache_295_gb300 as lib
+so = lib.library()
+fake = 0x100000
+def call(kv, scales, max_q=8):
+    ks = fake if scales else None
+    return so.paged_attention_prefill(fake, fake, fake, fake, fake, fake, 1, 8, max_q, 8, 2,
+                                      128, 16, 64, 4, 64, 0.1, 1, lib.BF16, kv, ks, ks, fake,
+                                      None, None)
+print(call(lib.F32, True), call(lib.INT8, True, max_q=0), call(lib.FP8_E4M3, False),
+      call(lib.INT8, False))
+"""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    # UNSUPPORTED; accepted (nothing to do); INVALID_ARG twice (scales required)
+    assert r.stdout.split() == ["5", "0", "1", "1"]
+
+
+def test_decode_test_hooks_check_their_arguments(lib):
+    """The kernel choice and the barrier stall used by the GPU tests refuse
+    unknown values and leave the setting unchanged (host only)."""
     so = lib.library()
-    fake = 0x100000
-
-    def call(kv, scales, max_q=8):
-        ks = fake if scales else None
-        return so.paged_attention_prefill(fake, fake, fake, fake, fake, fake, 1, 8, max_q, 8, 2,
-                                          128, 16, 64, 4, 64, 0.1, 1, lib.BF16, kv, ks, ks, fake,
-                                          None, None)
-
-    assert call(lib.F32, True) == 5                       # UNSUPPORTED
-    assert call(lib.INT8, True, max_q=0) == 0             # accepted: nothing to do
-    assert call(lib.FP8_E4M3, False) == 1                 # INVALID_ARG: scales required
-    assert call(lib.INT8, False) == 1
+    assert lib.STATUS[so.pkv_test_force_decode_kernel(3)] == "invalid_arg"
+    assert lib.STATUS[so.pkv_test_force_decode_kernel(-1)] == "invalid_arg"
+    for k in (1, 2, 0):
+        assert so.pkv_test_force_decode_kernel(k) == 0
+    assert lib.STATUS[so.pkv_test_decode_stall(8)] == "invalid_arg"
+    assert lib.STATUS[so.pkv_test_decode_stall(65552)] == "invalid_arg"
+    assert so.pkv_test_decode_stall(0) == 0

@@ -82,8 +82,7 @@ def _lens(S, seed):
 
 @pytest.mark.parametrize("name", sorted(CASES))
 @pytest.mark.parametrize("partition", [0, 64])
-def test_fused_equals_separate_and_oracle(lib, monkeypatch, name, partition):
-    monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
+def test_fused_equals_separate_and_oracle(lib, name, partition):
     w, _ = CASES[name]
     case, _ = GC.make_small(w, lens=_lens(w.num_seqs, w.seed), layers=1)
     (o_sep, c_sep, s_sep), (o_fus, c_fus, s_fus) = _both(case, case.step_slots, partition)
@@ -95,11 +94,10 @@ def test_fused_equals_separate_and_oracle(lib, monkeypatch, name, partition):
     assert np.abs(o_fus.astype(np.float64) - ref).max() <= TOL[w.kv_dtype]
 
 
-def test_fused_fp8_from_f32_rows(lib, monkeypatch):
+def test_fused_fp8_from_f32_rows(lib):
     """8-bit caches quantise f32 sources in the decode kernel exactly as the
     append kernel does."""
     import torch
-    monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
     w = W.DecodeWorkload("fa_fp8_f32", 10, 8, 2, 128, 16, "fp8_e4m3", "bf16", seed=36,
                          ctx_law="fixed")
     case, _ = GC.make_small(w, lens=_lens(10, 36), layers=1)
@@ -125,8 +123,8 @@ def test_fused_fp8_from_f32_rows(lib, monkeypatch):
 
 
 @pytest.mark.parametrize("path", ["simt", "mma"])
-def test_two_kernel_fallback_paths_agree(lib, monkeypatch, path):
-    monkeypatch.setenv("PKV_DECODE_PATH", path)
+def test_two_kernel_fallback_paths_agree(lib, decode_kernel, path):
+    decode_kernel(path)
     w, _ = CASES["bf16_g4"]
     case, _ = GC.make_small(w, lens=_lens(w.num_seqs, 5), layers=1)
     (o_sep, c_sep, s_sep), (o_fus, c_fus, s_fus) = _both(case, case.step_slots, 0)
@@ -135,13 +133,12 @@ def test_two_kernel_fallback_paths_agree(lib, monkeypatch, path):
     assert o_fus.tobytes() == o_sep.tobytes()
 
 
-def test_wrong_slot_is_flagged_and_not_written(lib, monkeypatch):
+def test_wrong_slot_is_flagged_and_not_written(lib):
     """A slot other than the block table's slot of position ctx - 1 is not
     written (another partition could be reading it) and flags BAD_SLOT; a
     negative slot appends nothing and flags nothing."""
     import torch
     import paged_kv_cache_295_gb300 as pkv
-    monkeypatch.delenv("PKV_DECODE_PATH", raising=False)
     w, _ = CASES["bf16_g4"]
     case, _ = GC.make_small(w, lens=_lens(w.num_seqs, 9), layers=1)
     # a sequence whose new token is not the first of its block, so slot - 1 is
