@@ -21,8 +21,14 @@
 //  * the array keeps whatever the previous call left in it.  Nothing has to
 //    start at zero: each call writes every partial before it reads it.
 //  * The first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress with that device current) and remembers it; make
-//    that first call before any stream capture begins.
+//    (cudaGetSymbolAddress with that device current) and remembers it with
+//    the unique id of the context it belongs to; make that first call before
+//    any stream capture begins.  When a later call finds another context
+//    current on that device (the old one was destroyed, e.g. by
+//    cudaDeviceReset, and the library's module loaded again), it looks the
+//    address up again, so that call too should come before any capture.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -33,12 +39,46 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;   // the context the address belongs to
+  void* addr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
+
+// Unique id of the calling thread's current context, or 0 when there is none
+// yet (the driver's functions are reached through the runtime, so the library
+// links no libcuda).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // symbol's name is only a host-side handle, never a device pointer, so the
-// kernels get the address cudaGetSymbolAddress returns.
+// kernels get the address cudaGetSymbolAddress returns.  It is looked up once
+// per device and context: again only when the device's context has changed.
 pkv_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -47,16 +87,19 @@ pkv_status scratch_address(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const unsigned long long id = current_context_id();
+  ScratchAddr& c = g_scratch[dev];
+  if (c.addr == nullptr || id == 0 || id != c.ctx_id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return PKV_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = current_context_id();   // the lookup made the context current if it was not
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return PKV_OK;
 }
 
