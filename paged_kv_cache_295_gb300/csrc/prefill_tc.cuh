@@ -41,7 +41,7 @@
 #pragma once
 
 #include "decode_mma_fp8.cuh"
-#include "decode_tc.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -523,6 +523,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool pos_scale = sl2 > 0.f;
     uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
     float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units
+    // INT8: the sum of P as the MMA sees it (fp16 hi + lo), the weight of the
+    // V codes' +1152 offset.  It can fall short of l: a P below 2^-14 keeps
+    // fewer bits in fp16 and one below 2^-25 is lost, which a single key far
+    // above the rest makes the common case.
+    float lm = 0.f;
     bool alive = true;
     for (int j = 0; j < my_nt && alive; ++j) {
       const int k0 = j * kPfKeys;
@@ -602,6 +607,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // PV(j-1) must be finished before P is overwritten and before O is scaled
       if (j >= 1 && !tc_wait(smem_u32(&o_done[t]), (j - 1) & 1, abort_flag)) alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
+      float2 lmt = make_float2(0.f, 0.f);   // INT8: this tile's P as the MMA sees it
 #pragma unroll
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
@@ -618,11 +624,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f), ab);   // ab - hi, exact
           wl[e] = FP8 ? pack_f16(lo.x, lo.y) : pack_bf16(lo.x, lo.y);
+          if constexpr (I8) {
+            const float2 lr = __half22float2(*reinterpret_cast<const __half2*>(&wl[e]));
+            lmt = __fadd2_rn(lmt, __fadd2_rn(hi, lr));
+          }
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
             make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
+      if constexpr (I8) lm = lm * alpha + (lmt.x + lmt.y);
       if (__any_sync(0xffffffffu, resc)) {   // after P is out of the registers
         tc_fence_after();
 #pragma unroll
@@ -660,11 +671,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
       // 1 / l, times the V scale for 8-bit caches.  INT8: V went in as
-      // code + 1152 and O and l share every rescale, so O / l carries + 1152
-      // exactly once (P as the MMA saw it, hi + lo, matches l to about 2^-22).
+      // code + 1152, so O carries 1152 times the sum of P as the MMA saw it
+      // (lm, rescaled with O and l), which comes off after the division.
       const float vsc = FP8 ? __ldg(p.v_scale + g) : 1.f;
       const float inv = l > 0.f ? vsc / l : 0.f;
-      const float off = (I8 && l > 0.f) ? 1152.f * vsc : 0.f;
+      const float off = (I8 && l > 0.f) ? 1152.f * vsc * (lm / l) : 0.f;
       float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads +
                              g * G + r % G) * kPfD;
 #pragma unroll

@@ -198,12 +198,16 @@ def run_gpu(case: SmallCase, partition=0, layers=None, tables=None):
     return eng, outs, int(status.item())
 
 
-def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None):
+def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None,
+                 shape_rows=None):
     """A seeded chunked-prefill step: the oracle pool and the C pool hand out the
     same slots; the cached prefix rows are placed by the oracle's append; the
     chunk's rows are left for the GPU append.  ``kv`` is the cache type (bf16,
     or fp8_e4m3 / int8 with per-head absmax / 448 or / 127 scales); ``q_mul`` cycles per-token
-    multipliers over q before its bf16 rounding.  Returns (device tensors, the
+    multipliers over q before its bf16 rounding; ``shape_rows(k, v, q, starts)``
+    may change the float32 K / V rows ([sum(ctx), Hkv, D], sequence s from row
+    starts[s]) and q ([sum(chunk), Hq, D]) in place before they are stored.
+    Returns (device tensors, the
     oracle's host arrays after the chunk's append, max chunk, max context)."""
     import torch
     import paged_kv_cache_295_gb300 as pkv
@@ -233,14 +237,16 @@ def make_prefill(w, chunk, prefix, seed=0, bad_block=None, kv="bf16", q_mul=None
         tables[bad_block] = nb + 5
     r = W.rng(w.seed + seed, 3)
     U = int(ctx.sum())
-    k_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
-    v_rows = W.store(r.standard_normal((U, hkv, d), dtype=np.float32), "bf16")
+    kf = r.standard_normal((U, hkv, d), dtype=np.float32)
+    vf = r.standard_normal((U, hkv, d), dtype=np.float32)
     T = int(n.sum())
     qf = r.standard_normal((T, hq, d), dtype=np.float32)
     if q_mul is not None:
         qf *= np.resize(np.asarray(q_mul, dtype=np.float32), T)[:, None, None]
-    q = W.store(qf, "bf16")
     off = np.concatenate([[0], np.cumsum(ctx)])
+    if shape_rows is not None:
+        shape_rows(kf, vf, qf, off[:-1])
+    k_rows, v_rows, q = W.store(kf, "bf16"), W.store(vf, "bf16"), W.store(qf, "bf16")
     pre_idx = np.concatenate([np.arange(off[s], off[s] + ctx[s] - n[s]) for s in range(S)])
     chk_idx = np.concatenate([np.arange(off[s] + ctx[s] - n[s], off[s + 1]) for s in range(S)])
     ps = np.concatenate(pre_slots) if pre_slots else np.zeros(0, np.int64)
