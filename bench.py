@@ -71,6 +71,14 @@ def parse_args(argv=None):
     ap.add_argument("--partition", type=int, default=0, help="split-KV tokens (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=0, help="e2e steps (0 = min(steps, 200))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the selected workload only (profiling runs)")
+    ap.add_argument("--sustain-seconds", type=float, default=1.0,
+                    help="after the timed steps, repeat the step this long for the clock record")
+    ap.add_argument("--clock-period-ms", type=int, default=20)
+    ap.add_argument("--cpu-cores", type=int, default=0,
+                    help="reference arm: oracle worker processes (0 = every core this "
+                         "process may run on)")
     ap.add_argument("--no-bandwidth-ref", action="store_true",
                     help="skip the in-run copy/read reference kernels (profiling runs)")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
@@ -90,7 +98,7 @@ def workload_of(args):
 # The sources the decode kernels (and their launch) are built from.
 DECODE_SOURCES = ("common.cuh", "decode_api.cu", "decode_kernel.cuh", "decode_launch.cuh",
                   "decode_mma.cuh", "decode_mma2.cuh", "decode_mma_fp8.cuh",
-                  "decode_mma_launch.cu", "decode_tc.cuh", "tmap.cuh")
+                  "decode_mma_launch.cu", "tmap.cuh")
 
 
 def kernel_sources_sha() -> str:
@@ -251,14 +259,10 @@ def model_tokens_per_s(w, step_s_per_layer):
 
 def decode_kernel_name(w) -> str:
     """The decode kernel the library picks for this workload's shape."""
-    forced = os.environ.get("PKV_DECODE_PATH")
-    if forced == "simt" or w.group > 16 or w.block_size < 8:
+    if w.group > 16 or w.block_size < 8:
         return "paged_decode_kernel"
-    if forced == "tc" and w.kv_dtype == "bf16" and w.head_dim == 128:
-        return "paged_decode_tc_kernel"
-    if forced != "mma" and w.group <= 8 and (
-            (w.kv_dtype == "bf16" and w.head_dim in (64, 128))
-            or (w.kv_dtype in ("fp8_e4m3", "int8") and w.head_dim == 128)):
+    if w.group <= 8 and ((w.kv_dtype == "bf16" and w.head_dim in (64, 128))
+                         or (w.kv_dtype in ("fp8_e4m3", "int8") and w.head_dim == 128)):
         return "paged_decode_mma2_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):
         return "paged_decode_mma_kernel"
@@ -360,6 +364,7 @@ class DeviceStep:
         """One decode step (every layer) through paged_attention_decode_append;
         ``ev`` = (start, end) event lists per layer around that call."""
         eng, k = self.eng, i % len(self.q[0])
+        self.runs = i + 1
         for layer in range(self.w.num_layers):
             if ev is not None:
                 ev[0][layer].record()
@@ -369,6 +374,33 @@ class DeviceStep:
                               device_status=self.status)
             if ev is not None:
                 ev[1][layer].record()
+
+
+    def sample(self, s):
+        """Host copies of what sequence ``s`` attended over in the last layer of
+        the last step, for a check against the oracle: its q row, its blocks
+        (in table order, so the table becomes 0 .. nb-1), the layer's scales and
+        the output row the kernel wrote."""
+        import torch
+        w, layer = self.w, self.w.num_layers - 1
+        L = int(self.lens[s])
+        nb = -(-L // w.block_size)
+        idx = torch.from_numpy(self.tables_h[s, :nb].astype(np.int64)).to(self.device)
+
+        def host(t):
+            t = t.contiguous().cpu()
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16)
+            return t.numpy()
+        k_last = (self.runs - 1) % len(self.q[layer])
+        ks = None if self.eng.k_scale is None else host(self.eng.k_scale[layer])
+        vs = None if self.eng.v_scale is None else host(self.eng.v_scale[layer])
+        return {"seq": int(s), "context": L, "layer": layer,
+                "q": host(self.q[layer][k_last][s:s + 1]),
+                "k": host(self.eng.k_cache(layer).index_select(0, idx)),
+                "v": host(self.eng.v_cache(layer).index_select(0, idx)),
+                "k_scale": ks, "v_scale": vs, "out": host(self.out[s:s + 1]),
+                "scale": self.eng.scale, "q_dtype": w.q_dtype, "kv_dtype": w.kv_dtype}
 
 
 # ------------------------------------------------- in-run HBM references ---
@@ -402,6 +434,90 @@ def in_run_bandwidth(device, nbytes=4 << 30, reps=10):
 
 
 # --------------------------------------------------------------- our arm ---
+# The workloads every default run also times, each in this process after the
+# headline one: the tiny fp32 case (parity only), the 70B-shaped GQA-8 layer,
+# the 128K-context split-KV layer and the ragged 32-layer FP8 step.
+CONFIG_SET = ("tiny_fp32_mha", "llama70b_gqa8_bf16", "long_ctx_splitkv_bf16",
+              "ragged_32layer_fp8")
+# max-abs tolerance against the oracle by cache type (f32 / bf16: 2e-3; 8-bit: 1e-2)
+ORACLE_TOL = {"f32": 2e-3, "bf16": 2e-3, "fp8_e4m3": 1e-2, "int8": 1e-2}
+
+
+def time_steps(st, n, first=0):
+    """Runs ``n`` steps of ``st`` with CUDA events around the whole region and
+    around every layer's call; returns (region seconds, per-call seconds)."""
+    import torch
+    L = st.w.num_layers
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(2)]
+          for _ in range(n)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(n):
+        st.run(first + i, ev[i])
+    t1.record()
+    torch.cuda.synchronize(st.device)
+    calls = [ev[i][0][l].elapsed_time(ev[i][1][l]) * 1e-3 for i in range(n) for l in range(L)]
+    return t0.elapsed_time(t1) * 1e-3, calls
+
+
+def prime_queue(device):
+    """A short device-side delay before a timed region, so the host enqueues
+    the first timed launches while the GPU is still busy (the first interval
+    then holds no launch latency).  It runs before the region's start event."""
+    import torch
+    torch.cuda._sleep(2_000_000)
+
+
+def call_stats(w, lens, calls, peak):
+    """Mean / median / p10 / p90 of one launch's time and the roofline
+    fractions they give (algorithmic bytes: unique K/V rows read, q, out,
+    tables, lengths, plus the appended rows)."""
+    alg = attention_alg_bytes(w, lens) + append_alg_bytes(w)
+    mean, med = statistics.fmean(calls), statistics.median(calls)
+    p10, p90 = (float(np.percentile(calls, q)) for q in (10, 90))
+    return {"us_per_layer_mean": round(mean * 1e6, 3), "us_per_layer_median": round(med * 1e6, 3),
+            "us_per_layer_p10_p90": [round(p10 * 1e6, 3), round(p90 * 1e6, 3)],
+            "alg_bytes_per_launch": alg,
+            "achieved_gbs_mean": round(alg / mean / 1e9, 2),
+            "achieved_gbs_median": round(alg / med / 1e9, 2),
+            "frac_mean": round(alg / mean / 1e9 / peak, 4),
+            "frac_median": round(alg / med / 1e9 / peak, 4)}
+
+
+def run_config(name, args, dev, peak):
+    """One more workload timed like the headline one (same steps and warm-up),
+    plus the host copy of one sequence for the oracle check; frees its pool."""
+    import torch
+    w = WORKLOADS[name]
+    st = DeviceStep(w, dev, partition=args.partition)
+    for i in range(args.warmup):
+        st.run(i)
+    torch.cuda.synchronize(dev)
+    prime_queue(dev)
+    dt, calls = time_steps(st, args.steps, args.warmup)
+    rec = {"kind": "parity only" if name == "tiny_fp32_mha" else "timed",
+           "num_layers": w.num_layers, "num_seqs": w.num_seqs,
+           "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+           "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+           "kernel": decode_kernel_name(w) + (" + paged_decode_reduce_kernel"
+                                              if st.max_parts > 1 else ""),
+           "partition_tokens": st.P, "max_partitions": st.max_parts,
+           "append": "fused into the decode kernel" if st.fused() else "append kernel, then decode",
+           "ms_per_step": round(dt / args.steps * 1e3, 5),
+           "kv_gb_per_step_unique": round(kv_bytes_unique(w, st.lens) * w.num_layers / 1e9, 4),
+           "value_logical_gbs": round(kv_bytes_logical(w, st.lens) * w.num_layers * args.steps
+                                      / dt / 1e9, 2),
+           "decode_tokens_per_s": round(w.num_seqs * args.steps / dt, 1),
+           "device_status": int(st.status.item())}
+    rec.update(call_stats(w, st.lens, calls, peak))
+    seqs = range(w.num_seqs) if w.num_seqs <= 2 else [int(np.argmax(st.lens))]
+    samples = [st.sample(s) for s in seqs]
+    del st
+    torch.cuda.empty_cache()
+    return rec, samples
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -416,38 +532,47 @@ def run_ours(args):
         raise SystemExit("--warmup must be >= 3")
     bw = None if args.no_bandwidth_ref else in_run_bandwidth(dev)
     st = DeviceStep(w, dev, partition=args.partition)
+    lens, nb = st.lens, st.eng.num_blocks
     L = w.num_layers
+    peak, peak_src = measured_peaks()
+    # nvidia-smi starts before the warm-up, so its start-up stays out of the region
+    clocks = ClockSampler(local, period_ms=args.clock_period_ms)
+    time.sleep(0.3)
     for i in range(Wm):
         st.run(i)
     torch.cuda.synchronize(dev)
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(2)]
-          for _ in range(K)]
-    clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for i in range(K):
-        st.run(i, ev[i])
-    t1.record()
-    torch.cuda.synchronize(dev)
+    prime_queue(dev)
+    dt_local, attn_s = time_steps(st, K, Wm)
     barrier(world)
+    # The same step again for at least --sustain-seconds while the sampler
+    # runs, so the clock record covers a region long enough to sample; its
+    # times are reported beside the K-step figures and never replace them.
+    sustain = None
+    if args.sustain_seconds > 0:
+        n_ext = max(K, int(math.ceil(args.sustain_seconds / max(dt_local / K, 1e-6))))
+        prime_queue(dev)
+        dt_ext, ext_s = time_steps(st, n_ext, Wm + K)
+        sustain = {"steps": n_ext, "seconds": round(dt_ext, 3),
+                   "ms_per_step": round(dt_ext / n_ext * 1e3, 5)}
+        sustain.update(call_stats(w, st.lens, ext_s, peak))
     clk = clocks.stop()
-    dt_local = t0.elapsed_time(t1) * 1e-3
     dt = max_over_ranks(dt_local, world, dev)
-    attn_s = [ev[i][0][l].elapsed_time(ev[i][1][l]) * 1e-3 for i in range(K) for l in range(L)]
     status = int(st.status.item())
+    samples = {w.name: [st.sample(int(np.argmax(lens)))]} if rank == 0 else {}
 
-    kv_log = kv_bytes_logical(w, st.lens) * L
-    kv_uni = kv_bytes_unique(w, st.lens) * L
+    kv_log = kv_bytes_logical(w, lens) * L
+    kv_uni = kv_bytes_unique(w, lens) * L
     total_kv = sum_over_ranks(kv_log * K, world, dev)
     value = total_kv / dt / 1e9
     # the timed call appends too: its rows count (0.04 % of the 7B layer's bytes)
-    attn_bytes = attention_alg_bytes(w, st.lens) + append_alg_bytes(w)
+    head = call_stats(w, lens, attn_s, peak)
+    attn_bytes = head["alg_bytes_per_launch"]
     attn_avg = statistics.fmean(attn_s)
-    peak, peak_src = measured_peaks()
     achieved = attn_bytes / attn_avg / 1e9
+    if clk.get("sm_mhz"):
+        head["us_median_x_sm_mhz"] = round(head["us_per_layer_median"] * clk["sm_mhz"], 1)
     sha = kernel_sources_sha()
     traffic = (NCU_TRAFFIC.get("bytes_per_launch")
                if NCU_TRAFFIC.get("sources_sha") == sha and NCU_TRAFFIC.get("workload") == w.name
@@ -457,9 +582,23 @@ def run_ours(args):
     if w.graph:   # the same step replayed as one CUDA graph (buckets 1..S, padding)
         graph, dt, value, dt_local = run_graph(st, K, Wm, world, dev, dt, kv_log)
     e2e = run_e2e(st, args, dev, world)
+    configs = None
+    if world == 1 and not args.no_configs and w.name == DEFAULT_WORKLOAD:
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        del st
+        torch.cuda.empty_cache()
+        configs = {w.name: dict(head, kind="timed (the headline line)", ms_per_step=round(
+            dt / K * 1e3, 5), device_status=status, kernel=decode_kernel_name(w) + (
+                " + paged_decode_reduce_kernel" if paged_parts(w, args.partition) > 1 else ""),
+            partition_tokens=paged_partition(w, args.partition))}
+        for name in CONFIG_SET:
+            configs[name], samples[name] = run_config(name, args, dev, peak)
+        configs["_note"] = (f"each workload timed in this process with the same steps / warm-up "
+                            f"({K} / {Wm}); frac = algorithmic bytes per launch / launch time / "
+                            f"{peak} GB/s; {nsm} SMs")
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args)
+        cpu = cpu_baseline(args, samples=samples, configs=configs)
     if rank != 0:
         return
     line = {
@@ -467,37 +606,64 @@ def run_ours(args):
         "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": workload_config(w, st.lens, st.eng.num_blocks),
-        "launch": {"partition_tokens": st.P, "max_partitions": st.max_parts,
+        "config": workload_config(w, lens, nb),
+        "launch": {"partition_tokens": paged_partition(w, args.partition),
                    "parallelism": f"replicas x{world}"},
         "kv_gb_per_step": {"logical": kv_log / 1e9, "unique": kv_uni / 1e9},
         "value_unique_gbs": round(sum_over_ranks(kv_uni * K, world, dev) / dt / 1e9, 2),
         "decode_tokens_per_s": round(world * w.num_seqs * K / dt, 1),
         "attention_us_per_layer": round(attn_avg * 1e6, 3),
-        "attention_us_p10_median_p90": [round(float(np.percentile(attn_s, q)) * 1e6, 3)
-                                        for q in (10, 50, 90)],
+        "attention_us_median": head["us_per_layer_median"],
+        "attention_us_p10_median_p90": [head["us_per_layer_p10_p90"][0],
+                                        head["us_per_layer_median"],
+                                        head["us_per_layer_p10_p90"][1]],
+        "attention_us_median_x_sm_mhz": head.get("us_median_x_sm_mhz"),
         "append_plus_attention_us_per_layer": round(dt_local / K / L * 1e6, 3),
         "decode_tokens_per_s_model": model_tokens_per_s(w, dt_local / K / L),
-        "append": "fused into the decode kernel" if st.fused() else "append kernel, then decode",
+        "append": "fused into the decode kernel" if decode_kernel_name(w) ==
+                  "paged_decode_mma2_kernel" and w.kv_dtype == "bf16"
+                  else "append kernel, then decode",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     "frac_median": head["frac_median"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if peak_src == "measured" else "fallback 6800 GB/s",
                      "kernel": decode_kernel_name(w) + (" + paged_decode_reduce_kernel"
-                                                        if st.max_parts > 1 else ""),
+                                                        if paged_parts(w, args.partition) > 1
+                                                        else ""),
                      "alg_bytes_per_launch": attn_bytes,
                      "frac_of_in_run_copy": round(achieved / bw["copy_gbs"], 4) if bw else None,
                      "frac_of_in_run_read": round(achieved / bw["read_gbs"], 4) if bw else None},
+        "sustained": sustain,
         "in_run_bandwidth_gbs": {k: round(v, 1) for k, v in bw.items()} if bw else None,
+        "configs": configs,
         "graph": graph,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * st.launches_per_step(),
+        "gpu_launches": K * launches_per_step(w, args.partition),
         "clocks": clk,
         "device_status": status,
         "kernel_sources_sha": sha,
     }
     print(json.dumps(line), flush=True)
+
+
+def paged_partition(w, partition=0) -> int:
+    import paged_kv_cache_295_gb300 as pkv
+    lens = W.context_lens(w)
+    return pkv.partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads, int(lens.max()),
+                                partition)
+
+
+def paged_parts(w, partition=0) -> int:
+    return max(1, -(-int(W.context_lens(w).max()) // paged_partition(w, partition)))
+
+
+def launches_per_step(w, partition=0) -> int:
+    """Our kernels per step: per layer one decode (with the append fused in,
+    else an append kernel too) and one reduce if split."""
+    fused = decode_kernel_name(w) == "paged_decode_mma2_kernel" and w.kv_dtype == "bf16"
+    return w.num_layers * ((1 if fused else 2) + (1 if paged_parts(w, partition) > 1 else 0))
 
 
 def run_graph(st, K, Wm, world, dev, dt_eager, kv_log):
@@ -1358,40 +1524,119 @@ class OracleStep:
         return int(self.lens[s]) * 2 * row_bytes(w)
 
 
+def _affinity_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(wname, seqs, steps, warm, ready, go, results):
+    """One reference worker process: the oracle on its own sequences of layer 0,
+    one sequence per step, after every worker has built its inputs."""
+    w = WORKLOADS[wname]
+    st = OracleStep(w, sorted(set(seqs)))
+    order = [seqs[i % len(seqs)] for i in range(warm + steps)]
+    for i in range(warm):
+        st.run(order[i])
+    ready.release()
+    go.wait()
+    t0, byts = time.monotonic(), 0
+    for i in range(steps):
+        byts += st.run(order[warm + i])
+    results.put((byts, t0, time.monotonic()))
+
+
 def run_reference(args):
+    """The oracle on this host's cores: ``--cpu-cores`` worker processes (all
+    the cores this process may run on by default), one NumPy thread each; a
+    step is one sequence of layer 0 per worker, worker i taking sequences i,
+    i + N, ... in turn."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = workload_of(args)
     K, Wm = args.steps, args.warmup
-    order = [i % w.num_seqs for i in range(Wm + K)]
-    st = OracleStep(w, sorted(set(order)))
-    for i in range(Wm):
-        st.run(order[i])
-    byts, t = 0, time.perf_counter()
-    for i in range(K):
-        byts += st.run(order[Wm + i])
-    dt = time.perf_counter() - t
+    cores = args.cpu_cores or _affinity_cores()
+    cores = max(1, min(cores, w.num_seqs))
+    if cores == 1:
+        order = [i % w.num_seqs for i in range(Wm + K)]
+        st = OracleStep(w, sorted(set(order)))
+        for i in range(Wm):
+            st.run(order[i])
+        byts, t = 0, time.perf_counter()
+        for i in range(K):
+            byts += st.run(order[Wm + i])
+        dt = time.perf_counter() - t
+        nb = st.nb
+    else:
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        ready, go, results = ctx.Semaphore(0), ctx.Event(), ctx.Queue()
+        procs = [ctx.Process(target=_oracle_worker,
+                             args=(w.name, list(range(i, w.num_seqs, cores)), K, Wm, ready, go,
+                                   results)) for i in range(cores)]
+        for pr in procs:
+            pr.start()
+        for _ in procs:
+            ready.acquire()
+        go.set()
+        res = [results.get() for _ in procs]
+        for pr in procs:
+            pr.join()
+        byts = sum(r[0] for r in res)
+        dt = max(r[2] for r in res) - min(r[1] for r in res)
+        nb = W.num_blocks(w, W.context_lens(w))
     value = byts / dt / 1e9
-    sample = (f"layer 0, one sequence per step in order 0..{w.num_seqs - 1} (repeating), "
-              f"{K} steps, numpy float64 oracle, 1 thread")
+    sample = (f"layer 0, one sequence per step per worker ({cores} worker process"
+              f"{'es' if cores > 1 else ''}, sequences dealt round-robin), {K} steps each, "
+              "numpy float64 oracle, 1 thread per process")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(dt / K * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, st.lens, st.nb),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "data": "synthetic", "config": workload_config(w, W.context_lens(w), nb),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample, "cpu_model": _cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(args):
-    """The oracle timed on this host (1 thread) on a bounded sample, in a fresh process."""
+def oracle_check(samples, configs):
+    """The oracle on each sampled sequence (the host copies of what the kernel
+    read), against the output row the kernel wrote: max-abs error per workload,
+    added to its ``configs`` record."""
+    from oracle import attention as OA
+    out = {}
+    for name, rows in samples.items():
+        errs, ctxs = [], []
+        for smp in rows:
+            nb = smp["k"].shape[0]
+            ref = OA.paged_attention_decode(
+                smp["q"], smp["k"], smp["v"], np.arange(nb, dtype=np.int64)[None, :],
+                np.array([smp["context"]]), smp["scale"], smp["q_dtype"], smp["kv_dtype"],
+                smp["k_scale"], smp["v_scale"])
+            errs.append(float(np.abs(smp["out"].astype(np.float64) - ref).max()))
+            ctxs.append(smp["context"])
+        tol = ORACLE_TOL[rows[0]["kv_dtype"]]
+        rec = {"seqs": [r["seq"] for r in rows], "contexts": ctxs, "layer": rows[0]["layer"],
+               "max_abs_err": max(errs), "tol": tol, "ok": bool(max(errs) <= tol)}
+        out[name] = rec
+        if configs is not None and name in configs:
+            configs[name]["oracle"] = rec
+    return out
+
+
+def cpu_baseline(args, samples=None, configs=None):
+    """The oracle timed on this host on a bounded sample of the workload, in
+    fresh processes: one worker with one thread, and (decode workloads) one
+    worker per core this process may run on.  With ``samples`` it first checks
+    the kernel's output rows against the oracle."""
     w = workload_of(args)
     prefill = isinstance(w, W.PrefillWorkload)
+    parity = oracle_check(samples, configs) if samples else None
     if isinstance(w, (W.ForkWorkload, W.SwapWorkload)):
         steps = 100
     else:
@@ -1400,25 +1645,62 @@ def cpu_baseline(args):
         steps = int(max(2, min(10 * w.num_seqs, args.cpu_seconds / per_step)))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                RANK="0", WORLD_SIZE="1", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-           w.name, "--steps", str(steps), "--warmup", "1"]
-    try:
-        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
-        line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
-        cb = line["cpu_baseline"]
-        cb["cpu_model"] = _cpu_model()
-        return cb
-    except Exception as e:   # the baseline is reported, never the target
-        return {"value": None, "unit": "TFLOP/s" if prefill else "GB/s", "cores": 1,
-                "kind": "oracle",
-                "sample": f"failed: {type(e).__name__}: {e}"[:200]}
+    unit = "TFLOP/s" if prefill else "GB/s"
+
+    def one(cores, nsteps):
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+               "--workload", w.name, "--steps", str(nsteps), "--warmup", "1",
+               "--cpu-cores", str(cores)]
+        try:
+            r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+            line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+            cb = line["cpu_baseline"]
+            cb["cpu_model"] = _cpu_model()
+            return cb
+        except Exception as e:   # the baseline is reported, never the target
+            return {"value": None, "unit": unit, "cores": cores, "kind": "oracle",
+                    "sample": f"failed: {type(e).__name__}: {e}"[:200]}
+
+    single = one(1, steps)
+    decode = isinstance(w, W.DecodeWorkload)
+    cores = min(_affinity_cores(), w.num_seqs) if decode else 1
+    if cores > 1:
+        cb = one(cores, steps)
+        cb["single_core"] = single
+    else:
+        cb = single
+    cb["threads_per_process"] = 1
+    if parity is not None:
+        cb["oracle_check"] = parity
+    return cb
+
+
+# Arm (implementer 0x41) CPU part numbers -> core names, for hosts whose
+# /proc/cpuinfo gives only the part number.
+_ARM_PARTS = {"0xd0c": "Arm Neoverse-N1", "0xd40": "Arm Neoverse-V1",
+              "0xd49": "Arm Neoverse-N2", "0xd4f": "Arm Neoverse-V2"}
 
 
 def _cpu_model():
     try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.lower().startswith("model name"):
+                name = ln.split(":", 1)[1].strip()
+                if name and name != "-":
+                    return name
+    except Exception:
+        pass
+    try:
+        part = None
         for ln in open("/proc/cpuinfo"):
-            if ln.lower().startswith(("model name", "cpu part")):
+            key = ln.lower()
+            if key.startswith("model name"):
                 return ln.split(":", 1)[1].strip()
+            if key.startswith("cpu part") and part is None:
+                part = ln.split(":", 1)[1].strip().lower()
+        if part is not None:
+            return _ARM_PARTS.get(part, f"Arm part {part}")
     except Exception:
         pass
     import platform
