@@ -85,6 +85,14 @@ __device__ __forceinline__ void s8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo,
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
 }
 
+// a - b on f16x2 words (round to nearest; exact where the difference is an
+// fp16 value, as code + 1152 - 1152 is).
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Two E4M3 codes (low byte first) -> f16x2 with the low byte in the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu),

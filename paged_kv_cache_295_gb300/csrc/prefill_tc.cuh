@@ -40,6 +40,8 @@
 // TMEM is released before the CTA exits.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma_fp8.cuh"
 #include "tcgen05.cuh"
 
@@ -319,7 +321,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int b = 0; b < kPfRawBufs; ++b) valids[b] = b < ntiles ? issue_raw(b, lookup(b)) : 0u;
       // Four codes -> two f16x2.  E4M3: exact.  INT8: code + 1152 (one XOR and
       // two PRMT): in K it adds the same 1152 * sum(q) to every logit of a row,
-      // which its softmax cancels; in V the epilogue takes 1152 back off O / l.
+      // which its softmax cancels.  V takes the offset off again (two HSUB2 per
+      // four codes): kept, it would make O about 1152 times the sum of P, and
+      // over tens of thousands of keys the float32 accumulation of those large
+      // products in the tensor cores drifts by more than the 8-bit bound (0.02
+      // on 32K keys with one key 13 nats above the rest, against 1e-2), and the
+      // P the MMA sees (fp16 hi + lo) need not sum to l either.
       auto widen4 = [&](uint32_t w, uint32_t& lo, uint32_t& hi) {
         if constexpr (I8)
           s8x4_to_f16x2x2_biased(w, lo, hi);
@@ -354,20 +361,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // every address is a per-lane offset (unit_off) plus a constant.
         const uint8_t* raw_l = raw + lane * 128;
         uint8_t* dst_l = dst + lane * 128;
+        auto widen_tile = [&](auto exact) {
 #pragma unroll
-        for (int it = 0; it < (kPfKeys / 32) * 8; ++it) {
-          const int rk = (it >> 3) * 32 * 128, u = it & 7;
-          const uint4 c = *reinterpret_cast<const uint4*>(raw_l + rk + unit_off[u]);
-          uint32_t h[8];
-          widen4(c.x, h[0], h[1]);
-          widen4(c.y, h[2], h[3]);
-          widen4(c.z, h[4], h[5]);
-          widen4(c.w, h[6], h[7]);
-          uint8_t* half = dst_l + (u >> 2) * LY::kKVHalf + rk;
-          const int uu = 2 * (u & 3);
-          *reinterpret_cast<uint4*>(half + unit_off[uu]) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(half + unit_off[uu + 1]) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
+          for (int it = 0; it < (kPfKeys / 32) * 8; ++it) {
+            const int rk = (it >> 3) * 32 * 128, u = it & 7;
+            const uint4 c = *reinterpret_cast<const uint4*>(raw_l + rk + unit_off[u]);
+            uint32_t h[8];
+            widen4(c.x, h[0], h[1]);
+            widen4(c.y, h[2], h[3]);
+            widen4(c.z, h[4], h[5]);
+            widen4(c.w, h[6], h[7]);
+            if constexpr (decltype(exact)::value) {   // code + 1152 - 1152: the code, exactly
+#pragma unroll
+              for (int e = 0; e < 8; ++e) h[e] = hsub2_u32(h[e], 0x64806480u);
+            }
+            uint8_t* half = dst_l + (u >> 2) * LY::kKVHalf + rk;
+            const int uu = 2 * (u & 3);
+            *reinterpret_cast<uint4*>(half + unit_off[uu]) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(half + unit_off[uu + 1]) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+        };
+        // INT8 V codes are widened exactly (K keeps the offset, see widen4)
+        if (I8 && is_v)
+          widen_tile(std::true_type{});
+        else
+          widen_tile(std::false_type{});
         fence_proxy_async();   // the stage's generic writes before the MMAs' reads; the
         __syncwarp();          // raw buffer's reads before the next copy into it
         if (lane == 0) {
@@ -523,11 +541,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool pos_scale = sl2 > 0.f;
     uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
     float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units
-    // INT8: the sum of P as the MMA sees it (fp16 hi + lo), the weight of the
-    // V codes' +1152 offset.  It can fall short of l: a P below 2^-14 keeps
-    // fewer bits in fp16 and one below 2^-25 is lost, which a single key far
-    // above the rest makes the common case.
-    float lm = 0.f;
     bool alive = true;
     for (int j = 0; j < my_nt && alive; ++j) {
       const int k0 = j * kPfKeys;
@@ -607,7 +620,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // PV(j-1) must be finished before P is overwritten and before O is scaled
       if (j >= 1 && !tc_wait(smem_u32(&o_done[t]), (j - 1) & 1, abort_flag)) alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
-      float2 lmt = make_float2(0.f, 0.f);   // INT8: this tile's P as the MMA sees it
 #pragma unroll
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
@@ -624,16 +636,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f), ab);   // ab - hi, exact
           wl[e] = FP8 ? pack_f16(lo.x, lo.y) : pack_bf16(lo.x, lo.y);
-          if constexpr (I8) {
-            const float2 lr = __half22float2(*reinterpret_cast<const __half2*>(&wl[e]));
-            lmt = __fadd2_rn(lmt, __fadd2_rn(hi, lr));
-          }
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
             make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
-      if constexpr (I8) lm = lm * alpha + (lmt.x + lmt.y);
       if (__any_sync(0xffffffffu, resc)) {   // after P is out of the registers
         tc_fence_after();
 #pragma unroll
@@ -670,12 +677,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_wait(smem_u32(&o_done[t]), (my_nt - 1) & 1, abort_flag);
     if (__all_sync(0xffffffffu, ok)) {   // warp-uniform: the TMEM load is warp-wide
       tc_fence_after();
-      // 1 / l, times the V scale for 8-bit caches.  INT8: V went in as
-      // code + 1152, so O carries 1152 times the sum of P as the MMA saw it
-      // (lm, rescaled with O and l), which comes off after the division.
+      // 1 / l, times the V scale for 8-bit caches
       const float vsc = FP8 ? __ldg(p.v_scale + g) : 1.f;
       const float inv = l > 0.f ? vsc / l : 0.f;
-      const float off = (I8 && l > 0.f) ? 1152.f * vsc * (lm / l) : 0.f;
       float* orow = p.out + (static_cast<int64_t>(q0 + tok0 + t * TQ + tl) * p.num_q_heads +
                              g * G + r % G) * kPfD;
 #pragma unroll
@@ -686,8 +690,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(orow + c + e) =
-                make_float4(fmaf(o[e], inv, -off), fmaf(o[e + 1], inv, -off),
-                            fmaf(o[e + 2], inv, -off), fmaf(o[e + 3], inv, -off));
+                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
         }
       }
     }

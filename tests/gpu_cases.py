@@ -80,8 +80,11 @@ class SmallCase:
     max_blocks: int
 
 
-def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None) -> tuple:
-    """Build a small case; returns (case, c-pool) after checking both pools agree."""
+def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None, shape_rows=None) -> tuple:
+    """Build a small case; returns (case, c-pool) after checking both pools agree.
+    ``shape_rows(k, v, k_new, v_new, q, starts)`` may change a layer's float32
+    prompt K / V rows ([U, Hkv, D], sequence s's first prompt row at
+    starts[s]), the step's new rows and q in place before they are stored."""
     import paged_kv_cache_295_gb300 as pkv
     from paged_kv_cache_295_gb300.engine import build_prompts
     lens = W.context_lens(w) if lens is None else np.asarray(lens, dtype=np.int64)
@@ -115,6 +118,8 @@ def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None) -> tuple:
     S, hkv, hq, d = len(lens), w.num_kv_heads, w.num_q_heads, w.head_dim
     sd = src_dtype(w)
     kh = W.k_head_scales(w)[None, :, None]
+    own = [len(x) for x in o_slots]
+    starts = np.cumsum([0] + own[:-1]) + (len(o_oslots) if o_oslots is not None else 0)
     pk, pv, kn, vn, qq, ks_l, vs_l = [], [], [], [], [], [], []
     for layer in range(L):
         base = 100 * (layer + 1)
@@ -123,6 +128,8 @@ def make_small(w: W.DecodeWorkload, lens=None, nb=None, layers=None) -> tuple:
         kn32 = W.normal_f32(w.seed, base + 2, (S, hkv, d)) * kh
         vn32 = W.normal_f32(w.seed, base + 3, (S, hkv, d))
         q32 = W.normal_f32(w.seed, base + 4, (S, hq, d))
+        if shape_rows is not None:
+            shape_rows(k32, v32, kn32, vn32, q32, starts)
         pk.append(W.store(k32, sd))
         pv.append(W.store(v32, sd))
         kn.append(W.store(kn32, sd))

@@ -189,6 +189,34 @@ def test_split_count_invariance(torch_cuda, name, decode_path):
     print(f"split invariance {name} {decode_path}: (partition, max |diff|, max diff/bound) {worst}")
 
 
+def _decode_sink(k0):
+    """Position 0 of every sequence far above the rest (as in the prefill
+    test): q is 3 on dimension 0, that key k0 there and 0 elsewhere, the other
+    keys (the step's new ones too) scaled by 1/4."""
+    def shape(k, v, kn, vn, q, starts):
+        q[:, :, 0] = 3.0
+        k *= 0.25
+        kn *= 0.25
+        for s0 in starts:
+            k[s0] = 0.0
+            k[s0, :, 0] = k0
+    return shape
+
+
+@pytest.mark.parametrize("k0", [67, 49])
+@pytest.mark.parametrize("kv", ["int8", "fp8_e4m3", "bf16"])
+def test_long_context_with_an_attention_sink(torch_cuda, decode_path, kv, k0):
+    """32K tokens and one key far above the rest: the other keys' P lie where
+    fp16 (the 8-bit paths' P) keeps few bits or none; the INT8 path's +1152 V
+    offset must still come off exactly once."""
+    w = W.DecodeWorkload(f"sink_{kv}", 2, 8, 2, 128, 16, kv, "bf16", seed=81, ctx_law="fixed")
+    case, _ = GC.make_small(w, lens=[32768, 30001], shape_rows=_decode_sink(k0))
+    eng, outs, st = GC.run_gpu(case)
+    assert st == 0
+    err = _check_layer(case, eng, outs, 0)
+    print(f"decode sink {kv} k0={k0} {decode_path}: max abs err {err}")
+
+
 def test_block_permutation_bit_identical(torch_cuda, decode_path):
     torch = torch_cuda
     w, lens = SMALL["llama7b_mha_bf16"]

@@ -107,29 +107,34 @@ def test_prefill_q_far_outside_fp16_range(lib, kv):
     assert np.abs(got - ref).max() <= (TOL if kv == "bf16" else 1e-2)
 
 
-def _attention_sink(k, v, q, starts):
+def attention_sink(k0):
     """Key 0 of every sequence far above the rest: q is 3 on dimension 0 and
-    that key 67 there (0 elsewhere), the other keys are scaled by 1/4, so its
-    logit sits about 17.8 nats above theirs, which spread a few tenths of a nat
-    around 0.  Their P (about 2^-25.6) is then below what fp16 keeps."""
-    q[:, :, 0] = 3.0
-    k *= 0.25
-    for s0 in starts:
-        k[s0] = 0.0
-        k[s0, :, 0] = 67.0
+    that key k0 there (0 elsewhere), the other keys are scaled by 1/4, so its
+    logit sits about 0.265 k0 nats above theirs, which spread a few tenths of a
+    nat around 0: k0 = 67 puts their P near 2^-25.6 (below every fp16 value),
+    k0 = 49 near 2^-18.7 (fp16 subnormals)."""
+    def shape(k, v, q, starts):
+        q[:, :, 0] = 3.0
+        k *= 0.25
+        for s0 in starts:
+            k[s0] = 0.0
+            k[s0, :, 0] = k0
+    return shape
 
 
+@pytest.mark.parametrize("k0", [67, 49])
 @pytest.mark.parametrize("kv", ["int8", "fp8_e4m3", "bf16"])
-def test_prefill_long_context_with_an_attention_sink(lib, kv):
+def test_prefill_long_context_with_an_attention_sink(lib, kv, k0):
     """32K cached tokens and one key far above the rest: every other key's P
-    is about 2^-25.6, which fp16 does not keep, so the P the MMA sees sums
-    about 3.5e-4 short of the float32 row sum; the INT8 path must weight its
+    is far below the largest, where fp16 keeps few bits or none, so the P the
+    MMA sees sums short of the float32 row sum; the INT8 path must weight its
     +1152 V offset by the former (weighting it by the row sum would be off by
-    about 0.03 here).  The 8-bit bound (1e-2) and the bf16 one (2e-3) hold."""
+    about 0.03 at k0 = 67).  The 8-bit bound (1e-2) and the bf16 one (2e-3)
+    hold."""
     import torch
     w = _w(8, 2, 16)
     dev, host, max_q, max_ctx = build(w, [64, 40], [32768, 32000], kv=kv,
-                                      shape_rows=_attention_sink)
+                                      shape_rows=attention_sink(k0))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = run_gpu(w, dev, max_q, max_ctx, causal=True, status=status)
     assert int(status.item()) == 0
@@ -137,7 +142,9 @@ def test_prefill_long_context_with_an_attention_sink(lib, kv):
                                       host["tables"], host["ctx"], w.scale, "bf16", kv,
                                       causal=True, k_scale=host["ks"], v_scale=host["vs"])
     assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= (TOL if kv == "bf16" else 1e-2)
+    err = np.abs(got - ref).max()
+    print(f"prefill sink {kv} k0={k0}: max abs err {err:.3e}")
+    assert err <= (TOL if kv == "bf16" else 1e-2)
 
 
 def test_single_token_chunks_match_decode_kernel(lib):
