@@ -52,11 +52,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "73c96296143abde4", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239850 GB read + 4.790 MB
-               # written, plus the reduce kernel's 1.434 MB
-               # (profiles/decode_mma2_llama7b_bf16.md)
-               "bytes_per_launch": 1239849984 + 4789760 + 1433856}
+NCU_TRAFFIC = {"sources_sha": "af65088d4dc1ad71", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239752 GB read + 5.341 MB
+               # written, plus the reduce kernel's 1.434 MB read
+               "bytes_per_launch": 1239752448 + 5341184 + 1433600}
 
 
 def parse_args(argv=None):
@@ -81,6 +80,8 @@ def parse_args(argv=None):
                          "process may run on)")
     ap.add_argument("--no-bandwidth-ref", action="store_true",
                     help="skip the in-run copy/read reference kernels (profiling runs)")
+    ap.add_argument("--bandwidth-gb", type=float, default=4.0,
+                    help="bytes the in-run copy and read kernels move (GB; smaller for captures)")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -530,7 +531,8 @@ def run_ours(args):
     K, Wm = args.steps, args.warmup
     if Wm < 3:
         raise SystemExit("--warmup must be >= 3")
-    bw = None if args.no_bandwidth_ref else in_run_bandwidth(dev)
+    bw = None if args.no_bandwidth_ref else in_run_bandwidth(
+        dev, nbytes=int(args.bandwidth_gb * (1 << 30)) // 64 * 64)
     st = DeviceStep(w, dev, partition=args.partition)
     lens, nb = st.lens, st.eng.num_blocks
     L = w.num_layers
