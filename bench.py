@@ -337,6 +337,8 @@ class DeviceStep:
         self.out = torch.empty((S, hq, d), dtype=torch.float32, device=device)
         self.ws = eng.workspace_for(S, hq, self.max_ctx, partition, device=device)
         self.P = pkv.partition_tokens(S, hq, hkv, self.max_ctx, partition)
+        if partition == 0 and w.kv_dtype in ("fp8_e4m3", "int8"):   # 8-bit rows: twice
+            self.P = min(4096, 2 * self.P)
         self.max_parts = max(1, -(-self.max_ctx // self.P))
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         torch.cuda.synchronize(device)
@@ -651,10 +653,14 @@ def run_ours(args):
 
 
 def paged_partition(w, partition=0) -> int:
+    """The partition the library picks (8-bit caches: twice the 16-bit one)."""
     import paged_kv_cache_295_gb300 as pkv
     lens = W.context_lens(w)
-    return pkv.partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads, int(lens.max()),
-                                partition)
+    P = pkv.partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads, int(lens.max()),
+                             partition)
+    if partition == 0 and w.kv_dtype in ("fp8_e4m3", "int8"):
+        P = min(4096, 2 * P)
+    return P
 
 
 def paged_parts(w, partition=0) -> int:

@@ -275,17 +275,20 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, const int64_t
 
 /* Tokens per split-KV partition that paged_attention_decode uses for this
  * problem when its partition_tokens argument is 0 (depends on the current
- * device's SM count and on the group size num_q_heads / num_kv_heads); a
- * non-zero partition_tokens (a multiple of 64) is returned as is.  Returns 0
- * on bad arguments (negative sizes, num_q_heads not a multiple of
- * num_kv_heads, partition_tokens not a multiple of 64). */
+ * device's SM count and on the group size num_q_heads / num_kv_heads) on f32
+ * and bf16 caches; FP8 and INT8 caches, whose rows are half the bytes, take
+ * twice this, at most 4096.  A non-zero partition_tokens (a multiple of 64) is
+ * returned as is.  Returns 0 on bad arguments (negative sizes, num_q_heads not
+ * a multiple of num_kv_heads, partition_tokens not a multiple of 64). */
 int32_t paged_attention_partition_tokens(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t max_context_len,
                                          int32_t partition_tokens);
 
 /* Device scratch that paged_attention_decode needs for its split-KV partials
  * (0 when every sequence fits one partition): num_seqs * num_q_heads *
- * ceil(max_context_len / P) * (head_dim + 2) * 4 bytes, P as above. */
+ * ceil(max_context_len / P) * (head_dim + 2) * 4 bytes, P as above for a
+ * 16-bit cache - enough for 8-bit caches too, whose automatic partitions are
+ * longer. */
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim,
                                        int32_t max_context_len, int32_t partition_tokens);

@@ -206,8 +206,16 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if ((kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) && (!k_scale || !v_scale))
     return PKV_ERR_INVALID_ARG;
 
-  const int32_t P =
+  int32_t P =
       resolve_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len, partition_tokens);
+  // 8-bit rows are half the bytes of 16-bit ones, so the automatic partition
+  // (counted in tokens for 16-bit rows) doubles, at most 4096: each CTA then
+  // moves the bytes it would for a bf16 cache and its fixed start-up and
+  // epilogue weigh the same.  Measured on the 7B-shaped layer: FP8 114.6 ->
+  // 112.1 us, INT8 116.6 -> 115.3.  The workspace this needs is never more
+  // than paged_attention_workspace_bytes gives for partition_tokens = 0.
+  if (partition_tokens == 0 && (kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) && P < 4096)
+    P *= 2;
   const int32_t parts = parts_for(max_context_len, P);
   const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
                                                       head_dim, max_context_len, P);
