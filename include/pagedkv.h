@@ -456,8 +456,8 @@ pkv_status swap_blocks(void* base, int32_t num_planes, int64_t plane_stride_byte
  * tensor cores (Q K^T and P V with P carried as bf16 hi + lo parts).  FP8 and
  * INT8 tiles are widened to fp16 in shared memory (exact), so the
  * contractions run in fp16 (each q row scaled by a power of two into fp16's
- * range, P as fp16 hi + lo), the K scale folded into the logit scale and the
- * V scale into the output.
+ * range, P as one fp16 value, as in decode), the K scale folded into the
+ * logit scale and the V scale into the output.
  * Supported: head_dim 128, bf16 q, bf16, FP8-E4M3 or INT8 caches (8-bit
  * caches need both scales), G = num_q_heads / num_kv_heads
  * <= 16, block_size a power of two in [8, 4096], 16-byte aligned q, caches and

@@ -17,7 +17,8 @@
 //   P_t  = 2^(S_t*scale*log2e - m)  in tile t's softmax warpgroup, one TMEM
 //                                   lane = one row
 //   O_t += P_t V      tcgen05.mma M=128 N=128 K=64    A = P_t (smem, K-major,
-//                                                          bf16 hi + lo parts)
+//                                                          bf16 hi + lo parts;
+//                                                          8-bit caches: fp16)
 //                                                     B = V tile (smem, MN-major)
 //
 // for t = A (the earlier tokens) and B.  TMEM: per tile, Q in 64 columns (row =
@@ -53,7 +54,7 @@ constexpr int kPfD = 128;
 constexpr int kPfThreads = 384;   // 2 softmax warpgroups, K producer, QK issuer, PV issuer,
                                   // V producer
 constexpr int kPfStages = 5;       // 16-bit caches
-constexpr int kPfStagesFp8 = 3;    // FP8 caches: two stages' room holds the raw tiles
+constexpr int kPfStagesFp8 = 3;    // 8-bit caches: the raw tiles take two stages' room
 constexpr int kPfRawBufs = 4;      // FP8 raw tiles in flight per tensor
 
 struct PrefillParams {
@@ -116,17 +117,18 @@ __device__ __forceinline__ void pf_ld64(uint32_t taddr, float* v) {
 }
 
 struct PfLayout {
-  // [P_A: hi 16 KB, lo 16 KB][P_B][FP8 only: raw tiles, K x4 then V x4, 8 KB each]
+  // [P_A][P_B]: 16-bit caches bf16 hi 16 KB + lo 16 KB per tile, 8-bit caches
+  // fp16 16 KB; [8-bit only: raw tiles, K x4 then V x4, 8 KB each]
   // [stages: K 16 KB, V 16 KB]
   static constexpr int kPPart = kPfRows * 128;         // [128 rows][64 keys x 2 B]
-  static constexpr int kPBuf = 2 * kPPart;             // hi + lo
+  __host__ __device__ static constexpr int pbuf(bool fp8) { return fp8 ? kPPart : 2 * kPPart; }
   static constexpr int kP = 0;                         // P_A, then P_B
   static constexpr int kKVHalf = kPfKeys * 128;        // [64 keys][128 B]
   static constexpr int kStage = 4 * kKVHalf;           // K (2 halves) + V (2 halves)
-  static constexpr int kRaw = kP + 2 * kPBuf;          // FP8 raw tiles
+  __host__ __device__ static constexpr int raw(bool fp8) { return kP + 2 * pbuf(fp8); }
   static constexpr int kRawTile = kPfKeys * 128;       // [64 keys][128 codes]
   static constexpr int kRawBytes = 2 * kPfRawBufs * kRawTile;   // (K, V) x buffers
-  __host__ __device__ static constexpr int ring(bool fp8) { return kRaw + (fp8 ? kRawBytes : 0); }
+  __host__ __device__ static constexpr int ring(bool fp8) { return raw(fp8) + (fp8 ? kRawBytes : 0); }
   static constexpr size_t bytes(int stages, bool fp8) {
     return 1024 + static_cast<size_t>(ring(fp8)) + static_cast<size_t>(stages) * kStage;
   }
@@ -286,8 +288,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // into the stage, in the swizzled K-major halves the MMAs read, and
       // arrives on the stage's barrier.  Tile j + kPfRawBufs's copy goes into
       // the raw buffer tile j has just left, so kPfRawBufs copies are in flight.
-      const uint32_t raw_a = sma + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
-      const uint8_t* raw_p = sm + LY::kRaw + (is_v ? kPfRawBufs * LY::kRawTile : 0);
+      const uint32_t raw_a = sma + LY::raw(true) + (is_v ? kPfRawBufs * LY::kRawTile : 0);
+      const uint8_t* raw_p = sm + LY::raw(true) + (is_v ? kPfRawBufs * LY::kRawTile : 0);
       // Lane i's block of box i of tile jj: -1 past the context, -2 out of range.
       // Looked up one tile ahead of its copy, so the table load's latency
       // overlaps the widening of the tile in between.
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // over tens of thousands of keys the float32 accumulation of those large
       // products in the tensor cores drifts by more than the 8-bit bound (0.02
       // on 32K keys with one key 13 nats above the rest, against 1e-2), and the
-      // P the MMA sees (fp16 hi + lo) need not sum to l either.
+      // P the MMA sees (rounded to fp16) need not sum to l either.
       auto widen4 = [&](uint32_t w, uint32_t& lo, uint32_t& hi) {
         if constexpr (I8)
           s8x4_to_f16x2x2_biased(w, lo, hi);
@@ -463,13 +465,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_fence_after();
           const uint32_t dO = tm + 256 * t + 2 * kPfKeys;
-          const uint64_t pd = tc_desc(sma + LY::kP + t * LY::kPBuf, 0, 1024);
+          const uint64_t pd = tc_desc(sma + LY::kP + t * LY::pbuf(FP8), 0, 1024);
           const uint64_t vd = tc_desc(vb, LY::kKVHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < kPfKeys / 16; ++kk) {
             const uint64_t bdesc = vd + ((kk * 2048) >> 4);
             tc_mma(dO, pd + ((kk * 32) >> 4), bdesc, idesc_pv, (j > 0 || kk > 0));
-            tc_mma(dO, pd + ((LY::kPPart + kk * 32) >> 4), bdesc, idesc_pv, 1);
+            if constexpr (!FP8) tc_mma(dO, pd + ((LY::kPPart + kk * 32) >> 4), bdesc, idesc_pv, 1);
           }
           tc_commit(smem_u32(&o_done[t]));
         }
@@ -539,7 +541,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int last = p.causal ? qpos : ctx - 1;         // last key it sees
     const float sl2 = FP8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) * q_unscale : p.qk_scale_log2;
     const bool pos_scale = sl2 > 0.f;
-    uint8_t* pb = sm + LY::kP + t * LY::kPBuf;
+    uint8_t* pb = sm + LY::kP + t * LY::pbuf(FP8);
     float m = -CUDART_INF_F, l = 0.f;                   // m in scaled (log2) units
     bool alive = true;
     for (int j = 0; j < my_nt && alive; ++j) {
@@ -620,26 +622,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // PV(j-1) must be finished before P is overwritten and before O is scaled
       if (j >= 1 && !tc_wait(smem_u32(&o_done[t]), (j - 1) & 1, abort_flag)) alive = false;
       if (!__all_sync(0xffffffffu, alive)) break;
+      // P for the MMA.  16-bit caches: bf16 hi part, then what it left (about
+      // 2^-17 relative together; bf16 alone would cost up to 2.7e-3 on N(0,1)
+      // inputs against the 2e-3 bound).  8-bit caches: fp16 alone, as in the
+      // decode kernels (2^-11 relative, within their 1e-2 bound by far).
 #pragma unroll
       for (int u = 0; u < 8; ++u) {   // 8 keys per 16-byte chunk
         uint32_t wh[4], wl[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {   // hi part, then what it left (bf16; fp16 for FP8)
+        for (int e = 0; e < 4; ++e) {
           const float2 ab = make_float2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
-          float2 hi;
-          if (FP8) {
+          if constexpr (FP8) {
             wh[e] = pack_f16(ab.x, ab.y);
-            hi = __half22float2(*reinterpret_cast<const __half2*>(&wh[e]));
           } else {
             wh[e] = pack_bf16(ab.x, ab.y);
-            hi = make_float2(__uint_as_float(wh[e] << 16), __uint_as_float(wh[e] & 0xFFFF0000u));
+            const float2 hi =
+                make_float2(__uint_as_float(wh[e] << 16), __uint_as_float(wh[e] & 0xFFFF0000u));
+            const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f), ab);   // ab - hi, exact
+            wl[e] = pack_bf16(lo.x, lo.y);
           }
-          const float2 lo = __ffma2_rn(hi, make_float2(-1.f, -1.f), ab);   // ab - hi, exact
-          wl[e] = FP8 ? pack_f16(lo.x, lo.y) : pack_bf16(lo.x, lo.y);
         }
         *reinterpret_cast<uint4*>(pb + swz(r, u)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
-            make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        if constexpr (!FP8)
+          *reinterpret_cast<uint4*>(pb + LY::kPPart + swz(r, u)) =
+              make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
       if (__any_sync(0xffffffffu, resc)) {   // after P is out of the registers
         tc_fence_after();

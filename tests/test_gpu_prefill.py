@@ -127,10 +127,10 @@ def attention_sink(k0):
 def test_prefill_long_context_with_an_attention_sink(lib, kv, k0):
     """32K cached tokens and one key far above the rest: every other key's P
     is far below the largest, where fp16 keeps few bits or none, so the P the
-    MMA sees sums short of the float32 row sum; the INT8 path must weight its
-    +1152 V offset by the former (weighting it by the row sum would be off by
-    about 0.03 at k0 = 67).  The 8-bit bound (1e-2) and the bf16 one (2e-3)
-    hold."""
+    MMA sees sums short of the float32 row sum.  The INT8 path widens V
+    exactly: a +1152 offset kept in V and taken off in the epilogue would be
+    off by about 0.03 at k0 = 67.  The 8-bit bound (1e-2) and the bf16 one
+    (2e-3) hold."""
     import torch
     w = _w(8, 2, 16)
     dev, host, max_q, max_ctx = build(w, [64, 40], [32768, 32000], kv=kv,
