@@ -56,6 +56,7 @@ constexpr int kPfThreads = 384;   // 2 softmax warpgroups, K producer, QK issuer
 constexpr int kPfStages = 5;       // 16-bit caches
 constexpr int kPfStagesFp8 = 3;    // 8-bit caches: the raw tiles take two stages' room
 constexpr int kPfRawBufs = 4;      // FP8 raw tiles in flight per tensor
+constexpr int kPfRankSeqs = 128;   // sequences ranked by context length for the work order
 
 struct PrefillParams {
   const __nv_bfloat16* q;        // [T, Hq, D]
@@ -156,18 +157,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __shared__ uint64_t key_mask[STAGES];   // per stage: keys with cache data
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int seq_sh;
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sma = smem_u32(sm);
   volatile int* abort_flag = &abort_sh;
 
-  const int s = blockIdx.z, g = blockIdx.y;
-  const int pair = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Work order.  CTAs start roughly in the order of their linear block index,
+  // so that index is mapped to (sequence, pair, KV head) longest context
+  // first: a long prompt's CTAs then start in the first waves instead of
+  // trailing the grid.  KV heads run fastest (their CTAs are alike), then the
+  // pairs of a sequence (latest, i.e. heaviest, first), then the sequences by
+  // context length, descending, ties by index.  Each CTA ranks the sequences
+  // itself (one pass over the context lengths per thread), so this is done
+  // for up to kPfRankSeqs sequences; more keep their order.
+  const uint64_t lin = blockIdx.x + static_cast<uint64_t>(gridDim.x) *
+                                        (blockIdx.y + static_cast<uint64_t>(gridDim.y) * blockIdx.z);
+  const int g = static_cast<int>(lin % gridDim.y);
+  const uint64_t unit = lin / gridDim.y;
+  const int pair = static_cast<int>(gridDim.x - 1 - unit % gridDim.x);
+  const int rank = static_cast<int>(unit / gridDim.x);   // < gridDim.z
+  int s = rank;
+  if (gridDim.z <= kPfRankSeqs) {
+    if (tid == 0) seq_sh = rank;   // kept if no sequence claims the rank
+    __syncthreads();
+    if (tid < static_cast<int>(gridDim.z)) {
+      const int c = __ldg(p.context_lens + tid);
+      int r = 0;
+      for (int i = 0; i < static_cast<int>(gridDim.z); ++i) {
+        const int ci = __ldg(p.context_lens + i);
+        r += (ci > c || (ci == c && i < tid)) ? 1 : 0;
+      }
+      if (r == rank) seq_sh = tid;   // ranks are distinct: one writer
+    }
+    __syncthreads();
+    s = seq_sh;
+  }
 
   const int q0 = __ldg(p.query_start + s);
   const int q1 = __ldg(p.query_start + s + 1);
   if (q0 < 0 || q1 < q0 || q1 > p.num_tokens) {   // rows outside q / out: touch nothing
-    if (blockIdx.x == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+    if (pair == 0 && g == 0 && tid == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
     return;
   }
   const int n = q1 - q0;
