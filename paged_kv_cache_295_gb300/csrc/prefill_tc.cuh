@@ -393,11 +393,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // every address is a per-lane offset (unit_off) plus a constant.
         const uint8_t* raw_l = raw + lane * 128;
         uint8_t* dst_l = dst + lane * 128;
+        // All of a lane's codes are loaded before the first store: the
+        // compiler cannot tell the raw buffer from the stage, so a load after
+        // a store would wait for it, and one load's latency per 16 codes made
+        // the widening of a tile take about 2,000 cycles.
         auto widen_tile = [&](auto exact) {
+          constexpr int kSteps = (kPfKeys / 32) * 8;
+          uint4 cs[kSteps];
 #pragma unroll
-          for (int it = 0; it < (kPfKeys / 32) * 8; ++it) {
+          for (int it = 0; it < kSteps; ++it)
+            cs[it] = *reinterpret_cast<const uint4*>(raw_l + (it >> 3) * 32 * 128 + unit_off[it & 7]);
+#pragma unroll
+          for (int it = 0; it < kSteps; ++it) {
             const int rk = (it >> 3) * 32 * 128, u = it & 7;
-            const uint4 c = *reinterpret_cast<const uint4*>(raw_l + rk + unit_off[u]);
+            const uint4 c = cs[it];
             uint32_t h[8];
             widen4(c.x, h[0], h[1]);
             widen4(c.y, h[2], h[3]);
