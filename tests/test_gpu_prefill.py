@@ -147,6 +147,29 @@ def test_prefill_long_context_with_an_attention_sink(lib, kv, k0):
     assert err <= (TOL if kv == "bf16" else 1e-2)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("chunk,prefix", [
+    ([10, 30, 10, 30, 20], [50, 30, 50, 30, 40]),   # equal contexts: ties in the work order
+    ([3, 1, 2] * 44, [(7 * i) % 61 for i in range(132)]),   # 132 sequences: not ranked
+])
+def test_work_order_covers_every_sequence(lib, kv, chunk, prefix):
+    """The kernel maps its blocks to (sequence, pair, KV head) longest context
+    first, ranking up to 128 sequences itself: with tied contexts and with
+    more sequences than it ranks, every row of every chunk still matches the
+    oracle (a sequence left out or done twice would not)."""
+    import torch
+    w = _w(8, 2, 16)
+    dev, host, max_q, max_ctx = build(w, chunk, prefix, kv=kv)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_gpu(w, dev, max_q, max_ctx, causal=True, status=status)
+    assert int(status.item()) == 0
+    ref = OPF.paged_attention_prefill(host["q"], host["qs"], host["kc"], host["vc"],
+                                      host["tables"], host["ctx"], w.scale, "bf16", kv,
+                                      causal=True, k_scale=host["ks"], v_scale=host["vs"])
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= (TOL if kv == "bf16" else 1e-2)
+
+
 def test_single_token_chunks_match_decode_kernel(lib):
     """A chunk of one token is a decode step: both kernels, both within tolerance
     of the oracle, on the same cache."""
