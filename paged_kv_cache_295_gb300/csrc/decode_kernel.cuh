@@ -384,14 +384,37 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
   if (nparts <= 1) return;   // written directly by the main kernel
   const float* ml = p.part_ml + static_cast<int64_t>(sh) * p.max_parts * 2;
   const float* po = p.part_o + static_cast<int64_t>(sh) * p.max_parts * D;
+  // Eight partitions per step with their own accumulators, so eight loads are
+  // in flight at once: one at a time, a long context's 60-odd partials cost
+  // as many round trips to L2 in a row.
+  constexpr int U = 8;
   float M = -CUDART_INF_F;
+#pragma unroll U
   for (int i = 0; i < nparts; ++i) M = fmaxf(M, ml[2 * i]);
   float L = 0.f;
+#pragma unroll U
   for (int i = 0; i < nparts; ++i) L = fmaf(ml[2 * i + 1], exp2f(ml[2 * i] - M), L);
   const float invL = 1.f / L;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    int i = 0;
+    for (; i + U <= nparts; i += U) {
+      float x[U], w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        x[u] = po[static_cast<int64_t>(i + u) * D + d];
+        w[u] = ml[2 * (i + u)];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = fmaf(x[u], exp2f(w[u] - M), acc[u]);
+    }
+    for (int u = 0; i < nparts; ++i, ++u)
+      acc[u] = fmaf(po[static_cast<int64_t>(i) * D + d], exp2f(ml[2 * i] - M), acc[u]);
     float O = 0.f;
-    for (int i = 0; i < nparts; ++i) O = fmaf(po[static_cast<int64_t>(i) * D + d], exp2f(ml[2 * i] - M), O);
+#pragma unroll
+    for (int u = 0; u < U; ++u) O += acc[u];
     p.out[static_cast<int64_t>(sh) * D + d] = O * invL;
   }
 }
