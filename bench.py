@@ -52,10 +52,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "4c7857ceaea219d4", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239788 GB read + 5.001 MB
+NCU_TRAFFIC = {"sources_sha": "d214cba9e03a9299", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239785 GB read + 4.838 MB
                # written, plus the reduce kernel's 1.434 MB read
-               "bytes_per_launch": 1239788288 + 5000704 + 1434112}
+               "bytes_per_launch": 1239785472 + 4837888 + 1434112}
 
 
 def parse_args(argv=None):
