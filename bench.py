@@ -52,10 +52,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "d214cba9e03a9299", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239785 GB read + 4.838 MB
-               # written, plus the reduce kernel's 1.434 MB read
-               "bytes_per_launch": 1239785472 + 4837888 + 1434112}
+NCU_TRAFFIC = {"sources_sha": "7f7d5c328970e0ce", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239752 GB read + 5.019 MB
+               # written, plus the reduce kernel's 1.434 MB read and 2 KB written
+               "bytes_per_launch": 1239752448 + 5019392 + 1433856 + 2048}
 
 
 def parse_args(argv=None):

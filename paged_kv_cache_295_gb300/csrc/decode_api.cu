@@ -65,6 +65,18 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
   if (want < floor_g) want = floor_g;
   int64_t P = 256;
   while (P * 2 <= want && P < 4096) P *= 2;
+  const int64_t slots = 3LL * device_sm_count();
+  const int64_t ctx = max_ctx > 0 ? max_ctx : 1;
+  const int64_t heads = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  // Long contexts: past 32 partitions per sequence the grid has CTAs to
+  // spare, and fewer, longer partitions spend less on each CTA's start-up,
+  // epilogue and partials.  P doubles (up to 4096) while a sequence still
+  // has more than 32 partitions and the doubled grid keeps two waves of CTA
+  // slots.  Measured on 8 sequences of 128K tokens, 8 KV heads (GQA-4):
+  // 386.6 us per layer at 4096 against 391.8 at 2048; the 7B- and 70B-shaped
+  // layers (2 to 8 partitions) keep 1024 and 2048, their best.
+  while (P < 4096 && (ctx + P - 1) / P > 32 && heads * ((ctx + 2 * P - 1) / (2 * P)) >= 2 * slots)
+    P *= 2;
   // Small batches: the rule above bottoms out at 256, but when the grid is
   // only a wave or two, each CTA's fixed start-up and epilogue dominate and
   // fewer, longer partitions finish sooner.  Up to 1024 tokens, P doubles
@@ -72,8 +84,6 @@ int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
   // in CUDA graphs on 32 heads, contexts U[256, 1024]: batch 8 runs 512
   // (19.0 us per layer against 21.0 at 256), batch 32 runs 1024 (63.7 against
   // 67.5), batch 2 keeps 256 (12.0 against 15.2 at 512).
-  const int64_t slots = 3LL * device_sm_count();
-  const int64_t ctx = max_ctx > 0 ? max_ctx : 1;
   while (P < 1024 &&
          static_cast<int64_t>(num_seqs) * num_kv_heads * ((ctx + 2 * P - 1) / (2 * P)) >= slots)
     P *= 2;

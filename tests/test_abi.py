@@ -288,6 +288,15 @@ def test_auto_partition_floor_grows_with_group(lib):
     assert lib.partition_tokens(64, 64, 8, 8117, 0) >= 2048        # 70B-shaped GQA-8 layer
 
 
+def test_auto_partition_long_contexts_take_longer_partitions(lib):
+    """Past 32 partitions per sequence the partition doubles (up to 4096)
+    while the doubled grid keeps two waves of three CTAs per SM (152 SMs)."""
+    assert lib.partition_tokens(8, 32, 8, 128932, 0) == 4096        # 64 -> 32 partitions
+    assert lib.partition_tokens(1, 32, 8, 128932, 0) == 1024        # too few CTAs to double
+    assert lib.partition_tokens(32, 32, 32, 4085, 0) == 1024        # 4 partitions: unchanged
+    assert lib.partition_tokens(64, 64, 8, 8117, 0) == 2048         # 4 partitions: unchanged
+
+
 def test_auto_partition_small_batches_fill_one_wave(lib):
     """Below 1024 tokens the partition doubles while the grid still fills one
     wave of three CTAs per SM (152 SMs here and without a device)."""
