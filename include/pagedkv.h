@@ -274,9 +274,9 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, const int64_t
 /* ------------------------------------------------------------------------ */
 
 /* Tokens per split-KV partition that paged_attention_decode uses for this
- * problem when its partition_tokens argument is 0 (depends on the current
- * device's SM count and on the group size num_q_heads / num_kv_heads) on f32
- * and bf16 caches; FP8 and INT8 caches, whose rows are half the bytes, take
+ * problem when its partition_tokens argument is 0 (a power of two in [256,
+ * 4096] that depends on the current device's SM count, the group size
+ * num_q_heads / num_kv_heads and the context length) on f32 and bf16 caches; FP8 and INT8 caches, whose rows are half the bytes, take
  * twice this, at most 4096.  A non-zero partition_tokens (a multiple of 64) is
  * returned as is.  Returns 0 on bad arguments (negative sizes, num_q_heads not
  * a multiple of num_kv_heads, partition_tokens not a multiple of 64). */
