@@ -370,12 +370,17 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-// Combine split-KV partials: one CTA per (sequence, query head).
+// Combine split-KV partials: one warp (a CTA of 32 threads) per (sequence,
+// query head).  Lane i reads the (m, l) of partitions i, i + 32, ...; the warp
+// takes their max and weighted sum by shuffles, so a sequence's partials
+// cost one round trip instead of one per partition.  Each lane then merges
+// output dims lane + 32 v over the partitions, eight partitions in flight.
 template <int D>
-__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(32) paged_decode_reduce_kernel(const DecodeParams p) {
   grid_dependency_wait();   // launched with launch_pdl: the partials are written
   allow_dependents();
   const int sh = blockIdx.x;
+  const int lane = threadIdx.x;
   const int s = sh / p.num_q_heads;
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);
@@ -384,39 +389,39 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
   if (nparts <= 1) return;   // written directly by the main kernel
   const float* ml = p.part_ml + static_cast<int64_t>(sh) * p.max_parts * 2;
   const float* po = p.part_o + static_cast<int64_t>(sh) * p.max_parts * D;
-  // Eight partitions per step with their own accumulators, so eight loads are
-  // in flight at once: one at a time, a long context's 60-odd partials cost
-  // as many round trips to L2 in a row.
-  constexpr int U = 8;
   float M = -CUDART_INF_F;
-#pragma unroll U
-  for (int i = 0; i < nparts; ++i) M = fmaxf(M, ml[2 * i]);
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[2 * i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float L = 0.f;
-#pragma unroll U
-  for (int i = 0; i < nparts; ++i) L = fmaf(ml[2 * i + 1], exp2f(ml[2 * i] - M), L);
+  for (int i = lane; i < nparts; i += 32) L = fmaf(ml[2 * i + 1], exp2f(ml[2 * i] - M), L);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float invL = 1.f / L;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc[U];
+  constexpr int V = D / 32;   // output dims per lane
+  constexpr int U = 8;        // partitions per step
+  float acc[V];
 #pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = 0.f;
-    int i = 0;
-    for (; i + U <= nparts; i += U) {
-      float x[U], w[U];
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  for (int i0 = 0; i0 < nparts; i0 += U) {
+    float x[U][V], w[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        x[u] = po[static_cast<int64_t>(i + u) * D + d];
-        w[u] = ml[2 * (i + u)];
-      }
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u;
+      const bool in = i < nparts;   // warp-uniform
+      w[u] = in ? ml[2 * i] : -CUDART_INF_F;
 #pragma unroll
-      for (int u = 0; u < U; ++u) acc[u] = fmaf(x[u], exp2f(w[u] - M), acc[u]);
+      for (int v = 0; v < V; ++v) x[u][v] = in ? po[static_cast<int64_t>(i) * D + lane + 32 * v] : 0.f;
     }
-    for (int u = 0; i < nparts; ++i, ++u)
-      acc[u] = fmaf(po[static_cast<int64_t>(i) * D + d], exp2f(ml[2 * i] - M), acc[u]);
-    float O = 0.f;
 #pragma unroll
-    for (int u = 0; u < U; ++u) O += acc[u];
-    p.out[static_cast<int64_t>(sh) * D + d] = O * invL;
+    for (int u = 0; u < U; ++u) {
+      const float wu = exp2f(w[u] - M);   // 2^-inf = 0 past the last partition
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc[v] = fmaf(x[u][v], wu, acc[v]);
+    }
   }
+#pragma unroll
+  for (int v = 0; v < V; ++v) p.out[static_cast<int64_t>(sh) * D + lane + 32 * v] = acc[v] * invL;
 }
 
 // Host launcher for one instantiation (defined in decode_launch.cuh).

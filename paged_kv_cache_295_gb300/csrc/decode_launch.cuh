@@ -26,7 +26,7 @@ pkv_status launch_decode(const DecodeLaunch& a) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {
-    e = launch_pdl(paged_decode_reduce_kernel<D>, dim3(a.num_seqs * p.num_q_heads), dim3(128), 0,
+    e = launch_pdl(paged_decode_reduce_kernel<D>, dim3(a.num_seqs * p.num_q_heads), dim3(32), 0,
                    a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }

@@ -147,8 +147,8 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
   if (p.max_parts > 1) {
     const dim3 rgrid(a.num_seqs * p.num_q_heads);
     const cudaError_t e =
-        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(128), 0, a.stream, p)
-                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(128), 0, a.stream, p);
+        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(32), 0, a.stream, p)
+                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(32), 0, a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -207,8 +207,8 @@ pkv_status launch_decode_mma(const DecodeLaunch& a, const void* k_cache, const v
   if (p.max_parts > 1) {
     const dim3 rgrid(a.num_seqs * p.num_q_heads);
     const cudaError_t e =
-        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(128), 0, a.stream, p)
-                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(128), 0, a.stream, p);
+        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(32), 0, a.stream, p)
+                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(32), 0, a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
