@@ -52,10 +52,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "7f7d5c328970e0ce", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239752 GB read + 5.019 MB
-               # written, plus the reduce kernel's 1.434 MB read and 2 KB written
-               "bytes_per_launch": 1239752448 + 5019392 + 1433856 + 2048}
+NCU_TRAFFIC = {"sources_sha": "2a5da666e0e3a105", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239783 GB read + 4.969 MB
+               # written, plus the reduce kernel's 1.436 MB read
+               "bytes_per_launch": 1239782656 + 4968704 + 1436416}
 
 
 def parse_args(argv=None):
