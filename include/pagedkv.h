@@ -300,7 +300,9 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   block_tables : device [num_seqs, max_blocks_per_seq] int32, row-major;
  *                  entry j of row s is the physical block of logical block j.
  *                  Entries at or beyond ceil(context_lens[s]/block_size) are
- *                  never read.
+ *                  never used; the kernel may load some of them (always inside
+ *                  the row) before it knows the context length, so the whole
+ *                  row must be readable device memory, whatever it holds.
  *   context_lens : device [num_seqs] int32, tokens to attend (including the
  *                  token appended this step).  0 gives an output of 0.
  *   max_context_len : host upper bound of context_lens (sizes the grid).

@@ -234,6 +234,29 @@ def test_block_permutation_bit_identical(torch_cuda, decode_path):
     assert out2.cpu().numpy().tobytes() == outs[0].tobytes()
 
 
+@pytest.mark.parametrize("partition", [0, 64])
+def test_table_entries_past_the_context_are_never_used(torch_cuda, decode_path, partition):
+    """Entries at or beyond ceil(ctx / bs) may hold anything: out-of-range ids
+    there (the kernels may load them before they know the context) raise no
+    flag and change no output bit."""
+    torch = torch_cuda
+    w, lens = SMALL["llama7b_mha_bf16"]
+    case, _ = GC.make_small(w, lens=lens)
+    eng, outs, st = GC.run_gpu(case, partition=partition)
+    assert st == 0
+    t2 = case.tables.copy()
+    for s, L in enumerate(case.lens):
+        nb = -(-int(L) // w.block_size)
+        t2[s, nb:] = np.where(np.arange(t2.shape[1] - nb) % 2 == 0, case.nb + 12345, -77)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out2 = eng.attend(0, GC.to_torch(case.q[0], w.q_dtype), torch.from_numpy(t2).cuda(),
+                      torch.from_numpy(case.lens.astype(np.int32)).cuda(), int(case.lens.max()),
+                      partition=partition, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert out2.cpu().numpy().tobytes() == outs[0].tobytes()
+
+
 def test_context_one_and_constant_v(torch_cuda, decode_path):
     torch = torch_cuda
     w = W.DecodeWorkload("c1", 4, 8, 2, 128, 16, "bf16", "bf16", seed=13, ctx_law="fixed")
