@@ -339,10 +339,10 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
 
 /* Decode kernel choice, for tests and profiles.  paged_attention_decode and
  * paged_attention_decode_append pick one kernel by shape: the transposed
- * mma.sync kernel for G <= 8 (bf16 head_dim 64 / 128, 8-bit head_dim 128,
- * block_size >= 8), else the heads-as-rows mma.sync kernel (bf16 head_dim
- * 64 / 128, FP8 head_dim 128, G <= 16, block_size >= 8), else the CUDA-core
- * kernel.  pkv_test_force_decode_kernel(k) makes every later call in the
+ * mma.sync kernel for G <= 8 or G = 16 (two CTAs of 8 heads per KV head;
+ * bf16 head_dim 64 / 128, 8-bit head_dim 128, block_size >= 8), else the
+ * heads-as-rows mma.sync kernel (bf16 head_dim 64 / 128, FP8 head_dim 128,
+ * G <= 16, block_size >= 8), else the CUDA-core kernel.  pkv_test_force_decode_kernel(k) makes every later call in the
  * process skip to kernel k where k supports the shape (falling back down the
  * same order where it does not); PKV_DECODE_KERNEL_AUTO restores the choice
  * by shape.  It exists so that tests can run every kernel on the same inputs.
@@ -358,7 +358,7 @@ pkv_status pkv_test_force_decode_kernel(int32_t kernel);
 
 /* Test of the bounded device waits, not a paged-attention operation of the
  * source pages.  pkv_test_decode_stall(bytes) with bytes > 0 makes every
- * later launch of the transposed decode kernel (the one chosen for G <= 8)
+ * later launch of the transposed decode kernel (chosen for G <= 8 and 16)
  * arm one barrier phase - warp 0, first stage, CTA (sequence 0, KV head 0,
  * partition 0) - for `bytes` more than its copies bring, before issuing them.
  * The copies land, the phase never completes, and after the 2 s bound the

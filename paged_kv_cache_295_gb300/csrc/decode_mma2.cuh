@@ -126,7 +126,11 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int KSTEPS = D / 16;   // QK k-steps
   constexpr int MT = D / 16;       // PV m-tiles (16 output dims each)
   const DecodeParams& p = mp.p;
-  const int G = p.num_q_heads / p.num_kv_heads;
+  // Groups of 16 heads run as two CTAs per KV head, each with 8 of the heads
+  // as the MMA's N columns; they read the same K/V rows one after the other
+  // (adjacent in the grid), so the second finds them in L2.
+  const int qs = mp.q_split > 1 ? mp.q_split : 1;
+  const int G = p.num_q_heads / p.num_kv_heads / qs;   // query heads of this CTA
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW][STAGES];
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int P = p.partition_tokens;
-  const int s = blockIdx.z, g = blockIdx.x, part = blockIdx.y;
+  const int s = blockIdx.z, g = blockIdx.x / qs, part = blockIdx.y;
   grid_dependency_wait();   // launched with launch_pdl: earlier work on the stream is done
   allow_dependents();
 
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(NW * 32)
       min(((t_begin + P - 1) >> p.bs_log2) - lb0 + 1, p.max_blocks_per_seq - lb0);
   const int32_t b_pre =
       static_cast<int>(threadIdx.x) < nlb_max ? __ldg(bt_row + lb0 + threadIdx.x) : -1;
-  const int hq0 = g * G;
+  const int hq0 = (g * qs + static_cast<int>(blockIdx.x) % qs) * G;
 
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);
@@ -210,7 +214,9 @@ __global__ void __launch_bounds__(NW * 32)
 
   // Fused append (16-bit caches): the partition's last chunk holds position
   // ctx - 1, the new token; the warp that owns that chunk copies the token's
-  // rows before its first copy, while the other warps start streaming.
+  // rows before its first copy, while the other warps start streaming.  With
+  // two CTAs per KV head both copy the same bytes, so each reads rows it has
+  // written itself.
   const bool fuse_here = !F8 && p.k_new != nullptr && part == nparts - 1 && my_n > 0 &&
                          warp == (nchunks - 1) % NW;
 

@@ -71,7 +71,7 @@ pkv_status launch_mma2_shape(const CUtensorMap& tk, const CUtensorMap& tv, const
   auto kern = paged_decode_mma2_kernel<KV, D, QF32, NW, STAGES, CH>;
   if (!opt_in_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return PKV_ERR_CUDA;
-  dim3 grid(mp.p.num_kv_heads, mp.p.max_parts, num_seqs);
+  dim3 grid(mp.p.num_kv_heads * mp.q_split, mp.p.max_parts, num_seqs);
   if (launch_pdl(kern, grid, dim3(NW * 32), smem, stream, tk, tv, mp) != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
@@ -112,7 +112,7 @@ bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_si
   } else {
     return false;
   }
-  if (group < 1 || group > 8) return false;
+  if (group < 1 || (group > 8 && group != 16)) return false;   // 16: two CTAs of 8 heads
   if (block_size < 8) return false;
   if (num_blocks * block_size > 0x7fffffffLL) return false;
   return encode_fn() != nullptr;
@@ -124,6 +124,7 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
   const int bs = 1 << p.bs_log2;
   const int ch = mma2_chunk(kv_dtype);
   MmaParams mp{p, bs < ch ? bs : ch};
+  mp.q_split = p.num_q_heads / p.num_kv_heads > 8 ? 2 : 1;
   CUtensorMap tk, tv;
   const int64_t rows = num_blocks * bs;
   const bool byte_codes = kv_dtype != PKV_BF16;
