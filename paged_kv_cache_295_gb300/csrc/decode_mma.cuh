@@ -47,8 +47,8 @@ constexpr uint32_t kWaitLimitNs = 2000000000u;   // 2 s bound on any mbarrier wa
 struct MmaParams {
   DecodeParams p;
   int32_t box_rows;      // rows per TMA box: min(block_size, 16)
-  int32_t q_split = 1;   // transposed kernel: CTAs per KV head, each taking
-                         // G / q_split of its query heads (2 for G = 16)
+  int32_t q_split = 1;   // transposed kernel: CTAs per KV head (1, or 2 for
+                         // G = 16), each taking G / q_split of its query heads
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {

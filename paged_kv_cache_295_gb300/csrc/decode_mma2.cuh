@@ -129,8 +129,8 @@ __global__ void __launch_bounds__(NW * 32)
   // Groups of 16 heads run as two CTAs per KV head, each with 8 of the heads
   // as the MMA's N columns; they read the same K/V rows one after the other
   // (adjacent in the grid), so the second finds them in L2.
-  const int qs = mp.q_split > 1 ? mp.q_split : 1;
-  const int G = p.num_q_heads / p.num_kv_heads / qs;   // query heads of this CTA
+  const int qsl = mp.q_split > 1 ? 1 : 0;   // log2 of the CTAs per KV head (1 or 2)
+  const int G = (p.num_q_heads / p.num_kv_heads) >> qsl;   // query heads of this CTA
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW][STAGES];
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int P = p.partition_tokens;
-  const int s = blockIdx.z, g = blockIdx.x / qs, part = blockIdx.y;
+  const int s = blockIdx.z, g = static_cast<int>(blockIdx.x) >> qsl, part = blockIdx.y;
   grid_dependency_wait();   // launched with launch_pdl: earlier work on the stream is done
   allow_dependents();
 
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(NW * 32)
       min(((t_begin + P - 1) >> p.bs_log2) - lb0 + 1, p.max_blocks_per_seq - lb0);
   const int32_t b_pre =
       static_cast<int>(threadIdx.x) < nlb_max ? __ldg(bt_row + lb0 + threadIdx.x) : -1;
-  const int hq0 = (g * qs + static_cast<int>(blockIdx.x) % qs) * G;
+  const int hq0 = static_cast<int>(blockIdx.x) * G;   // (g * CTAs per head + which) * G
 
   int ctx = __ldg(p.context_lens + s);
   const int cap = context_cap(p);
