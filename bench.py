@@ -262,7 +262,7 @@ def decode_kernel_name(w) -> str:
     """The decode kernel the library picks for this workload's shape."""
     if w.group > 16 or w.block_size < 8:
         return "paged_decode_kernel"
-    if (w.group <= 8 or w.group == 16) and ((w.kv_dtype == "bf16" and w.head_dim in (64, 128))
+    if (w.group <= 8 or w.group == 16) and ((w.kv_dtype == "bf16" and w.head_dim in (64, 128, 256))
                          or (w.kv_dtype in ("fp8_e4m3", "int8") and w.head_dim == 128)):
         return "paged_decode_mma2_kernel"
     if w.kv_dtype == "bf16" and w.head_dim in (64, 128):

@@ -340,7 +340,7 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
 /* Decode kernel choice, for tests and profiles.  paged_attention_decode and
  * paged_attention_decode_append pick one kernel by shape: the transposed
  * mma.sync kernel for G <= 8 or G = 16 (two CTAs of 8 heads per KV head;
- * bf16 head_dim 64 / 128, 8-bit head_dim 128, block_size >= 8), else the
+ * bf16 head_dim 64 / 128 / 256, 8-bit head_dim 128, block_size >= 8), else the
  * heads-as-rows mma.sync kernel (bf16 head_dim 64 / 128, FP8 head_dim 128,
  * G <= 16, block_size >= 8), else the CUDA-core kernel.  pkv_test_force_decode_kernel(k) makes every later call in the
  * process skip to kernel k where k supports the shape (falling back down the

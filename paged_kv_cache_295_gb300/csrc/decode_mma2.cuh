@@ -81,10 +81,10 @@ __device__ __forceinline__ void fused_append_row16(const DecodeParams& p, int s,
       if (lane == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
     } else {
       constexpr int SEGS = D * 2 / 16;   // 16-byte segments per row
-      static_assert(2 * SEGS <= 32, "one warp copies the K and V rows");
-      if (lane < 2 * SEGS) {
-        const bool is_v = lane >= SEGS;
-        const int seg = lane % SEGS;
+#pragma unroll
+      for (int i = lane; i < 2 * SEGS; i += 32) {   // one pass for D <= 128, two for 256
+        const bool is_v = i >= SEGS;
+        const int seg = i % SEGS;
         const int64_t row = static_cast<int64_t>(s) * p.num_kv_heads + g;
         const uint4 val =
             __ldg(reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row * SEGS + seg);

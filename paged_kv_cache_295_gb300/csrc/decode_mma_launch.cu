@@ -95,6 +95,8 @@ pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
                        int num_seqs, cudaStream_t stream) {
   if constexpr (D * KV::kBytes == 256)
     return launch_mma2_shape<KV, D, QF32, 4, 2, 16>(tk, tv, mp, num_seqs, stream);
+  else if constexpr (D * KV::kBytes == 512)   // bf16, head_dim 256: 16 KiB stages, 3 CTAs per SM
+    return launch_mma2_shape<KV, D, QF32, 2, 2, 16>(tk, tv, mp, num_seqs, stream);
   else if constexpr (KV::kBytes == 1)
     return launch_mma2_shape<KV, D, QF32, 4, 2, 32>(tk, tv, mp, num_seqs, stream);
   else
@@ -106,7 +108,7 @@ pkv_status launch_mma2(const CUtensorMap& tk, const CUtensorMap& tv, const MmaPa
 bool mma2_path_supported(int32_t kv_dtype, int head_dim, int group, int block_size,
                          int64_t num_blocks) {
   if (kv_dtype == PKV_BF16) {
-    if (head_dim != 64 && head_dim != 128) return false;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
   } else if (kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_INT8) {
     if (head_dim != 128) return false;
   } else {
@@ -138,6 +140,9 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
   else if (kv_dtype == PKV_INT8)
     st = q_f32 ? launch_mma2<INT8, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
                : launch_mma2<INT8, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
+  else if (head_dim == 256)
+    st = q_f32 ? launch_mma2<BF16, 256, true>(tk, tv, mp, a.num_seqs, a.stream)
+               : launch_mma2<BF16, 256, false>(tk, tv, mp, a.num_seqs, a.stream);
   else if (head_dim == 128)
     st = q_f32 ? launch_mma2<BF16, 128, true>(tk, tv, mp, a.num_seqs, a.stream)
                : launch_mma2<BF16, 128, false>(tk, tv, mp, a.num_seqs, a.stream);
@@ -148,8 +153,9 @@ pkv_status launch_decode_mma2(const DecodeLaunch& a, const void* k_cache, const 
   if (p.max_parts > 1) {
     const dim3 rgrid(a.num_seqs * p.num_q_heads);
     const cudaError_t e =
-        head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(32), 0, a.stream, p)
-                        : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(32), 0, a.stream, p);
+        head_dim == 256   ? launch_pdl(paged_decode_reduce_kernel<256>, rgrid, dim3(32), 0, a.stream, p)
+        : head_dim == 128 ? launch_pdl(paged_decode_reduce_kernel<128>, rgrid, dim3(32), 0, a.stream, p)
+                          : launch_pdl(paged_decode_reduce_kernel<64>, rgrid, dim3(32), 0, a.stream, p);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;

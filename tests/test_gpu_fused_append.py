@@ -70,6 +70,12 @@ CASES = {
                                 ctx_law="fixed"), None),
     "int8_g2": (W.DecodeWorkload("fa_int8", 14, 8, 4, 128, 32, "int8", "bf16", seed=35,
                                  ctx_law="fixed"), None),
+    # head_dim 256: the append's K and V rows take two passes of the warp
+    "bf16_d256_g2": (W.DecodeWorkload("fa_d256", 10, 8, 4, 256, 16, "bf16", "bf16", seed=36,
+                                      ctx_law="fixed"), None),
+    # 16 heads per KV head: two CTAs per KV head both copy the new row
+    "bf16_g16": (W.DecodeWorkload("fa_g16", 10, 32, 2, 128, 16, "bf16", "bf16", seed=37,
+                                  ctx_law="fixed"), None),
 }
 
 
