@@ -52,10 +52,10 @@ DEFAULT_WORKLOAD = W.LLAMA7B_LAYER.name
 
 # DRAM bytes (read + write) per launch of the decode kernel from an ncu capture,
 # valid only while the kernel sources hash to `sources_sha`.
-NCU_TRAFFIC = {"sources_sha": "999c343ea5ff2a16", "workload": "llama7b_layer_bf16",
-               # paged_decode_mma2_kernel (append fused in) 1.239755 GB read + 4.425 MB
-               # written, plus the reduce kernel's 1.436 MB read
-               "bytes_per_launch": 1239755264 + 4425216 + 1435904}
+NCU_TRAFFIC = {"sources_sha": "34bc4b5b2c71edc2", "workload": "llama7b_layer_bf16",
+               # paged_decode_mma2_kernel (append fused in) 1.239778 GB read + 4.985 MB
+               # written, plus the reduce kernel's 1.440 MB read
+               "bytes_per_launch": 1239777792 + 4985344 + 1440000}
 
 
 def parse_args(argv=None):
