@@ -41,7 +41,9 @@ def _sample_seqs(w, lens):
 
 
 @pytest.mark.parametrize("name", [w.name for w in W.ALL] + ["llama7b_layer_int8",
-                                                             "llama7b_layer_fp8"])
+                                                             "llama7b_layer_fp8",
+                                                             "gqa16_128q_8kv_bf16",
+                                                             "d256_gqa2_bf16"])
 def test_fullsize_sampled_parity(lib, name):
     import torch
     import bench

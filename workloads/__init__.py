@@ -88,7 +88,15 @@ LLAMA7B_LAYER_FP8 = DecodeWorkload("llama7b_layer_fp8", 32, 32, 32, 128, 16, FP8
 # launch cost matters: timed as a CUDA-graph replay (and eagerly, for contrast).
 LLAMA7B_B8_GRAPH = DecodeWorkload("llama7b_32layer_b8_graph", 8, 32, 32, 128, 16, BF16, BF16,
                                   seed=9, num_layers=32, ctx_lo=256, ctx_hi=1024, graph=True)
-EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8, LLAMA7B_LAYER_FP8, LLAMA7B_B8_GRAPH)
+# The 70B-shaped layer with 16 query heads per KV head (128 over 8, as in 405B-class
+# models): the transposed kernel runs it as two CTAs of 8 heads per KV head.
+GQA16_LAYER = DecodeWorkload("gqa16_128q_8kv_bf16", 64, 128, 8, 128, 128, BF16, BF16,
+                             seed=2, ctx_lo=1024, ctx_hi=8192)
+# The 7B layer's contexts with head_dim 256 and 2 query heads per KV head (16 over 8).
+D256_LAYER = DecodeWorkload("d256_gqa2_bf16", 32, 16, 8, 256, 16, BF16, BF16,
+                            seed=1, ctx_lo=512, ctx_hi=4096)
+EXTRA = (RAGGED_FP8_LAYER, LLAMA7B_LAYER_INT8, LLAMA7B_LAYER_FP8, LLAMA7B_B8_GRAPH, GQA16_LAYER,
+         D256_LAYER)
 
 
 @dataclass(frozen=True)
